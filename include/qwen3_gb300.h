@@ -1,0 +1,171 @@
+/*
+ * qwen3_gb300.h -- C ABI of a single-GPU (sm_103a) Qwen3-0.6B-style decoder forward.
+ *
+ * The forward computed here is the one hand-written in PyTorch by the pages
+ *   "手写Qwen3-0.6B推理"                 (Qwen3Model, Qwen3DecoderLayer, Qwen3RMSNorm,
+ *                                         Attention, Rope, MLP, 推理),
+ *   "第 3 章 前向与生成（代码走读）"      (3.1 packed [N,C] tokens, 3.2 fused residual +
+ *                                         RMSNorm, 3.3 QKV/RoPE/causal attention, 3.4 gated
+ *                                         MLP, 4.1 last-position lm_head, 4.3 greedy sampler),
+ *   "从零开始写Qwen3"                     (Attn: the decode-time causal alignment; rope),
+ *   "古法手撕简易LLM推理器"               (核心计算函数与Transformer层: the KV cache;
+ *                                         prefill与predict: prefill then one-token steps):
+ *
+ *   h_0 = E[id]                                     (no scaling)
+ *   per layer:  u = RMSNorm(h; g_in)
+ *               q,k,v = u Wq^T, u Wk^T, u Wv^T      (no bias)
+ *               q,k  <- per-head RMSNorm (g_q, g_k), then rotate-half RoPE at the
+ *                       absolute position p (pair (i, i+64), angle p * theta^(-2i/128))
+ *               cache <- (k, v) at p;  o_h = softmax(q_h K_g^T / sqrt(128)) V_g over keys
+ *                       0..p of the same sequence, g = h / (Hq/Hkv)
+ *               h <- h + o Wo^T;  h <- h + Wdown(silu(Wgate m) * Wup m), m = RMSNorm(h; g_post)
+ *   next token = argmax_v E_v . RMSNorm(h_L; g_final)   (tied head, lowest index on ties)
+ *
+ * Conventions common to every call
+ *  - All pointers named *_dev are device pointers on the current CUDA device; *_host are
+ *    host pointers.  The library never allocates device memory: the caller passes one
+ *    arena (qwen3_arena_bytes) that holds packed weights, the RoPE table, the KV cache
+ *    and all scratch, and must keep it alive until qwen3_free.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Calls that take a stream are asynchronous and stream-ordered; outputs are valid once
+ *    the stream has been synchronised.  Calls on one context must not overlap.
+ *  - Every call returns QWEN3_OK (0) or a negative QWEN3_E_* code; the message of the last
+ *    failure is returned by qwen3_last_error.  No call aborts, throws or traps.
+ *  - Token ids outside [0, vocab) are clamped on the device and flagged in the device
+ *    error word, which qwen3_get_status reports.
+ */
+#ifndef QWEN3_GB300_H
+#define QWEN3_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QWEN3_OK 0
+#define QWEN3_E_INVALID (-1)     /* NULL pointer, bad size, bad order, bad slot */
+#define QWEN3_E_CAPACITY (-2)    /* more tokens / sequences / context than the arena was sized for */
+#define QWEN3_E_UNSUPPORTED (-3) /* shape or device this build does not implement */
+#define QWEN3_E_CUDA (-4)        /* a CUDA runtime call failed */
+#define QWEN3_E_DEVICE (-5)      /* the device error word was set (e.g. a token id out of range) */
+
+/* qwen3_config.flags */
+#define QWEN3_FLAG_NO_GRAPH 1u   /* launch decode steps one kernel at a time instead of a CUDA graph */
+
+/* Model and capacity.  Supported: head_dim == 128; n_q_heads a multiple of n_kv_heads with
+ * n_q_heads / n_kv_heads <= 8; hidden, n_q_heads*head_dim and intermediate multiples of 256;
+ * vocab >= 1.  Qwen3-0.6B: 28, 1024, 16, 8, 128, 3072, 151936, 1e-6, 1e6 ("古法手撕简易LLM推理器",
+ * 处理参数和超参数). */
+typedef struct qwen3_config {
+    int32_t n_layers;
+    int32_t hidden;        /* C */
+    int32_t n_q_heads;     /* Hq */
+    int32_t n_kv_heads;    /* Hkv */
+    int32_t head_dim;      /* D */
+    int32_t intermediate;  /* I */
+    int32_t vocab;         /* V */
+    float rms_eps;
+    double rope_theta;
+    int32_t max_seqs;            /* KV-cache slots; also the largest decode batch */
+    int32_t max_ctx;             /* tokens per slot (prompt + generated) */
+    int32_t max_prefill_tokens;  /* largest N of one qwen3_prefill call */
+    uint32_t flags;              /* QWEN3_FLAG_* */
+} qwen3_config;
+
+/* Weights: device pointers to bf16 tensors in the checkpoint's layout ([out, in] row-major
+ * for matrices; "手写Qwen3-0.6B推理", 打印模型结构).  Per-layer members are HOST arrays of
+ * n_layers device pointers.  Read only during qwen3_create (packed into the arena). */
+typedef struct qwen3_weights {
+    const void *embed;       /* [V, C]; also the lm_head (tied) */
+    const void *final_norm;  /* [C] */
+    const void *const *in_norm;    /* [C] per layer */
+    const void *const *post_norm;  /* [C] */
+    const void *const *q_norm;     /* [D] */
+    const void *const *k_norm;     /* [D] */
+    const void *const *wq;         /* [Hq*D, C] */
+    const void *const *wk;         /* [Hkv*D, C] */
+    const void *const *wv;         /* [Hkv*D, C] */
+    const void *const *wo;         /* [C, Hq*D] */
+    const void *const *wgate;      /* [I, C] */
+    const void *const *wup;        /* [I, C] */
+    const void *const *wdown;      /* [C, I] */
+} qwen3_weights;
+
+typedef struct qwen3_ctx qwen3_ctx; /* opaque, owned by the library (host memory) */
+
+/* Bytes of device memory qwen3_create needs for this configuration (0 if the configuration
+ * is invalid or unsupported).  Pure host arithmetic. */
+size_t qwen3_arena_bytes(const qwen3_config *cfg);
+
+/* Builds a context: validates cfg, packs the weights into `arena_dev` (256-byte aligned,
+ * at least qwen3_arena_bytes(cfg) bytes), builds the RoPE table (angles in double
+ * precision) and empties every KV slot.  Synchronises `stream` before returning, so the
+ * weight buffers may be freed afterwards.  On success *out owns a context to be released
+ * with qwen3_free.  Errors: E_INVALID (NULL argument, small arena), E_UNSUPPORTED (shape or
+ * a device other than compute capability 10.3), E_CUDA. */
+int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_dev,
+                 size_t arena_bytes, void *stream, qwen3_ctx **out);
+
+/* Prefill ("第 3 章", 3.1 packed tokens; "古法手撕简易LLM推理器", prefill与predict):
+ * B sequences packed in tokens_dev[N] (int32), sequence b being rows
+ * cu_seqlens[b] .. cu_seqlens[b+1]-1 at positions 0 .. len_b-1.  Sequence b (re)starts KV
+ * slot slots[b] and leaves it holding len_b tokens.  Writes next_tok_dev[b] (int32), the
+ * greedy token after each sequence's last row ("第 3 章", 4.1), and, if logits_dev is not
+ * NULL, the fp32 logits of those rows to logits_dev[B, V].  cu_seqlens and slots are given
+ * twice, on the device and on the host (same values).  Errors: E_INVALID (NULL, B < 1,
+ * cu_seqlens not starting at 0 or not increasing, repeated or out-of-range slot),
+ * E_CAPACITY (B > max_seqs, N > max_prefill_tokens, len_b > max_ctx), E_CUDA. */
+int qwen3_prefill(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *cu_seqlens_dev,
+                  const int32_t *cu_seqlens_host, const int32_t *slots_dev,
+                  const int32_t *slots_host, int32_t B, float *logits_dev,
+                  int32_t *next_tok_dev, void *stream);
+
+/* One decode step ("古法手撕简易LLM推理器", predict): token tokens_dev[b] is appended to slot
+ * slots[b] at position = the slot's current length, attends to keys 0..position, and
+ * next_tok_dev[b] receives the greedy next token (logits_dev[B, V] too if not NULL).  Each
+ * slot's length grows by one.  next_tok_dev may be passed as the next step's tokens_dev.
+ * Unless QWEN3_FLAG_NO_GRAPH is set, the step is recorded once per (B, pointers, split
+ * plan) as a CUDA graph and replayed.  Errors: E_INVALID (NULL, B < 1, repeated slot, slot
+ * never prefilled), E_CAPACITY (B > max_seqs, a slot already holding max_ctx tokens),
+ * E_CUDA. */
+int qwen3_decode_step(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *slots_dev,
+                      const int32_t *slots_host, int32_t B, float *logits_dev,
+                      int32_t *next_tok_dev, void *stream);
+
+/* Debug dump of the residual stream: while hidden_dev is not NULL, every prefill and decode
+ * call writes h_0 (the embedding rows) and h_l after each layer l, fp32, to
+ * hidden_dev[(L+1), rows, C] where rows = N (prefill) or B (decode).  Needs
+ * bytes >= (L+1)*rows*C*4 for the calls made, else those calls fail with E_CAPACITY.
+ * Decode steps run without a graph while the dump is on.  NULL turns it off. */
+int qwen3_set_debug_dump(qwen3_ctx *ctx, float *hidden_dev, size_t bytes);
+
+/* Synchronises the device, then returns QWEN3_OK, E_CUDA (a pending CUDA error) or E_DEVICE
+ * (the device error word was set; the word is cleared). */
+int qwen3_get_status(qwen3_ctx *ctx);
+
+/* Message of the last failed call on ctx (or of the last failed qwen3_create when ctx is NULL). */
+const char *qwen3_last_error(const qwen3_ctx *ctx);
+
+/* Host-side length of KV slot `slot` (tokens cached), or -1 for a bad slot. */
+int32_t qwen3_slot_length(const qwen3_ctx *ctx, int32_t slot);
+
+/* Device pointers to layer `layer`, slot `slot` of the KV cache: K and V are each
+ * bf16 [Hkv][max_ctx][D] (rows 0..length-1 valid; K after q/k-norm and RoPE, V raw).
+ * Read-only for the caller.  Errors: E_INVALID. */
+int qwen3_kv_view(const qwen3_ctx *ctx, int32_t layer, int32_t slot, const void **k_dev,
+                  const void **v_dev);
+
+/* Number of kernels this context has launched so far (graph replays count every kernel
+ * node of the graph). */
+int64_t qwen3_launch_count(const qwen3_ctx *ctx);
+
+/* Releases the context and its graphs.  Does not free the arena or any caller memory. */
+void qwen3_free(qwen3_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QWEN3_GB300_H */

@@ -1,0 +1,254 @@
+"""ctypes binding of libqwen3_gb300.so: the C ABI's calls under the same names.
+
+The functions here only marshal arguments (device pointers as integers, host arrays as
+ctypes arrays) and turn a negative return code into ``Qwen3Error``.  Every step of the
+forward runs in the library's CUDA kernels; there is no fallback path.  ``Model`` is a
+convenience owner of the device memory (allocated with PyTorch) around one context.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libqwen3_gb300.so")
+
+QWEN3_OK = 0
+QWEN3_E_INVALID = -1
+QWEN3_E_CAPACITY = -2
+QWEN3_E_UNSUPPORTED = -3
+QWEN3_E_CUDA = -4
+QWEN3_E_DEVICE = -5
+QWEN3_FLAG_NO_GRAPH = 1
+
+_P = ctypes.c_void_p
+
+
+class qwen3_config(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("intermediate", ctypes.c_int32), ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float),
+        ("rope_theta", ctypes.c_double), ("max_seqs", ctypes.c_int32), ("max_ctx", ctypes.c_int32),
+        ("max_prefill_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32),
+    ]
+
+
+class qwen3_weights(ctypes.Structure):
+    _fields_ = [("embed", _P), ("final_norm", _P)] + [
+        (k, ctypes.POINTER(_P)) for k in
+        ("in_norm", "post_norm", "q_norm", "k_norm", "wq", "wk", "wv", "wo", "wgate", "wup", "wdown")
+    ]
+
+
+class Qwen3Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"qwen3 error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads the CUDA library (raises if it has not been built: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} is missing: build it with qwen3_decoder_forward_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    i32, i64, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    pi32 = ctypes.POINTER(i32)
+    sig = {
+        "qwen3_arena_bytes": (sz, [ctypes.POINTER(qwen3_config)]),
+        "qwen3_create": (ctypes.c_int, [ctypes.POINTER(qwen3_config), ctypes.POINTER(qwen3_weights), _P, sz, _P,
+                                        ctypes.POINTER(_P)]),
+        "qwen3_prefill": (ctypes.c_int, [_P, _P, _P, pi32, _P, pi32, i32, _P, _P, _P]),
+        "qwen3_decode_step": (ctypes.c_int, [_P, _P, _P, pi32, i32, _P, _P, _P]),
+        "qwen3_set_debug_dump": (ctypes.c_int, [_P, _P, sz]),
+        "qwen3_get_status": (ctypes.c_int, [_P]),
+        "qwen3_last_error": (ctypes.c_char_p, [_P]),
+        "qwen3_slot_length": (i32, [_P, i32]),
+        "qwen3_kv_view": (ctypes.c_int, [_P, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
+        "qwen3_launch_count": (i64, [_P]),
+        "qwen3_free": (None, [_P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, ctx) -> None:
+    if rc != QWEN3_OK:
+        msg = load_library().qwen3_last_error(ctx)
+        raise Qwen3Error(rc, msg.decode() if msg else "")
+
+
+def _i32_array(values: Sequence[int]):
+    return (ctypes.c_int32 * len(values))(*[int(v) for v in values])
+
+
+def make_config(shape, max_seqs: int, max_ctx: int, max_prefill_tokens: int, flags: int = 0) -> qwen3_config:
+    return qwen3_config(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
+                        shape.intermediate, shape.vocab, shape.rms_eps, shape.rope_theta, max_seqs, max_ctx,
+                        max_prefill_tokens, flags)
+
+
+# --- the C ABI, one wrapper per call ------------------------------------------------------
+
+def qwen3_arena_bytes(cfg: qwen3_config) -> int:
+    return int(load_library().qwen3_arena_bytes(ctypes.byref(cfg)))
+
+
+def qwen3_create(cfg: qwen3_config, weights: qwen3_weights, arena_ptr: int, arena_bytes: int,
+                 stream: int = 0):
+    ctx = _P()
+    rc = load_library().qwen3_create(ctypes.byref(cfg), ctypes.byref(weights), arena_ptr, arena_bytes,
+                                     stream, ctypes.byref(ctx))
+    _check(rc, None)
+    return ctx
+
+
+def qwen3_prefill(ctx, tokens_ptr: int, cu_dev_ptr: int, cu_host: Sequence[int], slots_dev_ptr: int,
+                  slots_host: Sequence[int], B: int, logits_ptr: Optional[int], next_ptr: int, stream: int = 0):
+    _check(load_library().qwen3_prefill(ctx, tokens_ptr, cu_dev_ptr, _i32_array(cu_host), slots_dev_ptr,
+                                        _i32_array(slots_host), B, logits_ptr, next_ptr, stream), ctx)
+
+
+def qwen3_decode_step(ctx, tokens_ptr: int, slots_dev_ptr: int, slots_host: Sequence[int], B: int,
+                      logits_ptr: Optional[int], next_ptr: int, stream: int = 0):
+    _check(load_library().qwen3_decode_step(ctx, tokens_ptr, slots_dev_ptr, _i32_array(slots_host), B,
+                                            logits_ptr, next_ptr, stream), ctx)
+
+
+def qwen3_set_debug_dump(ctx, hidden_ptr: Optional[int], nbytes: int):
+    _check(load_library().qwen3_set_debug_dump(ctx, hidden_ptr, nbytes), ctx)
+
+
+def qwen3_get_status(ctx) -> int:
+    return int(load_library().qwen3_get_status(ctx))
+
+
+def qwen3_last_error(ctx) -> str:
+    m = load_library().qwen3_last_error(ctx)
+    return m.decode() if m else ""
+
+
+def qwen3_slot_length(ctx, slot: int) -> int:
+    return int(load_library().qwen3_slot_length(ctx, slot))
+
+
+def qwen3_kv_view(ctx, layer: int, slot: int):
+    k, v = _P(), _P()
+    _check(load_library().qwen3_kv_view(ctx, layer, slot, ctypes.byref(k), ctypes.byref(v)), ctx)
+    return int(k.value), int(v.value)
+
+
+def qwen3_launch_count(ctx) -> int:
+    return int(load_library().qwen3_launch_count(ctx))
+
+
+def qwen3_free(ctx) -> None:
+    load_library().qwen3_free(ctx)
+
+
+# --- device-memory owner -------------------------------------------------------------------
+
+class Model:
+    """One context plus the device memory it runs in (PyTorch tensors on ``device``).
+
+    ``weights`` is the dict of bf16 tensors from ``synth.make_weights`` (any device).  The
+    weights are copied to the GPU, packed by qwen3_create into the arena, then released.
+    """
+
+    def __init__(self, shape, weights: Dict, max_seqs: int, max_ctx: int, max_prefill_tokens: int,
+                 flags: int = 0, device: str = "cuda"):
+        import torch
+
+        self.torch = torch
+        self.shape = shape
+        self.device = torch.device(device)
+        self.cfg = make_config(shape, max_seqs, max_ctx, max_prefill_tokens, flags)
+        nbytes = qwen3_arena_bytes(self.cfg)
+        if nbytes == 0:
+            raise Qwen3Error(QWEN3_E_UNSUPPORTED, "configuration not supported")
+        self.arena = torch.empty(nbytes + 256, dtype=torch.uint8, device=self.device)
+        base = self.arena.data_ptr()
+        self.arena_ptr = (base + 255) // 256 * 256
+        self.arena_bytes = nbytes
+        dev_w = {"embed": weights["embed"].to(self.device).contiguous(),
+                 "final_norm": weights["final_norm"].to(self.device).contiguous(),
+                 "layers": [{k: v.to(self.device).contiguous() for k, v in d.items()} for d in weights["layers"]]}
+        arrays = {}
+        for key in ("in_norm", "post_norm", "q_norm", "k_norm", "wq", "wk", "wv", "wo", "wgate", "wup", "wdown"):
+            arrays[key] = (_P * shape.n_layers)(*[d[key].data_ptr() for d in dev_w["layers"]])
+        w = qwen3_weights(dev_w["embed"].data_ptr(), dev_w["final_norm"].data_ptr(),
+                          *[ctypes.cast(arrays[k], ctypes.POINTER(_P)) for k in
+                            ("in_norm", "post_norm", "q_norm", "k_norm", "wq", "wk", "wv", "wo",
+                             "wgate", "wup", "wdown")])
+        stream = torch.cuda.current_stream(self.device).cuda_stream
+        self.ctx = qwen3_create(self.cfg, w, self.arena_ptr, self.arena_bytes, stream)
+        del dev_w, arrays
+
+    def close(self):
+        if getattr(self, "ctx", None) is not None:
+            qwen3_free(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _stream(self):
+        return self.torch.cuda.current_stream(self.device).cuda_stream
+
+    def prefill(self, tokens, lengths: Sequence[int], slots: Sequence[int], want_logits: bool = False,
+                next_out=None):
+        """tokens: int32 CUDA tensor [N]; returns (next_tok int32 [B], logits fp32 [B, V] or None)."""
+        torch = self.torch
+        B = len(lengths)
+        cu = [0]
+        for n in lengths:
+            cu.append(cu[-1] + int(n))
+        cu_d = torch.tensor(cu, dtype=torch.int32, device=self.device)
+        slots_d = torch.tensor(list(slots), dtype=torch.int32, device=self.device)
+        nxt = next_out if next_out is not None else torch.empty(B, dtype=torch.int32, device=self.device)
+        logits = torch.empty(B, self.shape.vocab, dtype=torch.float32, device=self.device) if want_logits else None
+        qwen3_prefill(self.ctx, tokens.data_ptr(), cu_d.data_ptr(), cu, slots_d.data_ptr(), list(slots), B,
+                      logits.data_ptr() if logits is not None else None, nxt.data_ptr(), self._stream())
+        self._keep = (cu_d, slots_d)
+        return nxt, logits
+
+    def decode_step(self, tokens, slots_dev, slots: Sequence[int], next_out, logits_out=None):
+        """tokens: int32 CUDA tensor [B]; writes next_out [B] (and logits_out [B, V] if given)."""
+        qwen3_decode_step(self.ctx, tokens.data_ptr(), slots_dev.data_ptr(), list(slots), len(slots),
+                          logits_out.data_ptr() if logits_out is not None else None, next_out.data_ptr(),
+                          self._stream())
+
+    def set_debug_dump(self, buf):
+        qwen3_set_debug_dump(self.ctx, buf.data_ptr() if buf is not None else None,
+                             buf.numel() * 4 if buf is not None else 0)
+
+    def status(self) -> int:
+        return qwen3_get_status(self.ctx)
+
+    def kv_rows(self, layer: int, slot: int, n: int):
+        """Copies K and V rows 0..n-1 of (layer, slot) to new tensors [n, Hkv, D] (bf16, device)."""
+        torch = self.torch
+        s = self.shape
+        per = s.n_kv_heads * self.cfg.max_ctx * s.head_dim
+        whole = self.arena.view(torch.bfloat16)
+        out = []
+        for p in qwen3_kv_view(self.ctx, layer, slot):
+            off = (p - self.arena.data_ptr()) // 2
+            t = whole[off: off + per].view(s.n_kv_heads, self.cfg.max_ctx, s.head_dim)
+            out.append(t[:, :n].permute(1, 0, 2).contiguous())
+        return out[0], out[1]

@@ -1,0 +1,101 @@
+// Host-side launchers of the Qwen3 decoder-forward kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "common.cuh"
+
+namespace q3 {
+
+struct Launch {
+    cudaStream_t stream = nullptr;
+    bool pdl = true;          // programmatic dependent launch on every kernel
+    int num_sms = 148;
+    int64_t *counter = nullptr;
+};
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch(const Launch &lc, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = lc.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = lc.pdl ? 1 : 0;
+    if (lc.counter) ++*lc.counter;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Row bookkeeping of one call: row r of the packed batch belongs to KV slot row_slot[r]
+// at absolute position row_pos[r].
+struct Rows {
+    const int32_t *cu_seqlens;  // [B+1] for prefill, nullptr for decode (one row per sequence)
+    const int32_t *slots;       // [B]
+    int32_t *row_slot;          // [rows] written by the embedding kernel
+    int32_t *row_pos;           // [rows]
+    int32_t *ctx_len;           // [max_seqs] tokens cached per slot
+    int32_t B;
+    int32_t rows;
+};
+
+// --- norm.cu ---------------------------------------------------------------------------
+cudaError_t launch_embed_rmsnorm(const Launch &lc, const int32_t *tokens, const Rows &r,
+                                 const bf16 *embed, const float *gamma, float *resid, bf16 *xn,
+                                 int C, int V, float eps, uint32_t *err);
+cudaError_t launch_rmsnorm(const Launch &lc, const float *resid, int rows, const float *gamma,
+                           bf16 *xn, int C, float eps);
+// Final norm of each sequence's last row: row cu_seqlens[b+1]-1 (or b) -> out[b].
+cudaError_t launch_final_norm(const Launch &lc, const float *resid, const int32_t *cu_seqlens,
+                              int B, const float *gamma, bf16 *out, int C, float eps);
+cudaError_t launch_bf16_to_f32(const Launch &lc, const bf16 *src, float *dst, int n);
+
+// --- gemm.cu (prefill; out[M,N] = A[M,K] W[N,K]^T) -----------------------------------------
+enum Epilogue : int {
+    EPI_F32 = 0,         // out fp32 [M, N]
+    EPI_RESID_ADD = 1,   // out fp32 [M, N] += result
+    EPI_SWIGLU = 2,      // W rows interleaved (gate_j, up_j): out bf16 [M, N/2] = silu(g)*u
+};
+cudaError_t launch_gemm(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N,
+                        int epi, void *out);
+
+// --- gemv.cu (decode; same contract as launch_gemm for small M) ---------------------------
+cudaError_t launch_gemv(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N,
+                        int epi, void *out);
+
+// --- rope_kv.cu --------------------------------------------------------------------------
+// qkv fp32 [rows, (Hq+2Hkv)*D] -> q bf16 [rows, Hq, D] (normed + rotated), K (normed +
+// rotated) and V into the layer's cache [slot][Hkv][max_ctx][D].
+cudaError_t launch_qknorm_rope_kv(const Launch &lc, const float *qkv, const Rows &r,
+                                  const float *q_gain, const float *k_gain, const float2 *rope,
+                                  bf16 *q_out, bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv,
+                                  int max_ctx, float eps, uint32_t *err);
+
+// --- attn_prefill.cu ---------------------------------------------------------------------
+cudaError_t launch_attn_prefill(const Launch &lc, const bf16 *q, const bf16 *k_layer,
+                                const bf16 *v_layer, const int32_t *cu_seqlens,
+                                const int32_t *slots, int B, int max_len, bf16 *out, int Hq,
+                                int Hkv, int max_ctx);
+
+// --- attn_decode.cu ----------------------------------------------------------------------
+cudaError_t launch_attn_decode(const Launch &lc, const bf16 *q, const bf16 *k_layer,
+                               const bf16 *v_layer, const Rows &r, int n_split,
+                               int keys_per_split, float *ws_ml, float *ws_o, bf16 *out, int Hq,
+                               int Hkv, int max_ctx);
+
+// --- lmhead.cu ---------------------------------------------------------------------------
+// next_tok[b] = argmax_v X[b] . E[v] (lowest index on ties); logits[B, V] if not null.
+// Also sets ctx_len[slot] = position + 1 of each sequence's last row.
+cudaError_t launch_lmhead_argmax(const Launch &lc, const bf16 *X, int B, int C, const bf16 *E,
+                                 int V, float *logits, float *part_val, int32_t *part_idx,
+                                 int n_parts, int32_t *next_tok, const Rows &r);
+int lmhead_parts(int num_sms);
+
+}  // namespace q3

@@ -1,0 +1,512 @@
+// C ABI of the Qwen3 decoder forward: arena layout, weight packing, argument checks and the
+// per-call kernel chains (prefill over a packed ragged batch; one decode step, recorded as a
+// CUDA graph and replayed).  See include/qwen3_gb300.h for the contract of every call.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "qwen3_gb300.h"
+
+using namespace q3;
+
+namespace {
+
+constexpr size_t ALIGN = 1024;
+constexpr int MAX_SPLIT = 64;   // decode attention: key ranges per (sequence, head)
+constexpr int MAX_PARTS = 1024; // lm_head partial results per row
+
+size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+
+struct Layout {
+    // per-layer strides (bytes) and offsets within layer 0
+    size_t layer_bytes = 0, o_wqkv = 0, o_wo = 0, o_wgu = 0, o_wdown = 0, o_gin = 0, o_gpost = 0,
+           o_gq = 0, o_gk = 0;
+    size_t o_layers = 0, o_embed = 0, o_gfinal = 0, o_rope = 0, o_kcache = 0, o_vcache = 0,
+           kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0;
+    size_t o_resid = 0, o_xn = 0, o_qkv = 0, o_q = 0, o_attn = 0, o_act = 0, o_rowslot = 0,
+           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0;
+    size_t total = 0;
+};
+
+bool config_supported(const qwen3_config &c, std::string *why) {
+    auto fail = [&](const char *m) {
+        if (why) *why = m;
+        return false;
+    };
+    if (c.n_layers < 1 || c.hidden < 1 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.vocab < 1 ||
+        c.intermediate < 1 || c.max_seqs < 1 || c.max_ctx < 1 || c.max_prefill_tokens < 1)
+        return fail("config: every size must be >= 1");
+    if (!(c.rms_eps >= 0.0f) || !(c.rope_theta > 0.0)) return fail("config: bad rms_eps or rope_theta");
+    if (c.head_dim != 128) return fail("config: head_dim must be 128");
+    if (c.n_q_heads % c.n_kv_heads != 0) return fail("config: n_q_heads must be a multiple of n_kv_heads");
+    const int g = c.n_q_heads / c.n_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return fail("config: n_q_heads/n_kv_heads must be 1, 2, 4 or 8");
+    const int qd = c.n_q_heads * c.head_dim;
+    if (c.hidden % 256 || c.hidden > 3072) return fail("config: hidden must be a multiple of 256, at most 3072");
+    if (qd % 256 || qd > 4096) return fail("config: n_q_heads*head_dim must be a multiple of 256, at most 4096");
+    if (c.intermediate % 256 || c.intermediate > 4096) return fail("config: intermediate must be a multiple of 256, at most 4096");
+    if (c.hidden % 128 || qd % 128 || ((c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim) % 128 ||
+        (2 * c.intermediate) % 128)
+        return fail("config: projection widths must be multiples of 128");
+    if (c.max_seqs > 1024) return fail("config: max_seqs must be at most 1024");
+    return true;
+}
+
+Layout make_layout(const qwen3_config &c) {
+    Layout L;
+    const size_t C = c.hidden, D = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads, I = c.intermediate;
+    const size_t qkv_n = (Hq + 2 * Hkv) * D;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes);
+        return at;
+    };
+    // one layer's block
+    L.o_wqkv = take(qkv_n * C * 2);
+    L.o_wo = take(C * Hq * D * 2);
+    L.o_wgu = take(2 * I * C * 2);
+    L.o_wdown = take(C * I * 2);
+    L.o_gin = take(C * 4);
+    L.o_gpost = take(C * 4);
+    L.o_gq = take(D * 4);
+    L.o_gk = take(D * 4);
+    L.layer_bytes = off;
+    off = 0;
+    L.o_layers = take(L.layer_bytes * c.n_layers);
+    L.o_embed = take((size_t)c.vocab * C * 2);
+    L.o_gfinal = take(C * 4);
+    L.o_rope = take((size_t)c.max_ctx * (D / 2) * 8);
+    L.kv_layer_bytes = (size_t)c.max_seqs * Hkv * c.max_ctx * D * 2;
+    L.o_kcache = take(L.kv_layer_bytes * c.n_layers);
+    L.o_vcache = take(L.kv_layer_bytes * c.n_layers);
+    L.o_ctxlen = take((size_t)c.max_seqs * 4);
+    L.o_err = take(16);
+    const size_t R = std::max(c.max_prefill_tokens, c.max_seqs);
+    L.o_resid = take(R * C * 4);
+    L.o_xn = take(R * C * 2);
+    L.o_qkv = take(R * qkv_n * 4);
+    L.o_q = take(R * Hq * D * 2);
+    L.o_attn = take(R * Hq * D * 2);
+    L.o_act = take(R * I * 2);
+    L.o_rowslot = take(R * 4);
+    L.o_rowpos = take(R * 4);
+    L.o_last = take((size_t)c.max_seqs * C * 2);
+    L.o_pval = take((size_t)c.max_seqs * MAX_PARTS * 4);
+    L.o_pidx = take((size_t)c.max_seqs * MAX_PARTS * 4);
+    L.o_wsml = take((size_t)c.max_seqs * Hq * MAX_SPLIT * 2 * 4);
+    L.o_wso = take((size_t)c.max_seqs * Hq * MAX_SPLIT * D * 4);
+    L.total = off;
+    return L;
+}
+
+thread_local std::string g_create_error;
+
+}  // namespace
+
+struct GraphEntry {
+    int B, n_split, kps;
+    const void *tokens, *slots;
+    void *logits, *next;
+    cudaGraphExec_t exec;
+    int64_t kernels;
+};
+
+struct qwen3_ctx {
+    qwen3_config cfg;
+    Layout lay;
+    uint8_t *arena = nullptr;
+    std::vector<int32_t> len_host;
+    int num_sms = 0, n_parts = 0;
+    float *dump = nullptr;
+    size_t dump_bytes = 0;
+    cudaStream_t cap_stream = nullptr;
+    std::vector<GraphEntry> graphs;
+    int64_t launches = 0;
+    std::string err;
+
+    template <typename T>
+    T *at(size_t off) const { return reinterpret_cast<T *>(arena + off); }
+    uint8_t *layer(int l) const { return arena + lay.o_layers + (size_t)l * lay.layer_bytes; }
+    bf16 *kcache(int l) const { return at<bf16>(lay.o_kcache + (size_t)l * lay.kv_layer_bytes); }
+    bf16 *vcache(int l) const { return at<bf16>(lay.o_vcache + (size_t)l * lay.kv_layer_bytes); }
+    int fail(int code, const std::string &m) {
+        err = m;
+        return code;
+    }
+    int cuda_fail(cudaError_t e, const char *where) {
+        err = std::string(where) + ": " + cudaGetErrorString(e);
+        return QWEN3_E_CUDA;
+    }
+};
+
+namespace {
+
+#define Q3_TRY(x)                               \
+    do {                                        \
+        cudaError_t e_ = (x);                   \
+        if (e_ != cudaSuccess) return e_;       \
+    } while (0)
+
+// Everything one call runs, in stream order.  `decode` selects the GEMV projections and the
+// split-KV attention; prefill uses the tiled GEMM and the flash prefill attention.
+cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, const Rows &rows,
+                        bool decode, int max_len, int n_split, int kps, float *logits,
+                        int32_t *next) {
+    const qwen3_config &k = c->cfg;
+    const Layout &L = c->lay;
+    const int C = k.hidden, D = k.head_dim, Hq = k.n_q_heads, Hkv = k.n_kv_heads, I = k.intermediate;
+    const int qkv_n = (Hq + 2 * Hkv) * D, R = rows.rows;
+    float *resid = c->at<float>(L.o_resid);
+    bf16 *xn = c->at<bf16>(L.o_xn);
+    float *qkv = c->at<float>(L.o_qkv);
+    bf16 *q = c->at<bf16>(L.o_q), *attn = c->at<bf16>(L.o_attn), *act = c->at<bf16>(L.o_act);
+    uint32_t *err = c->at<uint32_t>(L.o_err);
+    const bf16 *embed = c->at<bf16>(L.o_embed);
+    const float2 *rope = c->at<float2>(L.o_rope);
+    auto proj = [&](const bf16 *X, int Kd, const uint8_t *W, int N, int epi, void *out) {
+        return decode ? launch_gemv(lc, X, R, Kd, (const bf16 *)W, N, epi, out)
+                      : launch_gemm(lc, X, R, Kd, (const bf16 *)W, N, epi, out);
+    };
+    auto dump = [&](int l) -> cudaError_t {
+        if (!c->dump) return cudaSuccess;
+        return cudaMemcpyAsync(c->dump + (size_t)l * R * C, resid, (size_t)R * C * 4,
+                               cudaMemcpyDeviceToDevice, lc.stream);
+    };
+
+    Q3_TRY(launch_embed_rmsnorm(lc, tokens, rows, embed, (const float *)(c->layer(0) + L.o_gin),
+                                resid, xn, C, k.vocab, k.rms_eps, err));
+    Q3_TRY(dump(0));
+    for (int l = 0; l < k.n_layers; ++l) {
+        const uint8_t *lw = c->layer(l);
+        if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, (const float *)(lw + L.o_gin), xn, C, k.rms_eps));
+        Q3_TRY(proj(xn, C, lw + L.o_wqkv, qkv_n, EPI_F32, qkv));
+        Q3_TRY(launch_qknorm_rope_kv(lc, qkv, rows, (const float *)(lw + L.o_gq),
+                                     (const float *)(lw + L.o_gk), rope, q, c->kcache(l),
+                                     c->vcache(l), Hq, Hkv, k.max_ctx, k.rms_eps, err));
+        if (decode)
+            Q3_TRY(launch_attn_decode(lc, q, c->kcache(l), c->vcache(l), rows, n_split, kps,
+                                      c->at<float>(L.o_wsml), c->at<float>(L.o_wso), attn, Hq, Hkv,
+                                      k.max_ctx));
+        else
+            Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens,
+                                       rows.slots, rows.B, max_len, attn, Hq, Hkv, k.max_ctx));
+        Q3_TRY(proj(attn, Hq * D, lw + L.o_wo, C, EPI_RESID_ADD, resid));
+        Q3_TRY(launch_rmsnorm(lc, resid, R, (const float *)(lw + L.o_gpost), xn, C, k.rms_eps));
+        Q3_TRY(proj(xn, C, lw + L.o_wgu, 2 * I, EPI_SWIGLU, act));
+        Q3_TRY(proj(act, I, lw + L.o_wdown, C, EPI_RESID_ADD, resid));
+        Q3_TRY(dump(l + 1));
+    }
+    bf16 *last = c->at<bf16>(L.o_last);
+    Q3_TRY(launch_final_norm(lc, resid, rows.cu_seqlens, rows.B, c->at<float>(L.o_gfinal), last, C,
+                             k.rms_eps));
+    return launch_lmhead_argmax(lc, last, rows.B, C, embed, k.vocab, logits, c->at<float>(L.o_pval),
+                                c->at<int32_t>(L.o_pidx), c->n_parts, next, rows);
+}
+
+Rows make_rows(qwen3_ctx *c, const int32_t *cu, const int32_t *slots, int B, int rows) {
+    Rows r;
+    r.cu_seqlens = cu;
+    r.slots = slots;
+    r.row_slot = c->at<int32_t>(c->lay.o_rowslot);
+    r.row_pos = c->at<int32_t>(c->lay.o_rowpos);
+    r.ctx_len = c->at<int32_t>(c->lay.o_ctxlen);
+    r.B = B;
+    r.rows = rows;
+    return r;
+}
+
+int check_slots(qwen3_ctx *c, const int32_t *slots_host, int B) {
+    std::vector<char> seen(c->cfg.max_seqs, 0);
+    for (int b = 0; b < B; ++b) {
+        const int s = slots_host[b];
+        if (s < 0 || s >= c->cfg.max_seqs) return c->fail(QWEN3_E_INVALID, "slot out of range");
+        if (seen[s]) return c->fail(QWEN3_E_INVALID, "slot repeated within one call");
+        seen[s] = 1;
+    }
+    return QWEN3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qwen3_arena_bytes(const qwen3_config *cfg) {
+    if (!cfg || !config_supported(*cfg, nullptr)) return 0;
+    return make_layout(*cfg).total;
+}
+
+int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_dev,
+                 size_t arena_bytes, void *stream_v, qwen3_ctx **out) {
+    g_create_error.clear();
+    auto fail = [](int code, const std::string &m) {
+        g_create_error = m;
+        return code;
+    };
+    if (!cfg || !w || !arena_dev || !out) return fail(QWEN3_E_INVALID, "NULL argument");
+    *out = nullptr;
+    std::string why;
+    if (!config_supported(*cfg, &why)) return fail(QWEN3_E_UNSUPPORTED, why);
+    const Layout lay = make_layout(*cfg);
+    if (arena_bytes < lay.total) return fail(QWEN3_E_INVALID, "arena smaller than qwen3_arena_bytes()");
+    if (reinterpret_cast<uintptr_t>(arena_dev) % 256) return fail(QWEN3_E_INVALID, "arena not 256-byte aligned");
+    if (!w->embed || !w->final_norm || !w->in_norm || !w->post_norm || !w->q_norm || !w->k_norm ||
+        !w->wq || !w->wk || !w->wv || !w->wo || !w->wgate || !w->wup || !w->wdown)
+        return fail(QWEN3_E_INVALID, "NULL weight pointer");
+    for (int l = 0; l < cfg->n_layers; ++l)
+        if (!w->in_norm[l] || !w->post_norm[l] || !w->q_norm[l] || !w->k_norm[l] || !w->wq[l] ||
+            !w->wk[l] || !w->wv[l] || !w->wo[l] || !w->wgate[l] || !w->wup[l] || !w->wdown[l])
+            return fail(QWEN3_E_INVALID, "NULL per-layer weight pointer");
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(QWEN3_E_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return fail(QWEN3_E_CUDA, std::string("cudaGetDeviceProperties: ") + cudaGetErrorString(e));
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(QWEN3_E_UNSUPPORTED, "this build targets compute capability 10.3 (sm_103a)");
+
+    qwen3_ctx *c = new qwen3_ctx();
+    c->cfg = *cfg;
+    c->lay = lay;
+    c->arena = static_cast<uint8_t *>(arena_dev);
+    c->len_host.assign(cfg->max_seqs, 0);
+    c->num_sms = prop.multiProcessorCount;
+    c->n_parts = std::min(lmhead_parts(c->num_sms), MAX_PARTS);
+    cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+    Launch lc;
+    lc.stream = st;
+    lc.pdl = false;
+    lc.num_sms = c->num_sms;
+    lc.counter = &c->launches;
+
+    const size_t C = cfg->hidden, D = cfg->head_dim, Hq = cfg->n_q_heads, Hkv = cfg->n_kv_heads,
+                 I = cfg->intermediate;
+    auto d2d = [&](void *dst, const void *src, size_t bytes) {
+        return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+    };
+    auto body = [&]() -> cudaError_t {
+        for (int l = 0; l < cfg->n_layers; ++l) {
+            uint8_t *lw = c->layer(l);
+            // QKV rows stacked [q; k; v]
+            Q3_TRY(d2d(lw + lay.o_wqkv, w->wq[l], Hq * D * C * 2));
+            Q3_TRY(d2d(lw + lay.o_wqkv + Hq * D * C * 2, w->wk[l], Hkv * D * C * 2));
+            Q3_TRY(d2d(lw + lay.o_wqkv + (Hq + Hkv) * D * C * 2, w->wv[l], Hkv * D * C * 2));
+            Q3_TRY(d2d(lw + lay.o_wo, w->wo[l], C * Hq * D * 2));
+            // gate/up interleaved row by row: row 2j = gate_j, row 2j+1 = up_j
+            Q3_TRY(cudaMemcpy2DAsync(lw + lay.o_wgu, 2 * C * 2, w->wgate[l], C * 2, C * 2, I,
+                                     cudaMemcpyDeviceToDevice, st));
+            Q3_TRY(cudaMemcpy2DAsync(lw + lay.o_wgu + C * 2, 2 * C * 2, w->wup[l], C * 2, C * 2, I,
+                                     cudaMemcpyDeviceToDevice, st));
+            Q3_TRY(d2d(lw + lay.o_wdown, w->wdown[l], C * I * 2));
+            Q3_TRY(launch_bf16_to_f32(lc, (const bf16 *)w->in_norm[l], (float *)(lw + lay.o_gin), (int)C));
+            Q3_TRY(launch_bf16_to_f32(lc, (const bf16 *)w->post_norm[l], (float *)(lw + lay.o_gpost), (int)C));
+            Q3_TRY(launch_bf16_to_f32(lc, (const bf16 *)w->q_norm[l], (float *)(lw + lay.o_gq), (int)D));
+            Q3_TRY(launch_bf16_to_f32(lc, (const bf16 *)w->k_norm[l], (float *)(lw + lay.o_gk), (int)D));
+        }
+        Q3_TRY(d2d(c->arena + lay.o_embed, w->embed, (size_t)cfg->vocab * C * 2));
+        Q3_TRY(launch_bf16_to_f32(lc, (const bf16 *)w->final_norm, c->at<float>(lay.o_gfinal), (int)C));
+        // RoPE table: (cos, sin) of p * theta^(-2i/D), i < D/2, computed in double precision
+        std::vector<float2> tab((size_t)cfg->max_ctx * (D / 2));
+        for (int p = 0; p < cfg->max_ctx; ++p)
+            for (size_t i = 0; i < D / 2; ++i) {
+                const double inv_freq = std::pow(cfg->rope_theta, -2.0 * (double)i / (double)D);
+                const double a = (double)p * inv_freq;
+                tab[(size_t)p * (D / 2) + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+            }
+        Q3_TRY(cudaMemcpyAsync(c->arena + lay.o_rope, tab.data(), tab.size() * sizeof(float2),
+                               cudaMemcpyHostToDevice, st));
+        Q3_TRY(cudaMemsetAsync(c->arena + lay.o_ctxlen, 0, (size_t)cfg->max_seqs * 4, st));
+        Q3_TRY(cudaMemsetAsync(c->arena + lay.o_err, 0, 16, st));
+        Q3_TRY(cudaStreamSynchronize(st));
+        return cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
+    };
+    e = body();
+    if (e != cudaSuccess) {
+        delete c;
+        return fail(QWEN3_E_CUDA, std::string("qwen3_create: ") + cudaGetErrorString(e));
+    }
+    *out = c;
+    return QWEN3_OK;
+}
+
+int qwen3_prefill(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev,
+                  const int32_t *cu_host, const int32_t *slots_dev, const int32_t *slots_host,
+                  int32_t B, float *logits_dev, int32_t *next_tok_dev, void *stream_v) {
+    if (!c) return QWEN3_E_INVALID;
+    if (!tokens_dev || !cu_dev || !cu_host || !slots_dev || !slots_host || !next_tok_dev)
+        return c->fail(QWEN3_E_INVALID, "NULL argument");
+    if (B < 1) return c->fail(QWEN3_E_INVALID, "B must be >= 1");
+    if (B > c->cfg.max_seqs) return c->fail(QWEN3_E_CAPACITY, "B exceeds max_seqs");
+    if (cu_host[0] != 0) return c->fail(QWEN3_E_INVALID, "cu_seqlens[0] must be 0");
+    int max_len = 0;
+    for (int b = 0; b < B; ++b) {
+        const int n = cu_host[b + 1] - cu_host[b];
+        if (n < 1) return c->fail(QWEN3_E_INVALID, "cu_seqlens must be strictly increasing");
+        if (n > c->cfg.max_ctx) return c->fail(QWEN3_E_CAPACITY, "sequence longer than max_ctx");
+        max_len = std::max(max_len, n);
+    }
+    const int N = cu_host[B];
+    if (N > c->cfg.max_prefill_tokens) return c->fail(QWEN3_E_CAPACITY, "N exceeds max_prefill_tokens");
+    if (int rc = check_slots(c, slots_host, B)) return rc;
+    if (c->dump && c->dump_bytes < (size_t)(c->cfg.n_layers + 1) * N * c->cfg.hidden * 4)
+        return c->fail(QWEN3_E_CAPACITY, "debug dump buffer too small for this call");
+
+    Launch lc;
+    lc.stream = static_cast<cudaStream_t>(stream_v);
+    lc.num_sms = c->num_sms;
+    lc.counter = &c->launches;
+    const Rows rows = make_rows(c, cu_dev, slots_dev, B, N);
+    cudaError_t e = run_forward(c, lc, tokens_dev, rows, false, max_len, 0, 0, logits_dev, next_tok_dev);
+    if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_prefill");
+    for (int b = 0; b < B; ++b) c->len_host[slots_host[b]] = cu_host[b + 1] - cu_host[b];
+    return QWEN3_OK;
+}
+
+int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *slots_dev,
+                      const int32_t *slots_host, int32_t B, float *logits_dev,
+                      int32_t *next_tok_dev, void *stream_v) {
+    if (!c) return QWEN3_E_INVALID;
+    if (!tokens_dev || !slots_dev || !slots_host || !next_tok_dev)
+        return c->fail(QWEN3_E_INVALID, "NULL argument");
+    if (B < 1) return c->fail(QWEN3_E_INVALID, "B must be >= 1");
+    if (B > c->cfg.max_seqs) return c->fail(QWEN3_E_CAPACITY, "B exceeds max_seqs");
+    if (int rc = check_slots(c, slots_host, B)) return rc;
+    int max_len = 0;
+    for (int b = 0; b < B; ++b) {
+        const int n = c->len_host[slots_host[b]];
+        if (n < 1) return c->fail(QWEN3_E_INVALID, "slot has not been prefilled");
+        if (n + 1 > c->cfg.max_ctx) return c->fail(QWEN3_E_CAPACITY, "slot already holds max_ctx tokens");
+        max_len = std::max(max_len, n + 1);
+    }
+    if (c->dump && c->dump_bytes < (size_t)(c->cfg.n_layers + 1) * B * c->cfg.hidden * 4)
+        return c->fail(QWEN3_E_CAPACITY, "debug dump buffer too small for this call");
+
+    // Split plan of the decode attention: from a power-of-two bucket of the longest context,
+    // so a recorded graph stays valid while contexts grow inside the bucket.
+    int bucket = 64;
+    while (bucket < max_len) bucket <<= 1;
+    bucket = std::min(bucket, c->cfg.max_ctx);
+    const int want = (4 * c->num_sms + B * c->cfg.n_kv_heads - 1) / (B * c->cfg.n_kv_heads);
+    const int n_split = std::max(1, std::min({want, MAX_SPLIT, (bucket + 63) / 64}));
+    const int kps = ((bucket + n_split - 1) / n_split + 15) / 16 * 16;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+    const Rows rows = make_rows(c, nullptr, slots_dev, B, B);
+    const bool use_graph = !(c->cfg.flags & QWEN3_FLAG_NO_GRAPH) && !c->dump;
+    if (!use_graph) {
+        Launch lc;
+        lc.stream = st;
+        lc.num_sms = c->num_sms;
+        lc.counter = &c->launches;
+        cudaError_t e = run_forward(c, lc, tokens_dev, rows, true, 0, n_split, kps, logits_dev, next_tok_dev);
+        if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_decode_step");
+    } else {
+        GraphEntry *g = nullptr;
+        for (auto &x : c->graphs)
+            if (x.B == B && x.n_split == n_split && x.kps == kps && x.tokens == tokens_dev &&
+                x.slots == slots_dev && x.logits == logits_dev && x.next == next_tok_dev)
+                g = &x;
+        if (!g) {
+            Launch lc;
+            lc.stream = c->cap_stream;
+            lc.num_sms = c->num_sms;
+            cudaError_t e = cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal);
+            if (e != cudaSuccess) return c->cuda_fail(e, "cudaStreamBeginCapture");
+            e = run_forward(c, lc, tokens_dev, rows, true, 0, n_split, kps, logits_dev, next_tok_dev);
+            cudaGraph_t graph = nullptr;
+            const cudaError_t e2 = cudaStreamEndCapture(c->cap_stream, &graph);
+            if (e != cudaSuccess || e2 != cudaSuccess) {
+                if (graph) cudaGraphDestroy(graph);
+                return c->cuda_fail(e != cudaSuccess ? e : e2, "decode graph capture");
+            }
+            cudaGraphExec_t exec = nullptr;
+            e = cudaGraphInstantiate(&exec, graph, 0);
+            size_t n_nodes = 0;
+            if (e == cudaSuccess) e = cudaGraphGetNodes(graph, nullptr, &n_nodes);
+            std::vector<cudaGraphNode_t> nodes(n_nodes);
+            int64_t kernels = 0;
+            if (e == cudaSuccess && n_nodes) e = cudaGraphGetNodes(graph, nodes.data(), &n_nodes);
+            for (size_t i = 0; e == cudaSuccess && i < n_nodes; ++i) {
+                cudaGraphNodeType t;
+                e = cudaGraphNodeGetType(nodes[i], &t);
+                if (t == cudaGraphNodeTypeKernel) ++kernels;
+            }
+            cudaGraphDestroy(graph);
+            if (e != cudaSuccess) {
+                if (exec) cudaGraphExecDestroy(exec);
+                return c->cuda_fail(e, "decode graph instantiate");
+            }
+            c->graphs.push_back(GraphEntry{B, n_split, kps, tokens_dev, slots_dev, logits_dev,
+                                           next_tok_dev, exec, kernels});
+            g = &c->graphs.back();
+        }
+        cudaError_t e = cudaGraphLaunch(g->exec, st);
+        if (e != cudaSuccess) return c->cuda_fail(e, "cudaGraphLaunch");
+        c->launches += g->kernels;
+    }
+    for (int b = 0; b < B; ++b) c->len_host[slots_host[b]] += 1;
+    return QWEN3_OK;
+}
+
+int qwen3_set_debug_dump(qwen3_ctx *c, float *hidden_dev, size_t bytes) {
+    if (!c) return QWEN3_E_INVALID;
+    c->dump = hidden_dev;
+    c->dump_bytes = hidden_dev ? bytes : 0;
+    return QWEN3_OK;
+}
+
+int qwen3_get_status(qwen3_ctx *c) {
+    if (!c) return QWEN3_E_INVALID;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_get_status");
+    uint32_t word = 0;
+    e = cudaMemcpy(&word, c->arena + c->lay.o_err, 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_get_status");
+    if (word) {
+        cudaMemset(c->arena + c->lay.o_err, 0, 4);
+        std::string m = "device error word set:";
+        if (word & ERR_TOKEN_RANGE) m += " token id out of range (clamped);";
+        if (word & ERR_POSITION) m += " position beyond max_ctx (KV write skipped);";
+        return c->fail(QWEN3_E_DEVICE, m);
+    }
+    return QWEN3_OK;
+}
+
+const char *qwen3_last_error(const qwen3_ctx *c) {
+    return c ? c->err.c_str() : g_create_error.c_str();
+}
+
+int32_t qwen3_slot_length(const qwen3_ctx *c, int32_t slot) {
+    if (!c || slot < 0 || slot >= c->cfg.max_seqs) return -1;
+    return c->len_host[slot];
+}
+
+int qwen3_kv_view(const qwen3_ctx *c, int32_t layer, int32_t slot, const void **k_dev,
+                  const void **v_dev) {
+    if (!c || !k_dev || !v_dev) return QWEN3_E_INVALID;
+    if (layer < 0 || layer >= c->cfg.n_layers || slot < 0 || slot >= c->cfg.max_seqs)
+        return QWEN3_E_INVALID;
+    const size_t per_slot = (size_t)c->cfg.n_kv_heads * c->cfg.max_ctx * c->cfg.head_dim;
+    *k_dev = c->kcache(layer) + (size_t)slot * per_slot;
+    *v_dev = c->vcache(layer) + (size_t)slot * per_slot;
+    return QWEN3_OK;
+}
+
+int64_t qwen3_launch_count(const qwen3_ctx *c) { return c ? c->launches : 0; }
+
+void qwen3_free(qwen3_ctx *c) {
+    if (!c) return;
+    for (auto &g : c->graphs) cudaGraphExecDestroy(g.exec);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+    delete c;
+}
+
+}  // extern "C"

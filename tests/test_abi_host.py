@@ -1,0 +1,82 @@
+"""Host-side checks of the C ABI: the library builds, exports every declared call, sizes
+its arena and rejects bad arguments before touching the GPU."""
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from qwen3_decoder_forward_gb300 import binding, build, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(qwen3_\w+)\s*\(", text, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "qwen3_create" in names and "qwen3_decode_step" in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_arena_bytes(lib):
+    s = synth.QWEN3_0P6B
+    small = binding.qwen3_arena_bytes(binding.make_config(s, 1, 256, 128))
+    big = binding.qwen3_arena_bytes(binding.make_config(s, 16, 16416, 16384))
+    assert small > 0 and big > small
+    kv = 28 * 2 * 16 * 8 * 16416 * 128 * 2
+    weights = 28 * 15728640 * 2 + 151936 * 1024 * 2
+    assert kv + weights < big < kv + weights + 16 * 2 ** 30
+
+
+@pytest.mark.parametrize("field,value", [("head_dim", 64), ("n_kv_heads", 3), ("hidden", 1000),
+                                         ("max_seqs", 0), ("vocab", 0), ("intermediate", 100)])
+def test_unsupported_config_sizes_to_zero(lib, field, value):
+    cfg = binding.make_config(synth.QWEN3_0P6B, 4, 512, 512)
+    setattr(cfg, field, value)
+    assert binding.qwen3_arena_bytes(cfg) == 0
+
+
+def test_create_rejects_null_and_unsupported(lib):
+    cfg = binding.make_config(synth.QWEN3_TINY, 1, 64, 64)
+    w = binding.qwen3_weights()
+    with pytest.raises(binding.Qwen3Error) as e:
+        binding.qwen3_create(cfg, w, 0, 0)
+    assert e.value.code == binding.QWEN3_E_INVALID
+    cfg.head_dim = 64
+    with pytest.raises(binding.Qwen3Error) as e:
+        binding.qwen3_create(cfg, w, 1 << 20, 1 << 30)
+    assert e.value.code == binding.QWEN3_E_UNSUPPORTED
+    assert "head_dim" in binding.qwen3_last_error(None)
+
+
+def test_null_context_calls_are_rejected(lib):
+    assert lib.qwen3_get_status(None) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_slot_length(None, 0) == -1
+    assert lib.qwen3_launch_count(None) == 0
+    lib.qwen3_free(None)
+
+
+def test_package_import_loads_no_cuda():
+    import importlib
+    import sys
+    mod = importlib.import_module("qwen3_decoder_forward_gb300")
+    assert "libqwen3_gb300" not in str(sys.modules.get("qwen3_decoder_forward_gb300.binding", ""))
+    assert mod is not None
