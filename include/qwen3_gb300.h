@@ -53,6 +53,7 @@ extern "C" {
 
 /* qwen3_config.flags */
 #define QWEN3_FLAG_NO_GRAPH 1u   /* launch decode steps one kernel at a time instead of a CUDA graph */
+#define QWEN3_FLAG_NO_PDL 2u     /* launch kernels without programmatic dependent launch (for profilers) */
 
 /* Model and capacity.  Supported: head_dim == 128; n_q_heads a multiple of n_kv_heads with
  * n_q_heads / n_kv_heads <= 8; hidden, n_q_heads*head_dim and intermediate multiples of 256;
@@ -160,6 +161,40 @@ int qwen3_kv_view(const qwen3_ctx *ctx, int32_t layer, int32_t slot, const void 
 /* Number of kernels this context has launched so far (graph replays count every kernel
  * node of the graph). */
 int64_t qwen3_launch_count(const qwen3_ctx *ctx);
+
+/* ---- Single kernels, as the forward runs them (no context needed) ----------------------
+ * These run one step of the forward on caller buffers, for per-kernel tests and timing.
+ * All buffers are device memory; the calls are asynchronous on `stream`. */
+
+#define QWEN3_EPI_F32 0        /* out fp32 [M, N] = X W^T */
+#define QWEN3_EPI_RESID_ADD 1  /* out fp32 [M, N] += X W^T  (o_proj / down_proj into the residual) */
+#define QWEN3_EPI_SWIGLU 2     /* W rows interleaved (gate_0, up_0, gate_1, up_1, ...):
+                                  out bf16 [M, N/2] = silu(X Wg^T) * (X Wu^T)  ("手写Qwen3-0.6B推理", MLP) */
+
+/* Decode projection (weight-streaming GEMV): X bf16 [M, K] row-major, W bf16 [N, K] row-major
+ * ([out, in] as nn.Linear stores it, "手写Qwen3-0.6B推理", Attention/MLP), fp32 accumulation.
+ * K must be 256, 512, 768, 1024, 1536, 2048, 2560, 3072 or 4096; N a multiple of 2; M >= 1
+ * (processed in groups of 32 rows).  Errors: E_INVALID (NULL, bad size), E_CUDA. */
+int qwen3_op_gemv(const void *x_dev, int32_t M, int32_t K, const void *w_dev, int32_t N,
+                  int32_t epilogue, void *out_dev, void *stream);
+
+/* Prefill projection (tiled tensor-core GEMM), same operands and epilogues as qwen3_op_gemv;
+ * N a multiple of 128, K a multiple of 32, any M >= 1.  Errors: E_INVALID, E_CUDA. */
+int qwen3_op_gemm(const void *x_dev, int32_t M, int32_t K, const void *w_dev, int32_t N,
+                  int32_t epilogue, void *out_dev, void *stream);
+
+/* Bytes of workspace qwen3_op_lmhead_argmax needs for B rows. */
+size_t qwen3_op_lmhead_workspace_bytes(int32_t B);
+
+/* Tied lm_head + greedy argmax ("手写Qwen3-0.6B推理", Qwen3Model/推理; "第 3 章", 4.1 and 4.3):
+ * next_tok[b] = argmax_v E[v] . x[b] (fp32 logits, lowest index on ties) for x bf16 [B, C]
+ * (the final-normed last rows) and E bf16 [V, C]; logits_dev fp32 [B, V] is written when not
+ * NULL.  `workspace_dev` (>= qwen3_op_lmhead_workspace_bytes(B) bytes, 16-byte aligned) holds
+ * per-CTA partial maxima.  C one of the GEMV K values; 1 <= B <= 1024.
+ * Errors: E_INVALID (NULL, bad size, small workspace), E_CUDA. */
+int qwen3_op_lmhead_argmax(const void *x_dev, int32_t B, int32_t C, const void *embed_dev,
+                           int32_t V, float *logits_dev, int32_t *next_tok_dev,
+                           void *workspace_dev, size_t workspace_bytes, void *stream);
 
 /* Releases the context and its graphs.  Does not free the arena or any caller memory. */
 void qwen3_free(qwen3_ctx *ctx);

@@ -22,6 +22,10 @@ QWEN3_E_UNSUPPORTED = -3
 QWEN3_E_CUDA = -4
 QWEN3_E_DEVICE = -5
 QWEN3_FLAG_NO_GRAPH = 1
+QWEN3_FLAG_NO_PDL = 2
+QWEN3_EPI_F32 = 0
+QWEN3_EPI_RESID_ADD = 1
+QWEN3_EPI_SWIGLU = 2
 
 _P = ctypes.c_void_p
 
@@ -75,6 +79,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_kv_view": (ctypes.c_int, [_P, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
         "qwen3_launch_count": (i64, [_P]),
         "qwen3_free": (None, [_P]),
+        "qwen3_op_gemv": (ctypes.c_int, [_P, i32, i32, _P, i32, i32, _P, _P]),
+        "qwen3_op_gemm": (ctypes.c_int, [_P, i32, i32, _P, i32, i32, _P, _P]),
+        "qwen3_op_lmhead_workspace_bytes": (sz, [i32]),
+        "qwen3_op_lmhead_argmax": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P, sz, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -156,6 +164,24 @@ def qwen3_launch_count(ctx) -> int:
 
 def qwen3_free(ctx) -> None:
     load_library().qwen3_free(ctx)
+
+
+def qwen3_op_gemv(x_ptr: int, M: int, K: int, w_ptr: int, N: int, epilogue: int, out_ptr: int, stream: int = 0):
+    _check(load_library().qwen3_op_gemv(x_ptr, M, K, w_ptr, N, epilogue, out_ptr, stream), None)
+
+
+def qwen3_op_gemm(x_ptr: int, M: int, K: int, w_ptr: int, N: int, epilogue: int, out_ptr: int, stream: int = 0):
+    _check(load_library().qwen3_op_gemm(x_ptr, M, K, w_ptr, N, epilogue, out_ptr, stream), None)
+
+
+def qwen3_op_lmhead_workspace_bytes(B: int) -> int:
+    return int(load_library().qwen3_op_lmhead_workspace_bytes(B))
+
+
+def qwen3_op_lmhead_argmax(x_ptr: int, B: int, C: int, embed_ptr: int, V: int, logits_ptr: Optional[int],
+                           next_ptr: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
+    _check(load_library().qwen3_op_lmhead_argmax(x_ptr, B, C, embed_ptr, V, logits_ptr, next_ptr, ws_ptr,
+                                                 ws_bytes, stream), None)
 
 
 # --- device-memory owner -------------------------------------------------------------------

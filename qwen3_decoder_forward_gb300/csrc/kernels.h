@@ -37,13 +37,13 @@ cudaError_t launch(const Launch &lc, void (*kern)(KArgs...), dim3 grid, dim3 blo
 // Row bookkeeping of one call: row r of the packed batch belongs to KV slot row_slot[r]
 // at absolute position row_pos[r].
 struct Rows {
-    const int32_t *cu_seqlens;  // [B+1] for prefill, nullptr for decode (one row per sequence)
-    const int32_t *slots;       // [B]
-    int32_t *row_slot;          // [rows] written by the embedding kernel
-    int32_t *row_pos;           // [rows]
-    int32_t *ctx_len;           // [max_seqs] tokens cached per slot
-    int32_t B;
-    int32_t rows;
+    const int32_t *cu_seqlens = nullptr;  // [B+1] for prefill, nullptr for decode (one row per sequence)
+    const int32_t *slots = nullptr;       // [B]
+    int32_t *row_slot = nullptr;          // [rows] written by the embedding kernel
+    int32_t *row_pos = nullptr;           // [rows]
+    int32_t *ctx_len = nullptr;           // [max_seqs] tokens cached per slot (nullptr: no bookkeeping)
+    int32_t B = 0;
+    int32_t rows = 0;
 };
 
 // --- norm.cu ---------------------------------------------------------------------------

@@ -126,8 +126,10 @@ __global__ void __launch_bounds__(256) k_argmax_reduce(const float *__restrict__
     }
     if (threadIdx.x == 0) {
         next_tok[b] = si[0];
-        const int row = r.cu_seqlens ? r.cu_seqlens[b + 1] - 1 : b;
-        r.ctx_len[r.row_slot[row]] = r.row_pos[row] + 1;
+        if (r.ctx_len) {
+            const int row = r.cu_seqlens ? r.cu_seqlens[b + 1] - 1 : b;
+            r.ctx_len[r.row_slot[row]] = r.row_pos[row] + 1;
+        }
     }
 }
 

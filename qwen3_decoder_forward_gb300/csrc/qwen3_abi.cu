@@ -361,6 +361,7 @@ int qwen3_prefill(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev
 
     Launch lc;
     lc.stream = static_cast<cudaStream_t>(stream_v);
+    lc.pdl = !(c->cfg.flags & QWEN3_FLAG_NO_PDL);
     lc.num_sms = c->num_sms;
     lc.counter = &c->launches;
     const Rows rows = make_rows(c, cu_dev, slots_dev, B, N);
@@ -404,6 +405,7 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
     if (!use_graph) {
         Launch lc;
         lc.stream = st;
+        lc.pdl = !(c->cfg.flags & QWEN3_FLAG_NO_PDL);
         lc.num_sms = c->num_sms;
         lc.counter = &c->launches;
         cudaError_t e = run_forward(c, lc, tokens_dev, rows, true, 0, n_split, kps, logits_dev, next_tok_dev);
@@ -417,6 +419,7 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
         if (!g) {
             Launch lc;
             lc.stream = c->cap_stream;
+            lc.pdl = !(c->cfg.flags & QWEN3_FLAG_NO_PDL);
             lc.num_sms = c->num_sms;
             cudaError_t e = cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal);
             if (e != cudaSuccess) return c->cuda_fail(e, "cudaStreamBeginCapture");
@@ -501,6 +504,81 @@ int qwen3_kv_view(const qwen3_ctx *c, int32_t layer, int32_t slot, const void **
 }
 
 int64_t qwen3_launch_count(const qwen3_ctx *c) { return c ? c->launches : 0; }
+
+static bool gemv_k_ok(int K) {
+    return K == 256 || K == 512 || K == 768 || K == 1024 || K == 1536 || K == 2048 || K == 2560 ||
+           K == 3072 || K == 4096;
+}
+
+static Launch op_launch(void *stream) {
+    Launch lc;
+    lc.stream = static_cast<cudaStream_t>(stream);
+    lc.pdl = false;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&lc.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    return lc;
+}
+
+int qwen3_op_gemv(const void *x, int32_t M, int32_t K, const void *w, int32_t N, int32_t epi,
+                  void *out, void *stream) {
+    g_create_error.clear();
+    if (!x || !w || !out || M < 1 || N < 2 || N % 2 || !gemv_k_ok(K) || epi < 0 || epi > 2) {
+        g_create_error = "qwen3_op_gemv: bad argument";
+        return QWEN3_E_INVALID;
+    }
+    cudaError_t e = launch_gemv(op_launch(stream), (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out);
+    if (e != cudaSuccess) {
+        g_create_error = std::string("qwen3_op_gemv: ") + cudaGetErrorString(e);
+        return QWEN3_E_CUDA;
+    }
+    return QWEN3_OK;
+}
+
+int qwen3_op_gemm(const void *x, int32_t M, int32_t K, const void *w, int32_t N, int32_t epi,
+                  void *out, void *stream) {
+    g_create_error.clear();
+    if (!x || !w || !out || M < 1 || N < 128 || N % 128 || K < 32 || K % 32 || epi < 0 || epi > 2) {
+        g_create_error = "qwen3_op_gemm: bad argument";
+        return QWEN3_E_INVALID;
+    }
+    cudaError_t e = launch_gemm(op_launch(stream), (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out);
+    if (e != cudaSuccess) {
+        g_create_error = std::string("qwen3_op_gemm: ") + cudaGetErrorString(e);
+        return QWEN3_E_CUDA;
+    }
+    return QWEN3_OK;
+}
+
+size_t qwen3_op_lmhead_workspace_bytes(int32_t B) {
+    if (B < 1 || B > 1024) return 0;
+    return (size_t)B * MAX_PARTS * 8;
+}
+
+int qwen3_op_lmhead_argmax(const void *x, int32_t B, int32_t C, const void *embed, int32_t V,
+                           float *logits, int32_t *next_tok, void *ws, size_t ws_bytes,
+                           void *stream) {
+    g_create_error.clear();
+    if (!x || !embed || !next_tok || !ws || B < 1 || B > 1024 || V < 1 || !gemv_k_ok(C) ||
+        C > 3072 || reinterpret_cast<uintptr_t>(ws) % 16 || ws_bytes < qwen3_op_lmhead_workspace_bytes(B)) {
+        g_create_error = "qwen3_op_lmhead_argmax: bad argument";
+        return QWEN3_E_INVALID;
+    }
+    const Launch lc = op_launch(stream);
+    const int n_parts = std::min(lmhead_parts(lc.num_sms), MAX_PARTS);
+    float *pval = static_cast<float *>(ws);
+    int32_t *pidx = reinterpret_cast<int32_t *>(pval + (size_t)B * MAX_PARTS);
+    Rows r;  // no KV bookkeeping for a bare call
+    r.B = B;
+    r.rows = B;
+    cudaError_t e = launch_lmhead_argmax(lc, (const bf16 *)x, B, C, (const bf16 *)embed, V, logits,
+                                         pval, pidx, n_parts, next_tok, r);
+    if (e != cudaSuccess) {
+        g_create_error = std::string("qwen3_op_lmhead_argmax: ") + cudaGetErrorString(e);
+        return QWEN3_E_CUDA;
+    }
+    return QWEN3_OK;
+}
 
 void qwen3_free(qwen3_ctx *c) {
     if (!c) return;
