@@ -196,6 +196,33 @@ int qwen3_op_lmhead_argmax(const void *x_dev, int32_t B, int32_t C, const void *
                            int32_t V, float *logits_dev, int32_t *next_tok_dev,
                            void *workspace_dev, size_t workspace_bytes, void *stream);
 
+/* Allocation-free variant of qwen3_op_lmhead_argmax. The pages have no counterpart of
+ * this call.
+ *
+ * It is for callers that cannot allocate device memory: code enqueuing work while a stream
+ * is recorded into a CUDA graph (where cudaMalloc is refused or not recorded), plug-ins
+ * inside a framework that owns all device allocations, and latency-critical loops that must
+ * not call cudaMalloc/cudaFree (cudaFree synchronises the device).
+ *
+ * Scratch: the per-CTA partials live in a fixed 256 KiB array in the library's device
+ * memory. Every GPU that loads the library holds it until the process exits. The array
+ * limits B to at most 32 rows; a larger B fails with E_CAPACITY and a message naming the
+ * limit. The call itself allocates nothing.
+ *
+ * Set-up: the first call on each device looks up the array's address with that device
+ * current, so make that first call before any stream capture.
+ *
+ * Sharing: all calls on a device share the array, and it keeps the last call's contents.
+ * Every partial a call reads is written by that same call, so nothing needs clearing.
+ * Calls that overlap on the GPU (e.g. on two streams without ordering) race on the array
+ * and must not be issued.
+ *
+ * Arguments, outputs and the other errors are those of qwen3_op_lmhead_argmax; the message
+ * of a failure is returned by qwen3_last_error(NULL). */
+int qwen3_op_lmhead_argmax_noalloc(const void *x_dev, int32_t B, int32_t C,
+                                   const void *embed_dev, int32_t V, float *logits_dev,
+                                   int32_t *next_tok_dev, void *stream);
+
 /* Releases the context and its graphs.  Does not free the arena or any caller memory. */
 void qwen3_free(qwen3_ctx *ctx);
 

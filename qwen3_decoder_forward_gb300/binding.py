@@ -83,6 +83,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_op_gemm": (ctypes.c_int, [_P, i32, i32, _P, i32, i32, _P, _P]),
         "qwen3_op_lmhead_workspace_bytes": (sz, [i32]),
         "qwen3_op_lmhead_argmax": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P, sz, _P]),
+        "qwen3_op_lmhead_argmax_noalloc": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -182,6 +183,13 @@ def qwen3_op_lmhead_argmax(x_ptr: int, B: int, C: int, embed_ptr: int, V: int, l
                            next_ptr: int, ws_ptr: int, ws_bytes: int, stream: int = 0):
     _check(load_library().qwen3_op_lmhead_argmax(x_ptr, B, C, embed_ptr, V, logits_ptr, next_ptr, ws_ptr,
                                                  ws_bytes, stream), None)
+
+
+def qwen3_op_lmhead_argmax_noalloc(x_ptr: int, B: int, C: int, embed_ptr: int, V: int,
+                                   logits_ptr: Optional[int], next_ptr: int, stream: int = 0):
+    """lm_head + argmax with the library's fixed scratch instead of a caller workspace (B <= 32)."""
+    _check(load_library().qwen3_op_lmhead_argmax_noalloc(x_ptr, B, C, embed_ptr, V, logits_ptr, next_ptr,
+                                                         stream), None)
 
 
 # --- device-memory owner -------------------------------------------------------------------

@@ -110,6 +110,10 @@ thread_local std::string g_create_error;
 
 }  // namespace
 
+namespace q3 {
+void set_last_error(const std::string &msg) { g_create_error = msg; }
+}  // namespace q3
+
 struct GraphEntry {
     int B, n_split, kps;
     const void *tokens, *slots;
