@@ -173,29 +173,52 @@ class KVCache:
 
     [P4] 核心计算函数与Transformer层: the cache keeps projected, normed and
     rotated K and projected V; prefill stores all rows, each step appends one.
+    Rows live in preallocated arrays that grow when full, so an append copies
+    only the new rows.
     """
 
     def __init__(self, n_layers: int):
-        self.k: List[Optional[np.ndarray]] = [None] * n_layers
-        self.v: List[Optional[np.ndarray]] = [None] * n_layers
+        self._k: List[Optional[np.ndarray]] = [None] * n_layers
+        self._v: List[Optional[np.ndarray]] = [None] * n_layers
+        self._n = [0] * n_layers
 
     @property
     def length(self) -> int:
-        return 0 if self.k[0] is None else self.k[0].shape[0]
+        return self._n[0]
+
+    def keys(self, layer: int) -> np.ndarray:
+        return self._k[layer][: self._n[layer]]
+
+    def values(self, layer: int) -> np.ndarray:
+        return self._v[layer][: self._n[layer]]
 
     def append(self, layer: int, k: np.ndarray, v: np.ndarray) -> None:
-        if self.k[layer] is None:
-            self.k[layer], self.v[layer] = k, v
-        else:
-            self.k[layer] = np.concatenate([self.k[layer], k], axis=0)
-            self.v[layer] = np.concatenate([self.v[layer], v], axis=0)
+        n, t = self._n[layer], k.shape[0]
+        if self._k[layer] is None or n + t > self._k[layer].shape[0]:
+            cap = max(n + t, 2 * n, 16)
+            grown_k = np.empty((cap,) + k.shape[1:], dtype=DTYPE)
+            grown_v = np.empty((cap,) + v.shape[1:], dtype=DTYPE)
+            if n:
+                grown_k[:n] = self._k[layer][:n]
+                grown_v[:n] = self._v[layer][:n]
+            self._k[layer], self._v[layer] = grown_k, grown_v
+        self._k[layer][n: n + t] = k
+        self._v[layer][n: n + t] = v
+        self._n[layer] = n + t
 
     @staticmethod
-    def from_arrays(k_layers: Sequence[np.ndarray], v_layers: Sequence[np.ndarray]) -> "KVCache":
-        """A cache built from given rows, each [S, Hkv, D] (e.g. another implementation's cache)."""
+    def from_arrays(k_layers: Sequence[np.ndarray], v_layers: Sequence[np.ndarray],
+                    spare: int = 0) -> "KVCache":
+        """A cache holding given rows, each [S, Hkv, D] (e.g. another implementation's
+        cache), with room for `spare` more rows per layer."""
         c = KVCache(len(k_layers))
-        c.k = [np.asarray(a, dtype=DTYPE) for a in k_layers]
-        c.v = [np.asarray(a, dtype=DTYPE) for a in v_layers]
+        for layer, (k, v) in enumerate(zip(k_layers, v_layers)):
+            s = k.shape[0]
+            c._k[layer] = np.empty((s + spare,) + k.shape[1:], dtype=DTYPE)
+            c._v[layer] = np.empty((s + spare,) + v.shape[1:], dtype=DTYPE)
+            c._k[layer][:s] = k
+            c._v[layer][:s] = v
+            c._n[layer] = s
         return c
 
 
@@ -222,8 +245,8 @@ def decoder_layer(cfg: Config, w: Dict[str, np.ndarray], layer: int, h: np.ndarr
     q = apply_rope(q, positions, cfg.rope_theta)
     k = apply_rope(k, positions, cfg.rope_theta)
     cache.append(layer, k, v)
-    k_pos = np.arange(cache.k[layer].shape[0])
-    o = causal_gqa_attention(q, cache.k[layer], cache.v[layer], positions, k_pos)
+    k_pos = np.arange(cache.keys(layer).shape[0])
+    o = causal_gqa_attention(q, cache.keys(layer), cache.values(layer), positions, k_pos)
     if trace is not None:
         trace.setdefault("q", []).append(q)
         trace.setdefault("k", []).append(k)
