@@ -46,7 +46,7 @@ def parse_args():
     p.add_argument("--workload", default="decode_b1")
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--launch", default="graph", choices=["graph", "direct"],
+    p.add_argument("--launch", default="graph", choices=["graph", "graph-nopdl", "direct"],
                    help="direct: decode steps launched kernel by kernel, without PDL (for profilers)")
     p.add_argument("--decode-steps", type=int, default=None,
                    help="override the workload's decode steps (shorter runs for profilers)")
@@ -397,7 +397,8 @@ def gpu_arm(args, wl):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     device = torch.device("cuda", local_rank)
     peaks, peak_kind = load_peaks()
-    flags = 0 if args.launch == "graph" else (binding.QWEN3_FLAG_NO_GRAPH | binding.QWEN3_FLAG_NO_PDL)
+    flags = {"graph": 0, "graph-nopdl": binding.QWEN3_FLAG_NO_PDL,
+             "direct": binding.QWEN3_FLAG_NO_GRAPH | binding.QWEN3_FLAG_NO_PDL}[args.launch]
     runner = GpuRunner(wl, device, flags)
     units, unit = units_per_step(wl)
 

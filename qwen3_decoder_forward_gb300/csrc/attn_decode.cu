@@ -173,6 +173,317 @@ __global__ void __launch_bounds__(D) k_attn_decode_combine(const float *__restri
     out[((size_t)b * Hq + h) * D + d] = __float2bfloat16(o / lsum);
 }
 
+// ---- fused variant: QK-norm + RoPE + KV write in the prologue, split merge by the last CTA --
+//
+// Reads the new row's q/k/v straight from the QKV projection (fp32 [B, (Hq+2Hkv)*128]).
+// Each CTA normalises and rotates its query heads and the new key in registers (lane `sub`
+// of each 8-lane group holds elements sub*16 .. sub*16+15, so the RoPE partner i+64 of
+// element i sits in lane sub^4).  The new K (rounded to bf16, as the cache stores it) and V
+// are written to the cache by split 0 and taken from shared memory by the split that covers
+// the new position; every other key comes from the cache.
+//
+// Cached keys stream through a ring of shared-memory stages filled by bulk asynchronous
+// copies.  Every kernel of the decode chain passes its own dependency wait before it lets
+// the next kernel launch, so when this kernel starts, every kernel before the QKV projection
+// has completed: the cached rows 0..pos-1, the row positions, the gains and the RoPE table
+// are final, and the first stages are requested before the wait.  Only q/k/v of the new
+// row come from the immediately preceding kernel.
+//
+// The CTA that finishes last for a (sequence, KV head) merges all splits (a counter per
+// pair, incremented after a memory fence and reset by that CTA): no second kernel and no
+// waiting on other CTAs.
+
+constexpr int CHUNK = 32;    // keys per stage
+constexpr int STAGES = 4;
+constexpr int STAGE_BYTES = CHUNK * D * 2 * 2;  // K and V rows of one chunk (16 KB)
+
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16(x)); }
+
+template <int G>
+__global__ void __launch_bounds__(WARPS * 32) k_attn_decode_fused(
+    const float *__restrict__ qkv, Rows r, const float *__restrict__ q_gain,
+    const float *__restrict__ k_gain, const float2 *__restrict__ rope, bf16 *__restrict__ k_layer,
+    bf16 *__restrict__ v_layer, int kps, float *__restrict__ ws_ml, float *__restrict__ ws_o,
+    int *__restrict__ counters, bf16 *__restrict__ out, int Hq, int Hkv, int max_ctx, float eps,
+    float scale_log2, uint32_t *err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);              // [STAGES]
+    uint8_t *ring = smem + 128;                                        // [STAGES][K | V]
+    float *s_new = reinterpret_cast<float *>(ring + STAGES * STAGE_BYTES);  // new K, new V [2][D]
+    __shared__ float red_ml[WARPS][G][2];
+    __shared__ float red_o[WARPS][G][D];
+    __shared__ int s_last;
+
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int n_split = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane & 7, kg = lane >> 3;
+    // Written by kernels that have completed (see above): safe before the dependency wait.
+    const int slot = r.row_slot[b];
+    const int pos = r.row_pos[b];
+    const bool pos_ok = pos < max_ctx;
+    const int k_begin = split * kps;
+    const int k_end = pos_ok ? min(pos + 1, k_begin + kps) : k_begin;
+    const int cache_end = max(k_begin, min(k_end, pos));  // cached keys [k_begin, cache_end)
+    const int n_chunks = (cache_end - k_begin + CHUNK - 1) / CHUNK;
+    const size_t head_base = ((size_t)slot * Hkv + g) * max_ctx * D;
+
+    auto issue = [&](int c) {  // chunk c of this split into stage c % STAGES
+        const int st = c % STAGES;
+        const int j0 = k_begin + c * CHUNK;
+        const int n = min(CHUNK, cache_end - j0);
+        const uint32_t bytes = (uint32_t)n * D * 2;
+        mbar_expect_tx(&full[st], 2 * bytes);
+        bulk_g2s(ring + st * STAGE_BYTES, k_layer + head_base + (size_t)j0 * D, bytes, &full[st]);
+        bulk_g2s(ring + st * STAGE_BYTES + CHUNK * D * 2, v_layer + head_base + (size_t)j0 * D, bytes, &full[st]);
+    };
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < STAGES; ++st) mbar_init(&full[st], 1);
+        for (int c = 0; c < min(STAGES, n_chunks); ++c) issue(c);
+    }
+    float gq[16], gk[16];
+    float2 cs[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        gq[e] = q_gain[sub * 16 + e];
+        gk[e] = k_gain[sub * 16 + e];
+        cs[e] = pos_ok ? rope[(size_t)pos * (D / 2) + (sub & 3) * 16 + e] : make_float2(1.0f, 0.0f);
+    }
+    __syncthreads();  // the barriers are initialised before anyone waits on them
+
+    pdl_wait();
+    pdl_trigger();
+    if (!pos_ok) {
+        if (threadIdx.x == 0 && split == 0) atomicOr(err, ERR_POSITION);
+        return;  // no copy was issued
+    }
+    const int heads = Hq + 2 * Hkv;
+    const float *row = qkv + (size_t)b * heads * D;
+    // one round trip: every q/k/v value this lane needs
+    float x[G + 2][16];
+#pragma unroll
+    for (int hh = 0; hh < G + 2; ++hh) {
+        const int head = hh < G ? g * G + hh : (hh == G ? Hq + g : Hq + Hkv + g);
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(row + (size_t)head * D + sub * 16 + e);
+            x[hh][e] = t.x; x[hh][e + 1] = t.y; x[hh][e + 2] = t.z; x[hh][e + 3] = t.w;
+        }
+    }
+    // per-head RMSNorm + rotate-half RoPE of the G query heads and the new key
+    float qv[G][16];
+#pragma unroll
+    for (int hh = 0; hh < G + 1; ++hh) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) ss += x[hh][e] * x[hh][e];
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+        const float inv = rsqrtf(ss * (1.0f / D) + eps);
+        const float *gn = hh < G ? gq : gk;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[hh][e] *= inv * gn[e];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float partner = __shfl_xor_sync(0xffffffffu, x[hh][e], 4);
+            const float rot = sub < 4 ? x[hh][e] * cs[e].x - partner * cs[e].y   // x_i cos - x_{i+64} sin
+                                      : x[hh][e] * cs[e].x + partner * cs[e].y;  // x_{i+64} cos + x_i sin
+            if (hh < G) qv[hh < G ? hh : 0][e] = rot * scale_log2;
+            else x[G][e] = round_bf16(rot);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) x[G + 1][e] = round_bf16(x[G + 1][e]);
+    if (warp == 0 && kg == 0) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            s_new[sub * 16 + e] = x[G][e];
+            s_new[D + sub * 16 + e] = x[G + 1][e];
+        }
+        if (split == 0) {
+            uint4 pk[2], pv[2];
+            uint32_t *a = reinterpret_cast<uint32_t *>(pk), *c = reinterpret_cast<uint32_t *>(pv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                a[e] = pack_bf16x2(x[G][2 * e], x[G][2 * e + 1]);
+                c[e] = pack_bf16x2(x[G + 1][2 * e], x[G + 1][2 * e + 1]);
+            }
+            uint4 *kd = reinterpret_cast<uint4 *>(k_layer + head_base + (size_t)pos * D + sub * 16);
+            uint4 *vd = reinterpret_cast<uint4 *>(v_layer + head_base + (size_t)pos * D + sub * 16);
+            kd[0] = pk[0]; kd[1] = pk[1];
+            vd[0] = pv[0]; vd[1] = pv[1];
+        }
+    }
+
+    float m[G], l[G], acc[G][16];
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+        m[gi] = -INFINITY;
+        l[gi] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[gi][e] = 0.0f;
+    }
+    auto update = [&](const float *kf, const float *vf, bool valid) {
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+            float s = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) s = fmaf(qv[gi][e], kf[e], s);
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            s += __shfl_xor_sync(0xffffffffu, s, 2);
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            if (valid) {
+                const float mn = fmaxf(m[gi], s);
+                const float c = exp2f(m[gi] - mn);
+                const float p = exp2f(s - mn);
+                l[gi] = l[gi] * c + p;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[gi][e] = fmaf(p, vf[e], acc[gi][e] * c);
+                m[gi] = mn;
+            }
+        }
+    };
+
+    bool ok = true;
+    for (int c = 0; c < n_chunks; ++c) {
+        const int st = c % STAGES;
+        const bool late = !mbar_wait_bounded(&full[st], (c / STAGES) & 1, err);
+        if (__syncthreads_or(late)) {  // the whole CTA gives up together
+            ok = false;
+            break;
+        }
+        const uint8_t *ks = ring + st * STAGE_BYTES;
+        const uint8_t *vs = ks + CHUNK * D * 2;
+        const int n = min(CHUNK, cache_end - (k_begin + c * CHUNK));
+#pragma unroll
+        for (int it = 0; it < CHUNK / (WARPS * 4); ++it) {
+            const int jj = it * WARPS * 4 + warp * 4 + kg;
+            const bool valid = jj < n;
+            const int js = valid ? jj : 0;
+            const uint4 *kp = reinterpret_cast<const uint4 *>(ks + (size_t)js * D * 2 + sub * 32);
+            const uint4 *vp = reinterpret_cast<const uint4 *>(vs + (size_t)js * D * 2 + sub * 32);
+            float kf[16], vf[16];
+            unpack8(kp[0], kf);
+            unpack8(kp[1], kf + 8);
+            unpack8(vp[0], vf);
+            unpack8(vp[1], vf + 8);
+            update(kf, vf, valid);
+        }
+        __syncthreads();  // every warp is done with stage st
+        if (threadIdx.x == 0 && c + STAGES < n_chunks) issue(c + STAGES);
+    }
+    if (!ok) {
+        // give the copies already issued a bounded chance to land, then leave
+        for (int c = 0; c < min(STAGES, n_chunks); ++c) mbar_wait_bounded(&full[c % STAGES], 0, nullptr);
+        return;
+    }
+    __syncthreads();  // s_new is visible
+    if (warp == 0 && k_begin <= pos && pos < k_end) {  // the new key, from shared memory
+        float kf[16], vf[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            kf[e] = s_new[sub * 16 + e];
+            vf[e] = s_new[D + sub * 16 + e];
+        }
+        update(kf, vf, kg == 0);
+    }
+
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m[gi], off);
+            const float lo = __shfl_xor_sync(0xffffffffu, l[gi], off);
+            const float mn = fmaxf(m[gi], mo);
+            const float c1 = mn == -INFINITY ? 0.0f : exp2f(m[gi] - mn);
+            const float c2 = mn == -INFINITY ? 0.0f : exp2f(mo - mn);
+            l[gi] = l[gi] * c1 + lo * c2;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float ao = __shfl_xor_sync(0xffffffffu, acc[gi][e], off);
+                acc[gi][e] = acc[gi][e] * c1 + ao * c2;
+            }
+            m[gi] = mn;
+        }
+    }
+    if (kg == 0) {
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) {
+            if (sub == 0) {
+                red_ml[warp][gi][0] = m[gi];
+                red_ml[warp][gi][1] = l[gi];
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) red_o[warp][gi][sub * 16 + e] = acc[gi][e];
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * D; idx += WARPS * 32) {
+        const int gi = idx / D, d = idx % D;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) mx = fmaxf(mx, red_ml[w][gi][0]);
+        float lsum = 0.0f, o = 0.0f;
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) {
+            const float c = mx == -INFINITY ? 0.0f : exp2f(red_ml[w][gi][0] - mx);
+            lsum += red_ml[w][gi][1] * c;
+            o += red_o[w][gi][d] * c;
+        }
+        const int h = g * G + gi;
+        if (n_split == 1) {
+            out[((size_t)b * Hq + h) * D + d] = __float2bfloat16(o / lsum);
+        } else {
+            const size_t part = ((size_t)b * Hq + h) * n_split + split;
+            ws_o[part * D + d] = o;
+            if (d == 0) {
+                ws_ml[part * 2] = mx;
+                ws_ml[part * 2 + 1] = lsum;
+            }
+        }
+    }
+    if (n_split == 1) return;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(&counters[b * Hkv + g], 1) == n_split - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int idx = threadIdx.x; idx < G * D; idx += WARPS * 32) {
+        const int gi = idx / D, d = idx % D;
+        const int h = g * G + gi;
+        const size_t base = ((size_t)b * Hq + h) * n_split;
+        float mx = -INFINITY;
+        for (int sp = 0; sp < n_split; ++sp) mx = fmaxf(mx, __ldcg(ws_ml + (base + sp) * 2));
+        float lsum = 0.0f, o = 0.0f;
+        for (int sp = 0; sp < n_split; ++sp) {
+            const float ms = __ldcg(ws_ml + (base + sp) * 2);
+            if (ms == -INFINITY) continue;
+            const float c = exp2f(ms - mx);
+            lsum += __ldcg(ws_ml + (base + sp) * 2 + 1) * c;
+            o += __ldcg(ws_o + (base + sp) * D + d) * c;
+        }
+        out[((size_t)b * Hq + h) * D + d] = __float2bfloat16(o / lsum);
+    }
+    if (threadIdx.x == 0) counters[b * Hkv + g] = 0;
+}
+
+template <int G>
+cudaError_t run_fused(const Launch &lc, const float *qkv, const Rows &r, const float *q_gain,
+                      const float *k_gain, const float2 *rope, bf16 *k_layer, bf16 *v_layer, int n_split,
+                      int kps, float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq, int Hkv,
+                      int max_ctx, float eps, uint32_t *err) {
+    const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+    const size_t smem = 128 + (size_t)STAGES * STAGE_BYTES + 2 * D * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_fused<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch(lc, k_attn_decode_fused<G>, dim3(n_split, Hkv, r.B), dim3(WARPS * 32), smem, qkv, r, q_gain,
+                  k_gain, rope, k_layer, v_layer, kps, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps,
+                  scale_log2, err);
+}
+
 template <int G>
 cudaError_t run(const Launch &lc, const bf16 *q, const bf16 *k_layer, const bf16 *v_layer,
                 const Rows &r, int n_split, int kps, float *ws_ml, float *ws_o, bf16 *out, int Hq,
@@ -196,6 +507,20 @@ cudaError_t launch_attn_decode(const Launch &lc, const bf16 *q, const bf16 *k_la
         case 2: return run<2>(lc, q, k_layer, v_layer, r, n_split, keys_per_split, ws_ml, ws_o, out, Hq, Hkv, max_ctx);
         case 4: return run<4>(lc, q, k_layer, v_layer, r, n_split, keys_per_split, ws_ml, ws_o, out, Hq, Hkv, max_ctx);
         case 8: return run<8>(lc, q, k_layer, v_layer, r, n_split, keys_per_split, ws_ml, ws_o, out, Hq, Hkv, max_ctx);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const Rows &r,
+                                     const float *q_gain, const float *k_gain, const float2 *rope,
+                                     bf16 *k_layer, bf16 *v_layer, int n_split, int keys_per_split,
+                                     float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
+                                     int Hkv, int max_ctx, float eps, uint32_t *err) {
+    switch (Hq / Hkv) {
+        case 1: return run_fused<1>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err);
+        case 2: return run_fused<2>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err);
+        case 4: return run_fused<4>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err);
+        case 8: return run_fused<8>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err);
     }
     return cudaErrorInvalidValue;
 }

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <unordered_set>
 #include <utility>
 
 #include "common.cuh"
@@ -17,9 +19,25 @@ struct Launch {
     int64_t *counter = nullptr;
 };
 
+// Every kernel asks for the largest shared-memory carveout, so that the L1/shared split is the
+// same for all of them and a kernel launched early under programmatic dependent launch can
+// be resident on an SM next to its predecessor.
+inline cudaError_t prefer_max_shared(const void *kern) {
+    static std::mutex mu;
+    static std::unordered_set<const void *> done;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(kern)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess) done.insert(kern);
+    return e;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch(const Launch &lc, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                    Args &&...args) {
+    cudaError_t pe = prefer_max_shared(reinterpret_cast<const void *>(kern));
+    if (pe != cudaSuccess) return pe;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -69,6 +87,14 @@ cudaError_t launch_gemm(const Launch &lc, const bf16 *A, int M, int K, const bf1
 // --- gemv.cu (decode; same contract as launch_gemm for small M) ---------------------------
 cudaError_t launch_gemv(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N,
                         int epi, void *out);
+// M <= 8 rows: the weight block of each CTA is bulk-copied before the dependency wait.  With
+// norm_gain, X is fp32 residual rows [M, K] normalised (RMSNorm, eps) on the way in; else X is
+// bf16 [M, K].  W_ahead (same shape as W, may be null): weights of a later launch whose
+// matching block each CTA asks L2 to fetch now.
+bool gemv_fused_supported(int M, int K);
+cudaError_t launch_gemv_fused(const Launch &lc, const void *X, int M, int K, const bf16 *W, int N,
+                              int epi, void *out, const float *norm_gain, float eps, uint32_t *err,
+                              const bf16 *W_ahead = nullptr);
 
 // --- rope_kv.cu --------------------------------------------------------------------------
 // qkv fp32 [rows, (Hq+2Hkv)*D] -> q bf16 [rows, Hq, D] (normed + rotated), K (normed +
@@ -89,6 +115,16 @@ cudaError_t launch_attn_decode(const Launch &lc, const bf16 *q, const bf16 *k_la
                                const bf16 *v_layer, const Rows &r, int n_split,
                                int keys_per_split, float *ws_ml, float *ws_o, bf16 *out, int Hq,
                                int Hkv, int max_ctx);
+
+// Decode attention fed directly by the QKV projection (fp32 [B, (Hq+2Hkv)*D]): per-head
+// QK-norm + RoPE + KV-cache write of the new row, attention over keys 0..pos, and the
+// merge of the n_split key ranges by the last CTA of each (sequence, KV head).  counters
+// [max_seqs * Hkv] must be zero on entry and are left zero.
+cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const Rows &r,
+                                     const float *q_gain, const float *k_gain, const float2 *rope,
+                                     bf16 *k_layer, bf16 *v_layer, int n_split, int keys_per_split,
+                                     float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
+                                     int Hkv, int max_ctx, float eps, uint32_t *err);
 
 // --- lmhead.cu ---------------------------------------------------------------------------
 // next_tok[b] = argmax_v X[b] . E[v] (lowest index on ties); logits[B, V] if not null.

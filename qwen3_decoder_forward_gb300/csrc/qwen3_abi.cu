@@ -30,7 +30,7 @@ struct Layout {
     size_t o_layers = 0, o_embed = 0, o_gfinal = 0, o_rope = 0, o_kcache = 0, o_vcache = 0,
            kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0;
     size_t o_resid = 0, o_xn = 0, o_qkv = 0, o_q = 0, o_attn = 0, o_act = 0, o_rowslot = 0,
-           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0;
+           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0;
     size_t total = 0;
 };
 
@@ -102,6 +102,7 @@ Layout make_layout(const qwen3_config &c) {
     L.o_pidx = take((size_t)c.max_seqs * MAX_PARTS * 4);
     L.o_wsml = take((size_t)c.max_seqs * Hq * MAX_SPLIT * 2 * 4);
     L.o_wso = take((size_t)c.max_seqs * Hq * MAX_SPLIT * D * 4);
+    L.o_counters = take((size_t)c.max_seqs * Hkv * 4);
     L.total = off;
     return L;
 }
@@ -174,10 +175,6 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
     uint32_t *err = c->at<uint32_t>(L.o_err);
     const bf16 *embed = c->at<bf16>(L.o_embed);
     const float2 *rope = c->at<float2>(L.o_rope);
-    auto proj = [&](const bf16 *X, int Kd, const uint8_t *W, int N, int epi, void *out) {
-        return decode ? launch_gemv(lc, X, R, Kd, (const bf16 *)W, N, epi, out)
-                      : launch_gemm(lc, X, R, Kd, (const bf16 *)W, N, epi, out);
-    };
     auto dump = [&](int l) -> cudaError_t {
         if (!c->dump) return cudaSuccess;
         return cudaMemcpyAsync(c->dump + (size_t)l * R * C, resid, (size_t)R * C * 4,
@@ -187,24 +184,52 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
     Q3_TRY(launch_embed_rmsnorm(lc, tokens, rows, embed, (const float *)(c->layer(0) + L.o_gin),
                                 resid, xn, C, k.vocab, k.rms_eps, err));
     Q3_TRY(dump(0));
+    const bool fused = decode && gemv_fused_supported(R, C) && gemv_fused_supported(R, Hq * D) &&
+                       gemv_fused_supported(R, I);
     for (int l = 0; l < k.n_layers; ++l) {
         const uint8_t *lw = c->layer(l);
-        if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, (const float *)(lw + L.o_gin), xn, C, k.rms_eps));
-        Q3_TRY(proj(xn, C, lw + L.o_wqkv, qkv_n, EPI_F32, qkv));
-        Q3_TRY(launch_qknorm_rope_kv(lc, qkv, rows, (const float *)(lw + L.o_gq),
-                                     (const float *)(lw + L.o_gk), rope, q, c->kcache(l),
-                                     c->vcache(l), Hq, Hkv, k.max_ctx, k.rms_eps, err));
-        if (decode)
-            Q3_TRY(launch_attn_decode(lc, q, c->kcache(l), c->vcache(l), rows, n_split, kps,
-                                      c->at<float>(L.o_wsml), c->at<float>(L.o_wso), attn, Hq, Hkv,
-                                      k.max_ctx));
-        else
-            Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens,
-                                       rows.slots, rows.B, max_len, attn, Hq, Hkv, k.max_ctx));
-        Q3_TRY(proj(attn, Hq * D, lw + L.o_wo, C, EPI_RESID_ADD, resid));
-        Q3_TRY(launch_rmsnorm(lc, resid, R, (const float *)(lw + L.o_gpost), xn, C, k.rms_eps));
-        Q3_TRY(proj(xn, C, lw + L.o_wgu, 2 * I, EPI_SWIGLU, act));
-        Q3_TRY(proj(act, I, lw + L.o_wdown, C, EPI_RESID_ADD, resid));
+        const float *g_in = (const float *)(lw + L.o_gin), *g_post = (const float *)(lw + L.o_gpost);
+        const float *g_q = (const float *)(lw + L.o_gq), *g_k = (const float *)(lw + L.o_gk);
+        const bf16 *w_qkv = (const bf16 *)(lw + L.o_wqkv), *w_o = (const bf16 *)(lw + L.o_wo);
+        const bf16 *w_gu = (const bf16 *)(lw + L.o_wgu), *w_down = (const bf16 *)(lw + L.o_wdown);
+        if (fused) {
+            // decode, few rows: 5 kernels per layer, the norms folded into the GEMV prologues.
+            // Each projection also asks L2 for its block of the next layer's weights (the next
+            // step's layer 0 after the last layer), so HBM streams ahead of the kernel chain.
+            const uint8_t *ahead = c->layer((l + 1) % k.n_layers);
+            Q3_TRY(launch_gemv_fused(lc, resid, R, C, w_qkv, qkv_n, EPI_F32, qkv, g_in, k.rms_eps, err,
+                                     (const bf16 *)(ahead + L.o_wqkv)));
+            Q3_TRY(launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
+                                            kps, c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
+                                            c->at<int>(L.o_counters), attn, Hq, Hkv, k.max_ctx, k.rms_eps, err));
+            Q3_TRY(launch_gemv_fused(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, resid, nullptr, 0.0f, err,
+                                     (const bf16 *)(ahead + L.o_wo)));
+            Q3_TRY(launch_gemv_fused(lc, resid, R, C, w_gu, 2 * I, EPI_SWIGLU, act, g_post, k.rms_eps, err,
+                                     (const bf16 *)(ahead + L.o_wgu)));
+            Q3_TRY(launch_gemv_fused(lc, act, R, I, w_down, C, EPI_RESID_ADD, resid, nullptr, 0.0f, err,
+                                     (const bf16 *)(ahead + L.o_wdown)));
+        } else if (decode) {
+            if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
+            Q3_TRY(launch_gemv(lc, xn, R, C, w_qkv, qkv_n, EPI_F32, qkv));
+            Q3_TRY(launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
+                                            kps, c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
+                                            c->at<int>(L.o_counters), attn, Hq, Hkv, k.max_ctx, k.rms_eps, err));
+            Q3_TRY(launch_gemv(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, resid));
+            Q3_TRY(launch_rmsnorm(lc, resid, R, g_post, xn, C, k.rms_eps));
+            Q3_TRY(launch_gemv(lc, xn, R, C, w_gu, 2 * I, EPI_SWIGLU, act));
+            Q3_TRY(launch_gemv(lc, act, R, I, w_down, C, EPI_RESID_ADD, resid));
+        } else {
+            if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
+            Q3_TRY(launch_gemm(lc, xn, R, C, w_qkv, qkv_n, EPI_F32, qkv));
+            Q3_TRY(launch_qknorm_rope_kv(lc, qkv, rows, g_q, g_k, rope, q, c->kcache(l), c->vcache(l), Hq, Hkv,
+                                         k.max_ctx, k.rms_eps, err));
+            Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots, rows.B,
+                                       max_len, attn, Hq, Hkv, k.max_ctx));
+            Q3_TRY(launch_gemm(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, resid));
+            Q3_TRY(launch_rmsnorm(lc, resid, R, g_post, xn, C, k.rms_eps));
+            Q3_TRY(launch_gemm(lc, xn, R, C, w_gu, 2 * I, EPI_SWIGLU, act));
+            Q3_TRY(launch_gemm(lc, act, R, I, w_down, C, EPI_RESID_ADD, resid));
+        }
         Q3_TRY(dump(l + 1));
     }
     bf16 *last = c->at<bf16>(L.o_last);
@@ -329,6 +354,7 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
                                cudaMemcpyHostToDevice, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_ctxlen, 0, (size_t)cfg->max_seqs * 4, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_err, 0, 16, st));
+        Q3_TRY(cudaMemsetAsync(c->arena + lay.o_counters, 0, (size_t)cfg->max_seqs * cfg->n_kv_heads * 4, st));
         Q3_TRY(cudaStreamSynchronize(st));
         return cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
     };
@@ -531,7 +557,10 @@ int qwen3_op_gemv(const void *x, int32_t M, int32_t K, const void *w, int32_t N,
         g_create_error = "qwen3_op_gemv: bad argument";
         return QWEN3_E_INVALID;
     }
-    cudaError_t e = launch_gemv(op_launch(stream), (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out);
+    const Launch lc = op_launch(stream);
+    cudaError_t e = gemv_fused_supported(M, K)
+                        ? launch_gemv_fused(lc, x, M, K, (const bf16 *)w, N, epi, out, nullptr, 0.0f, nullptr)
+                        : launch_gemv(lc, (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out);
     if (e != cudaSuccess) {
         g_create_error = std::string("qwen3_op_gemv: ") + cudaGetErrorString(e);
         return QWEN3_E_CUDA;
