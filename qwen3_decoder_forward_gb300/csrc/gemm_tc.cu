@@ -1,0 +1,269 @@
+// Prefill projection GEMM on the 5th-generation tensor cores: out[M,N] = A[M,K] . W[N,K]^T,
+// bf16 operands, fp32 accumulation in tensor memory.  Same contract and epilogues as the
+// mma.sync GEMM (QKV, o, gate_up + SwiGLU, down: "手写Qwen3-0.6B推理", Attention and MLP;
+// "第 3 章", 3.3/3.4 merged projections).
+//
+// One CTA per 128 x 256 output tile, 4 warps:
+//   warp 0, one thread : TMA producer -- A and W tiles (64 K-columns, 128-byte swizzle) into a
+//                        4-stage shared-memory ring, completion counted on mbarriers;
+//   warp 1, one thread : MMA issuer -- tcgen05.mma (M=128, N=256, K=16) per stage, the stage
+//                        released back to the producer by tcgen05.commit;
+//   warps 0-3          : epilogue -- tcgen05.ld of TMEM lanes 32w..32w+31 (one output row per
+//                        thread), then the fp32 / residual-add / SwiGLU store.
+// Rows of A beyond M are zero-filled by TMA and dropped on store (ragged token counts).
+// Every mbarrier wait is bounded: on timeout the CTA flags ERR_TIMEOUT, drains, frees its
+// tensor memory and returns.
+
+#include <cuda.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+namespace q3 {
+
+namespace {
+
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4, TC_THREADS = 128;
+constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;                  // 16 KB
+constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;                  // 32 KB
+constexpr int TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;        // 48 KB
+constexpr int TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 256 + 1024;  // ring + barriers + alignment
+constexpr uint32_t TC_TMEM_COLS = 256;
+
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with the 128-byte
+// swizzle: rows of 128 bytes (64 elements), 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)(16 >> 4) << 16;            // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: next 8-row group
+    d |= (uint64_t)1 << 46;                    // descriptor version
+    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *v) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmA,
+                                                           const __grid_constant__ CUtensorMap tmB, int M,
+                                                           int N, int K, void *out, uint32_t *err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + TC_STAGES * TC_STAGE_BYTES);
+    uint64_t *empty = full + TC_STAGES;
+    uint64_t *acc_full = empty + TC_STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * TC_BN, m0 = blockIdx.y * TC_BM;
+    const int KB = K / TC_BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TC_STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(TC_TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    pdl_wait();  // A is the previous kernel's output
+
+    bool ok = true;
+    int issued = 0;  // stages the producer filled (for the drain after a timeout)
+    if (warp == 0 && lane == 0) {
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % TC_STAGES;
+            if (kb >= TC_STAGES && !mbar_wait_bounded(&empty[s], ((kb / TC_STAGES) & 1) ^ 1, err)) {
+                ok = false;
+                break;
+            }
+            uint8_t *sa = smem + s * TC_STAGE_BYTES;
+            mbar_expect_tx(&full[s], TC_STAGE_BYTES);
+            tma_load_2d(sa, &tmA, kb * TC_BK, m0, &full[s]);
+            tma_load_2d(sa + TC_A_BYTES, &tmB, kb * TC_BK, n0, &full[s]);
+            issued = kb + 1;
+        }
+        if (!ok) {  // let the copies in flight land before anyone leaves
+            for (int kb = (issued > TC_STAGES ? issued - TC_STAGES : 0); kb < issued; ++kb)
+                mbar_wait_bounded(&full[kb % TC_STAGES], (kb / TC_STAGES) & 1, nullptr);
+        }
+    } else if (warp == 1 && lane == 0) {
+        constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % TC_STAGES;
+            if (!mbar_wait_bounded(&full[s], (kb / TC_STAGES) & 1, err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_addr(smem + s * TC_STAGE_BYTES), sb = sa + TC_A_BYTES;
+#pragma unroll
+            for (int k = 0; k < TC_BK / 16; ++k)  // 16 elements = 32 bytes further along K
+                tc_mma(tmem, sdesc_k_sw128(sa + k * 32), sdesc_k_sw128(sb + k * 32), idesc, (kb | k) != 0);
+            tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(acc_full);
+    }
+    __syncwarp();
+
+    // Epilogue: thread t of warp w owns output row m0 + 32w + t (TMEM lane 32w + t).
+    // warp-uniform: tcgen05.ld must be executed by all 32 lanes together
+    const bool have = __all_sync(0xffffffffu, mbar_wait_bounded(acc_full, 0, err));
+    tc_fence_after();
+    if (have) {
+        const int row = m0 + warp * 32 + lane;
+        const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+        for (int c = 0; c < TC_BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(t_row + c * 32, v);
+            if (row < M) {
+                const int col = n0 + c * 32;
+                if (EPI == EPI_F32) {
+                    float4 *dst = reinterpret_cast<float4 *>((float *)out + (size_t)row * N + col);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                } else if (EPI == EPI_RESID_ADD) {
+                    float4 *dst = reinterpret_cast<float4 *>((float *)out + (size_t)row * N + col);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float4 r = dst[j];
+                        r.x += __uint_as_float(v[4 * j]);
+                        r.y += __uint_as_float(v[4 * j + 1]);
+                        r.z += __uint_as_float(v[4 * j + 2]);
+                        r.w += __uint_as_float(v[4 * j + 3]);
+                        dst[j] = r;
+                    }
+                } else {  // columns (2j, 2j+1) are (gate_j, up_j)
+                    uint32_t o[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float a0 = silu(__uint_as_float(v[4 * j])) * __uint_as_float(v[4 * j + 1]);
+                        const float a1 = silu(__uint_as_float(v[4 * j + 2])) * __uint_as_float(v[4 * j + 3]);
+                        o[j] = pack_bf16x2(a0, a1);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>((bf16 *)out + (size_t)row * (N / 2) + col / 2);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+        }
+    }
+    pdl_trigger();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D map of a row-major bf16 matrix [rows, cols] read as boxes of 64 columns x box_rows rows.
+bool make_map(CUtensorMap *map, const bf16 *base, int rows, int cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16 *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t run_tc(const Launch &lc, const CUtensorMap &ma, const CUtensorMap &mb, int M, int N, int K, void *out,
+                   uint32_t *err) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    if (e != cudaSuccess) return e;
+    return launch(lc, k_gemm_tc<EPI>, dim3(N / TC_BN, (M + TC_BM - 1) / TC_BM), dim3(TC_THREADS), TC_SMEM, ma, mb,
+                  M, N, K, out, err);
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int M, int K, int N) {
+    return M >= 1 && K >= TC_BK && K % TC_BK == 0 && N >= TC_BN && N % TC_BN == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, int epi,
+                           void *out, uint32_t *err) {
+    if (!gemm_tc_supported(M, K, N)) return cudaErrorInvalidValue;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(W)) & 15) return cudaErrorInvalidValue;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A, M, K, TC_BM) || !make_map(&mb, W, N, K, TC_BN)) return cudaErrorInvalidValue;
+    switch (epi) {
+        case EPI_F32: return run_tc<EPI_F32>(lc, ma, mb, M, N, K, out, err);
+        case EPI_RESID_ADD: return run_tc<EPI_RESID_ADD>(lc, ma, mb, M, N, K, out, err);
+        case EPI_SWIGLU: return run_tc<EPI_SWIGLU>(lc, ma, mb, M, N, K, out, err);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace q3

@@ -84,6 +84,11 @@ enum Epilogue : int {
 cudaError_t launch_gemm(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N,
                         int epi, void *out);
 
+// --- gemm_tc.cu (prefill on tcgen05 tensor cores; K % 64 == 0, N % 256 == 0) -------------
+bool gemm_tc_supported(int M, int K, int N);
+cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, int epi,
+                           void *out, uint32_t *err);
+
 // --- gemv.cu (decode; same contract as launch_gemm for small M) ---------------------------
 cudaError_t launch_gemv(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N,
                         int epi, void *out);

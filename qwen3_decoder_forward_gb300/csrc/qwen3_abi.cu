@@ -219,16 +219,21 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
             Q3_TRY(launch_gemv(lc, xn, R, C, w_gu, 2 * I, EPI_SWIGLU, act));
             Q3_TRY(launch_gemv(lc, act, R, I, w_down, C, EPI_RESID_ADD, resid));
         } else {
+            // prefill: tensor-core GEMMs (tcgen05, TMA) where the shape allows, else mma.sync
+            auto gemm = [&](const bf16 *X, int Kd, const bf16 *W, int N, int epi, void *out) {
+                return gemm_tc_supported(R, Kd, N) ? launch_gemm_tc(lc, X, R, Kd, W, N, epi, out, err)
+                                                   : launch_gemm(lc, X, R, Kd, W, N, epi, out);
+            };
             if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
-            Q3_TRY(launch_gemm(lc, xn, R, C, w_qkv, qkv_n, EPI_F32, qkv));
+            Q3_TRY(gemm(xn, C, w_qkv, qkv_n, EPI_F32, qkv));
             Q3_TRY(launch_qknorm_rope_kv(lc, qkv, rows, g_q, g_k, rope, q, c->kcache(l), c->vcache(l), Hq, Hkv,
                                          k.max_ctx, k.rms_eps, err));
             Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots, rows.B,
                                        max_len, attn, Hq, Hkv, k.max_ctx));
-            Q3_TRY(launch_gemm(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, resid));
+            Q3_TRY(gemm(attn, Hq * D, w_o, C, EPI_RESID_ADD, resid));
             Q3_TRY(launch_rmsnorm(lc, resid, R, g_post, xn, C, k.rms_eps));
-            Q3_TRY(launch_gemm(lc, xn, R, C, w_gu, 2 * I, EPI_SWIGLU, act));
-            Q3_TRY(launch_gemm(lc, act, R, I, w_down, C, EPI_RESID_ADD, resid));
+            Q3_TRY(gemm(xn, C, w_gu, 2 * I, EPI_SWIGLU, act));
+            Q3_TRY(gemm(act, I, w_down, C, EPI_RESID_ADD, resid));
         }
         Q3_TRY(dump(l + 1));
     }
@@ -575,7 +580,10 @@ int qwen3_op_gemm(const void *x, int32_t M, int32_t K, const void *w, int32_t N,
         g_create_error = "qwen3_op_gemm: bad argument";
         return QWEN3_E_INVALID;
     }
-    cudaError_t e = launch_gemm(op_launch(stream), (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out);
+    const Launch lc = op_launch(stream);
+    cudaError_t e = gemm_tc_supported(M, K, N)
+                        ? launch_gemm_tc(lc, (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out, nullptr)
+                        : launch_gemm(lc, (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out);
     if (e != cudaSuccess) {
         g_create_error = std::string("qwen3_op_gemm: ") + cudaGetErrorString(e);
         return QWEN3_E_CUDA;

@@ -1,0 +1,89 @@
+"""Single kernels through the C ABI against plain PyTorch fp32 on the GPU.
+
+The projections (prefill GEMM, decode GEMV) are checked on ragged row counts and every
+epilogue; the lm_head + argmax on its logits and its choice.  Operands are bf16; the
+reference widens them to fp32 and multiplies in fp32, so only summation order differs.
+"""
+
+import pytest
+import torch
+import torch.nn.functional as F
+
+import gpu_common as gc
+from qwen3_decoder_forward_gb300 import binding
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand(shape, seed, scale=1.0):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return (torch.randn(shape, generator=g) * scale).to(torch.bfloat16).cuda()
+
+
+def _run(op, M, K, N, epi, seed):
+    x = _rand((M, K), seed)
+    w = _rand((N, K), seed + 1, 0.02)
+    ref = x.float() @ w.float().T
+    stream = torch.cuda.current_stream().cuda_stream
+    if epi == binding.QWEN3_EPI_F32:
+        out = torch.full((M, N), float("nan"), device="cuda")
+        op(x.data_ptr(), M, K, w.data_ptr(), N, epi, out.data_ptr(), stream)
+        return out, ref
+    if epi == binding.QWEN3_EPI_RESID_ADD:
+        base = _rand((M, N), seed + 2).float()
+        out = base.clone()
+        op(x.data_ptr(), M, K, w.data_ptr(), N, epi, out.data_ptr(), stream)
+        return out, base + ref
+    out = torch.full((M, N // 2), float("nan"), dtype=torch.bfloat16, device="cuda")
+    op(x.data_ptr(), M, K, w.data_ptr(), N, epi, out.data_ptr(), stream)
+    return out.float(), F.silu(ref[:, 0::2]) * ref[:, 1::2]
+
+
+EPIS = [binding.QWEN3_EPI_F32, binding.QWEN3_EPI_RESID_ADD, binding.QWEN3_EPI_SWIGLU]
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1024, 256), (77, 1024, 4096), (128, 2048, 1024), (300, 3072, 1024),
+                                   (1000, 1024, 6144), (4099, 1024, 512)])
+@pytest.mark.parametrize("epi", EPIS)
+def test_prefill_gemm_vs_torch(M, K, N, epi):
+    gc.ensure_library()
+    out, ref = _run(binding.qwen3_op_gemm, M, K, N, epi, seed=M + K + N + epi)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    tol = 4e-3 if epi == binding.QWEN3_EPI_SWIGLU else 1e-5
+    assert gc.rel_l2(out.cpu().numpy(), ref.cpu().numpy()) <= tol
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 17, 32])
+@pytest.mark.parametrize("K,N", [(1024, 4096), (2048, 1024), (3072, 1024), (1024, 6144)])
+@pytest.mark.parametrize("epi", EPIS)
+def test_decode_gemv_vs_torch(M, K, N, epi):
+    gc.ensure_library()
+    out, ref = _run(binding.qwen3_op_gemv, M, K, N, epi, seed=7 * M + K + N + epi)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    tol = 4e-3 if epi == binding.QWEN3_EPI_SWIGLU else 1e-5
+    assert gc.rel_l2(out.cpu().numpy(), ref.cpu().numpy()) <= tol
+
+
+@pytest.mark.parametrize("B,V", [(1, 151936), (7, 4096), (32, 50021)])
+def test_lmhead_argmax_vs_torch(B, V):
+    gc.ensure_library()
+    C = 1024
+    x = _rand((B, C), B + V)
+    e = _rand((V, C), B + V + 1, 0.02)
+    ws_bytes = binding.qwen3_op_lmhead_workspace_bytes(B)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    tok = torch.empty(B, dtype=torch.int32, device="cuda")
+    logits = torch.empty(B, V, device="cuda")
+    binding.qwen3_op_lmhead_argmax(x.data_ptr(), B, C, e.data_ptr(), V, logits.data_ptr(), tok.data_ptr(),
+                                   ws.data_ptr(), ws_bytes, torch.cuda.current_stream().cuda_stream)
+    ref = x.float() @ e.float().T
+    torch.cuda.synchronize()
+    assert gc.rel_l2(logits.cpu().numpy(), ref.cpu().numpy()) <= 1e-5
+    # the choice is exactly the argmax of the kernel's own logits (first index on ties) ...
+    assert torch.equal(tok.long(), torch.argmax(logits, dim=1))
+    # ... and the reference's wherever its top-2 gap is clear
+    top2 = torch.topk(ref, 2, dim=1).values
+    clear = (top2[:, 0] - top2[:, 1]) > 1e-3
+    assert torch.equal(tok.long()[clear], torch.argmax(ref, dim=1)[clear])
