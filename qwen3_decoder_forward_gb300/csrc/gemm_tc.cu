@@ -3,7 +3,7 @@
 // mma.sync GEMM (QKV, o, gate_up + SwiGLU, down: "手写Qwen3-0.6B推理", Attention and MLP;
 // "第 3 章", 3.3/3.4 merged projections).
 //
-// One CTA per 128 x 256 output tile, 4 warps:
+// Tiles of 128 x 256 outputs, 4 roles:
 //   warp 0, one thread : TMA producer -- A and W tiles (64 K-columns, 128-byte swizzle) into a
 //                        4-stage shared-memory ring, completion counted on mbarriers;
 //   warp 1, one thread : MMA issuer -- tcgen05.mma (M=128, N=256, K=16) per stage, the stage
@@ -83,128 +83,242 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *v) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Persistent form: each CTA walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... (row-block
+// major, so CTAs running together share A rows).  Two TMEM accumulators of 256 columns: the
+// MMA thread fills one while the epilogue warps drain the other.
+//   warp 0 (1 thread) TMA producer; warp 1 (1 thread) MMA issuer and TMEM owner;
+//   warps 2-5 epilogue, warp w reading TMEM lanes 32*(w%4) .. 32*(w%4)+31.
+constexpr int TCP_THREADS = 192;
+constexpr uint32_t TCP_TMEM_COLS = 512;
+
+struct EpiArgs {
+    void *out;
+    // EPI_QKV: per-head RMSNorm + rotate-half RoPE of q and k, V as projected; q to q_out
+    // [rows, Hq, 128], k and v into the layer's cache at (row_slot, row_pos).
+    const int32_t *row_slot, *row_pos;
+    const float *q_gain, *k_gain;
+    const float2 *rope;
+    bf16 *q_out, *k_layer, *v_layer;
+    int Hq, Hkv, max_ctx;
+    float eps;
+};
+
+__device__ __forceinline__ void store_chunk(int EPI_, const uint32_t *v, int row, int col, int N, void *out) {
+    if (EPI_ == EPI_F32) {
+        float4 *dst = reinterpret_cast<float4 *>((float *)out + (size_t)row * N + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                                 __uint_as_float(v[4 * j + 3]));
+    } else if (EPI_ == EPI_RESID_ADD) {
+        float4 *dst = reinterpret_cast<float4 *>((float *)out + (size_t)row * N + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 r = dst[j];
+            r.x += __uint_as_float(v[4 * j]);
+            r.y += __uint_as_float(v[4 * j + 1]);
+            r.z += __uint_as_float(v[4 * j + 2]);
+            r.w += __uint_as_float(v[4 * j + 3]);
+            dst[j] = r;
+        }
+    } else {  // SwiGLU: columns (2j, 2j+1) are (gate_j, up_j)
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float a0 = silu(__uint_as_float(v[4 * j])) * __uint_as_float(v[4 * j + 1]);
+            const float a1 = silu(__uint_as_float(v[4 * j + 2])) * __uint_as_float(v[4 * j + 3]);
+            o[j] = pack_bf16x2(a0, a1);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>((bf16 *)out + (size_t)row * (N / 2) + col / 2);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// Stores 32 bf16 values (already in fp32 registers) at dst.
+__device__ __forceinline__ void store_bf16x32(bf16 *dst, const float *x) {
+    uint32_t o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+}
+
 template <int EPI>
-__global__ void __launch_bounds__(TC_THREADS, 1) k_gemm_tc(const __grid_constant__ CUtensorMap tmA,
-                                                           const __grid_constant__ CUtensorMap tmB, int M,
-                                                           int N, int K, void *out, uint32_t *err) {
+__global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_constant__ CUtensorMap tmA,
+                                                             const __grid_constant__ CUtensorMap tmB, int M, int N,
+                                                             int K, EpiArgs ea, uint32_t *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + TC_STAGES * TC_STAGE_BYTES);
     uint64_t *empty = full + TC_STAGES;
-    uint64_t *acc_full = empty + TC_STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    uint64_t *tm_full = empty + TC_STAGES;  // [2]
+    uint64_t *tm_empty = tm_full + 2;       // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tm_empty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * TC_BN, m0 = blockIdx.y * TC_BM;
     const int KB = K / TC_BK;
+    const int tiles_n = N / TC_BN, tiles = ((M + TC_BM - 1) / TC_BM) * tiles_n;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < TC_STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(acc_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tm_full[a], 1);
+            mbar_init(&tm_empty[a], 4);  // one arrival per epilogue warp
+        }
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(TC_TMEM_COLS));
+                     "r"(TCP_TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
     pdl_wait();  // A is the previous kernel's output
 
-    bool ok = true;
-    int issued = 0;  // stages the producer filled (for the drain after a timeout)
-    if (warp == 0 && lane == 0) {
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % TC_STAGES;
-            if (kb >= TC_STAGES && !mbar_wait_bounded(&empty[s], ((kb / TC_STAGES) & 1) ^ 1, err)) {
-                ok = false;
-                break;
-            }
-            uint8_t *sa = smem + s * TC_STAGE_BYTES;
-            mbar_expect_tx(&full[s], TC_STAGE_BYTES);
-            tma_load_2d(sa, &tmA, kb * TC_BK, m0, &full[s]);
-            tma_load_2d(sa + TC_A_BYTES, &tmB, kb * TC_BK, n0, &full[s]);
-            issued = kb + 1;
-        }
-        if (!ok) {  // let the copies in flight land before anyone leaves
-            for (int kb = (issued > TC_STAGES ? issued - TC_STAGES : 0); kb < issued; ++kb)
-                mbar_wait_bounded(&full[kb % TC_STAGES], (kb / TC_STAGES) & 1, nullptr);
-        }
-    } else if (warp == 1 && lane == 0) {
-        constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
-        for (int kb = 0; kb < KB; ++kb) {
-            const int s = kb % TC_STAGES;
-            if (!mbar_wait_bounded(&full[s], (kb / TC_STAGES) & 1, err)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t sa = smem_addr(smem + s * TC_STAGE_BYTES), sb = sa + TC_A_BYTES;
-#pragma unroll
-            for (int k = 0; k < TC_BK / 16; ++k)  // 16 elements = 32 bytes further along K
-                tc_mma(tmem, sdesc_k_sw128(sa + k * 32), sdesc_k_sw128(sb + k * 32), idesc, (kb | k) != 0);
-            tc_commit(&empty[s]);
-        }
-        if (ok) tc_commit(acc_full);
-    }
-    __syncwarp();
-
-    // Epilogue: thread t of warp w owns output row m0 + 32w + t (TMEM lane 32w + t).
-    // warp-uniform: tcgen05.ld must be executed by all 32 lanes together
-    const bool have = __all_sync(0xffffffffu, mbar_wait_bounded(acc_full, 0, err));
-    tc_fence_after();
-    if (have) {
-        const int row = m0 + warp * 32 + lane;
-        const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll 1
-        for (int c = 0; c < TC_BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(t_row + c * 32, v);
-            if (row < M) {
-                const int col = n0 + c * 32;
-                if (EPI == EPI_F32) {
-                    float4 *dst = reinterpret_cast<float4 *>((float *)out + (size_t)row * N + col);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                } else if (EPI == EPI_RESID_ADD) {
-                    float4 *dst = reinterpret_cast<float4 *>((float *)out + (size_t)row * N + col);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float4 r = dst[j];
-                        r.x += __uint_as_float(v[4 * j]);
-                        r.y += __uint_as_float(v[4 * j + 1]);
-                        r.z += __uint_as_float(v[4 * j + 2]);
-                        r.w += __uint_as_float(v[4 * j + 3]);
-                        dst[j] = r;
+    if (warp == 0) {
+        if (lane == 0) {
+            int it = 0;  // k-blocks issued so far (ring position)
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int m0 = (t / tiles_n) * TC_BM, n0 = (t % tiles_n) * TC_BN;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % TC_STAGES;
+                    if (it >= TC_STAGES && !mbar_wait_bounded(&empty[s], ((it / TC_STAGES) & 1) ^ 1, err)) {
+                        ok = false;
+                        break;
                     }
-                } else {  // columns (2j, 2j+1) are (gate_j, up_j)
-                    uint32_t o[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float a0 = silu(__uint_as_float(v[4 * j])) * __uint_as_float(v[4 * j + 1]);
-                        const float a1 = silu(__uint_as_float(v[4 * j + 2])) * __uint_as_float(v[4 * j + 3]);
-                        o[j] = pack_bf16x2(a0, a1);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>((bf16 *)out + (size_t)row * (N / 2) + col / 2);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    uint8_t *sa = smem + s * TC_STAGE_BYTES;
+                    mbar_expect_tx(&full[s], TC_STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, kb * TC_BK, m0, &full[s]);
+                    tma_load_2d(sa + TC_A_BYTES, &tmB, kb * TC_BK, n0, &full[s]);
                 }
             }
+            if (!ok)  // let the copies in flight land before the CTA can leave
+                for (int j = (it > TC_STAGES ? it - TC_STAGES : 0); j < it; ++j)
+                    mbar_wait_bounded(&full[j % TC_STAGES], (j / TC_STAGES) & 1, nullptr);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(TC_BM, TC_BN);
+            int it = 0, local = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
+                const int a = local & 1;
+                if (local >= 2 && !mbar_wait_bounded(&tm_empty[a], ((local >> 1) & 1) ^ 1, err)) break;
+                tc_fence_after();
+                const uint32_t acc = tmem + a * TC_BN;
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % TC_STAGES;
+                    if (!mbar_wait_bounded(&full[s], (it / TC_STAGES) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(smem + s * TC_STAGE_BYTES), sb = sa + TC_A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < TC_BK / 16; ++k)
+                        tc_mma(acc, sdesc_k_sw128(sa + k * 32), sdesc_k_sw128(sb + k * 32), idesc, (kb | k) != 0);
+                    tc_commit(&empty[s]);
+                }
+                if (ok) tc_commit(&tm_full[a]);
+            }
+        }
+    } else {
+        // epilogue warps 2..5
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        int local = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
+            const int a = local & 1;
+            const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&tm_full[a], (local >> 1) & 1, err));
+            if (!ready) break;
+            tc_fence_after();
+            const int m0 = (t / tiles_n) * TC_BM, n0 = (t % tiles_n) * TC_BN;
+            const int row = m0 + q * 32 + lane;
+            const uint32_t t_row = tmem + a * TC_BN + ((uint32_t)(q * 32) << 16);
+            if (EPI != EPI_QKV) {
+#pragma unroll 1
+                for (int c = 0; c < TC_BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(t_row + c * 32, v);
+                    if (row < M) store_chunk(EPI, v, row, n0 + c * 32, N, ea.out);
+                }
+            } else {
+                // two heads of 128 columns per tile: head index within [q | k | v]
+                const int slot = row < M ? ea.row_slot[row] : 0;
+                const int pos = row < M ? ea.row_pos[row] : 0;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int head = n0 / 128 + hh;
+                    const uint32_t th = t_row + hh * 128;
+                    const bool is_v = head >= ea.Hq + ea.Hkv;
+                    float inv = 1.0f;
+                    if (!is_v) {  // pass 1: sum of squares over the head's 128 columns
+                        float ss = 0.0f;
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t v[32];
+                            tmem_ld32(th + c * 32, v);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) ss += __uint_as_float(v[j]) * __uint_as_float(v[j]);
+                        }
+                        inv = rsqrtf(ss * (1.0f / 128.0f) + ea.eps);
+                    }
+                    const float *gain = head < ea.Hq ? ea.q_gain : ea.k_gain;
+                    bf16 *dst;
+                    if (head < ea.Hq)
+                        dst = ea.q_out + ((size_t)row * ea.Hq + head) * 128;
+                    else {
+                        const int g = is_v ? head - ea.Hq - ea.Hkv : head - ea.Hq;
+                        dst = (is_v ? ea.v_layer : ea.k_layer) + (((size_t)slot * ea.Hkv + g) * ea.max_ctx + pos) * 128;
+                    }
+                    // pass 2: elements i (chunk c) and i+64 (chunk c+2) rotate together
+#pragma unroll 1
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t lo[32], hi[32];
+                        tmem_ld32(th + c * 32, lo);
+                        tmem_ld32(th + (c + 2) * 32, hi);
+                        if (row < M && pos < ea.max_ctx) {
+                            float xl[32], xh[32];
+                            if (is_v) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    xl[j] = __uint_as_float(lo[j]);
+                                    xh[j] = __uint_as_float(hi[j]);
+                                }
+                            } else {
+                                const float2 *cs = ea.rope + (size_t)pos * 64 + c * 32;
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    const float a0 = __uint_as_float(lo[j]) * inv * gain[c * 32 + j];
+                                    const float b0 = __uint_as_float(hi[j]) * inv * gain[64 + c * 32 + j];
+                                    const float2 r = cs[j];
+                                    xl[j] = a0 * r.x - b0 * r.y;  // x_i cos - x_{i+64} sin
+                                    xh[j] = b0 * r.x + a0 * r.y;  // x_{i+64} cos + x_i sin
+                                }
+                            }
+                            store_bf16x32(dst + c * 32, xl);
+                            store_bf16x32(dst + 64 + c * 32, xh);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&tm_empty[a])) : "memory");
         }
     }
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
     if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TCP_TMEM_COLS));
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -238,12 +352,13 @@ bool make_map(CUtensorMap *map, const bf16 *base, int rows, int cols, int box_ro
 }
 
 template <int EPI>
-cudaError_t run_tc(const Launch &lc, const CUtensorMap &ma, const CUtensorMap &mb, int M, int N, int K, void *out,
-                   uint32_t *err) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+cudaError_t run_tcp(const Launch &lc, const CUtensorMap &ma, const CUtensorMap &mb, int M, int N, int K,
+                    const EpiArgs &ea, uint32_t *err) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tcp<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
     if (e != cudaSuccess) return e;
-    return launch(lc, k_gemm_tc<EPI>, dim3(N / TC_BN, (M + TC_BM - 1) / TC_BM), dim3(TC_THREADS), TC_SMEM, ma, mb,
-                  M, N, K, out, err);
+    const int tiles = ((M + TC_BM - 1) / TC_BM) * (N / TC_BN);
+    const int grid = tiles < lc.num_sms ? tiles : lc.num_sms;
+    return launch(lc, k_gemm_tcp<EPI>, dim3(grid), dim3(TCP_THREADS), TC_SMEM, ma, mb, M, N, K, ea, err);
 }
 
 }  // namespace
@@ -254,16 +369,41 @@ bool gemm_tc_supported(int M, int K, int N) {
 
 cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, int epi,
                            void *out, uint32_t *err) {
-    if (!gemm_tc_supported(M, K, N)) return cudaErrorInvalidValue;
+    if (!gemm_tc_supported(M, K, N) || epi == EPI_QKV) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(W)) & 15) return cudaErrorInvalidValue;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, M, K, TC_BM) || !make_map(&mb, W, N, K, TC_BN)) return cudaErrorInvalidValue;
+    EpiArgs ea = {};
+    ea.out = out;
     switch (epi) {
-        case EPI_F32: return run_tc<EPI_F32>(lc, ma, mb, M, N, K, out, err);
-        case EPI_RESID_ADD: return run_tc<EPI_RESID_ADD>(lc, ma, mb, M, N, K, out, err);
-        case EPI_SWIGLU: return run_tc<EPI_SWIGLU>(lc, ma, mb, M, N, K, out, err);
+        case EPI_F32: return run_tcp<EPI_F32>(lc, ma, mb, M, N, K, ea, err);
+        case EPI_RESID_ADD: return run_tcp<EPI_RESID_ADD>(lc, ma, mb, M, N, K, ea, err);
+        case EPI_SWIGLU: return run_tcp<EPI_SWIGLU>(lc, ma, mb, M, N, K, ea, err);
     }
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, const Rows &r,
+                               const float *q_gain, const float *k_gain, const float2 *rope, bf16 *q_out,
+                               bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv, int max_ctx, float eps,
+                               uint32_t *err) {
+    if (!gemm_tc_supported(M, K, N) || N != (Hq + 2 * Hkv) * 128) return cudaErrorInvalidValue;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A, M, K, TC_BM) || !make_map(&mb, W, N, K, TC_BN)) return cudaErrorInvalidValue;
+    EpiArgs ea = {};
+    ea.row_slot = r.row_slot;
+    ea.row_pos = r.row_pos;
+    ea.q_gain = q_gain;
+    ea.k_gain = k_gain;
+    ea.rope = rope;
+    ea.q_out = q_out;
+    ea.k_layer = k_layer;
+    ea.v_layer = v_layer;
+    ea.Hq = Hq;
+    ea.Hkv = Hkv;
+    ea.max_ctx = max_ctx;
+    ea.eps = eps;
+    return run_tcp<EPI_QKV>(lc, ma, mb, M, N, K, ea, err);
 }
 
 }  // namespace q3

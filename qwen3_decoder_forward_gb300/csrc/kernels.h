@@ -80,6 +80,7 @@ enum Epilogue : int {
     EPI_F32 = 0,         // out fp32 [M, N]
     EPI_RESID_ADD = 1,   // out fp32 [M, N] += result
     EPI_SWIGLU = 2,      // W rows interleaved (gate_j, up_j): out bf16 [M, N/2] = silu(g)*u
+    EPI_QKV = 3,         // QKV projection straight into q (normed, rotated) and the KV cache
 };
 cudaError_t launch_gemm(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N,
                         int epi, void *out);
@@ -88,6 +89,11 @@ cudaError_t launch_gemm(const Launch &lc, const bf16 *A, int M, int K, const bf1
 bool gemm_tc_supported(int M, int K, int N);
 cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, int epi,
                            void *out, uint32_t *err);
+// QKV projection with the epilogue of launch_qknorm_rope_kv fused in (no fp32 qkv buffer).
+cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, const Rows &r,
+                               const float *q_gain, const float *k_gain, const float2 *rope, bf16 *q_out,
+                               bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv, int max_ctx, float eps,
+                               uint32_t *err);
 
 // --- gemv.cu (decode; same contract as launch_gemm for small M) ---------------------------
 cudaError_t launch_gemv(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N,

@@ -225,9 +225,14 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
                                                    : launch_gemm(lc, X, R, Kd, W, N, epi, out);
             };
             if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
-            Q3_TRY(gemm(xn, C, w_qkv, qkv_n, EPI_F32, qkv));
-            Q3_TRY(launch_qknorm_rope_kv(lc, qkv, rows, g_q, g_k, rope, q, c->kcache(l), c->vcache(l), Hq, Hkv,
-                                         k.max_ctx, k.rms_eps, err));
+            if (gemm_tc_supported(R, C, qkv_n)) {  // QK-norm, RoPE and the KV write in the GEMM epilogue
+                Q3_TRY(launch_gemm_tc_qkv(lc, xn, R, C, w_qkv, qkv_n, rows, g_q, g_k, rope, q, c->kcache(l),
+                                          c->vcache(l), Hq, Hkv, k.max_ctx, k.rms_eps, err));
+            } else {
+                Q3_TRY(gemm(xn, C, w_qkv, qkv_n, EPI_F32, qkv));
+                Q3_TRY(launch_qknorm_rope_kv(lc, qkv, rows, g_q, g_k, rope, q, c->kcache(l), c->vcache(l), Hq,
+                                             Hkv, k.max_ctx, k.rms_eps, err));
+            }
             Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots, rows.B,
                                        max_len, attn, Hq, Hkv, k.max_ctx));
             Q3_TRY(gemm(attn, Hq * D, w_o, C, EPI_RESID_ADD, resid));
