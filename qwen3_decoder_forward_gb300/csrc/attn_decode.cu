@@ -193,25 +193,29 @@ __global__ void __launch_bounds__(D) k_attn_decode_combine(const float *__restri
 // pair, incremented after a memory fence and reset by that CTA): no second kernel and no
 // waiting on other CTAs.
 
-constexpr int CHUNK = 32;    // keys per stage
 constexpr int STAGES = 4;
-constexpr int STAGE_BYTES = CHUNK * D * 2 * 2;  // K and V rows of one chunk (16 KB)
+// keys per ring stage for NW warps: at least 32, and one step of 4 keys per warp
+template <int NW> struct Ring {
+    static constexpr int CHUNK = NW * 4 > 32 ? NW * 4 : 32;
+    static constexpr int STAGE_BYTES = CHUNK * D * 2 * 2;  // K and V rows of one chunk
+};
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16(x)); }
 
-template <int G>
-__global__ void __launch_bounds__(WARPS * 32) k_attn_decode_fused(
+template <int G, int NW>
+__global__ void __launch_bounds__(NW * 32) k_attn_decode_fused(
     const float *__restrict__ qkv, Rows r, const float *__restrict__ q_gain,
     const float *__restrict__ k_gain, const float2 *__restrict__ rope, bf16 *__restrict__ k_layer,
     bf16 *__restrict__ v_layer, int kps, float *__restrict__ ws_ml, float *__restrict__ ws_o,
     int *__restrict__ counters, bf16 *__restrict__ out, int Hq, int Hkv, int max_ctx, float eps,
     float scale_log2, uint32_t *err) {
     extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int CHUNK = Ring<NW>::CHUNK, STAGE_BYTES = Ring<NW>::STAGE_BYTES;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);              // [STAGES]
     uint8_t *ring = smem + 128;                                        // [STAGES][K | V]
     float *s_new = reinterpret_cast<float *>(ring + STAGES * STAGE_BYTES);  // new K, new V [2][D]
-    __shared__ float red_ml[WARPS][G][2];
-    __shared__ float red_o[WARPS][G][D];
+    __shared__ float red_ml[NW][G][2];
+    __shared__ float red_o[NW][G][D];
     __shared__ int s_last;
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -357,8 +361,8 @@ __global__ void __launch_bounds__(WARPS * 32) k_attn_decode_fused(
         const uint8_t *vs = ks + CHUNK * D * 2;
         const int n = min(CHUNK, cache_end - (k_begin + c * CHUNK));
 #pragma unroll
-        for (int it = 0; it < CHUNK / (WARPS * 4); ++it) {
-            const int jj = it * WARPS * 4 + warp * 4 + kg;
+        for (int it = 0; it < CHUNK / (NW * 4); ++it) {
+            const int jj = it * NW * 4 + warp * 4 + kg;
             const bool valid = jj < n;
             const int js = valid ? jj : 0;
             const uint4 *kp = reinterpret_cast<const uint4 *>(ks + (size_t)js * D * 2 + sub * 32);
@@ -419,14 +423,14 @@ __global__ void __launch_bounds__(WARPS * 32) k_attn_decode_fused(
         }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < G * D; idx += WARPS * 32) {
+    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
         const int gi = idx / D, d = idx % D;
         float mx = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) mx = fmaxf(mx, red_ml[w][gi][0]);
+        for (int w = 0; w < NW; ++w) mx = fmaxf(mx, red_ml[w][gi][0]);
         float lsum = 0.0f, o = 0.0f;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const float c = mx == -INFINITY ? 0.0f : exp2f(red_ml[w][gi][0] - mx);
             lsum += red_ml[w][gi][1] * c;
             o += red_o[w][gi][d] * c;
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(WARPS * 32) k_attn_decode_fused(
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    for (int idx = threadIdx.x; idx < G * D; idx += WARPS * 32) {
+    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
         const int gi = idx / D, d = idx % D;
         const int h = g * G + gi;
         const size_t base = ((size_t)b * Hq + h) * n_split;
@@ -469,17 +473,17 @@ __global__ void __launch_bounds__(WARPS * 32) k_attn_decode_fused(
     if (threadIdx.x == 0) counters[b * Hkv + g] = 0;
 }
 
-template <int G>
+template <int G, int NW>
 cudaError_t run_fused(const Launch &lc, const float *qkv, const Rows &r, const float *q_gain,
                       const float *k_gain, const float2 *rope, bf16 *k_layer, bf16 *v_layer, int n_split,
                       int kps, float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq, int Hkv,
                       int max_ctx, float eps, uint32_t *err) {
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-    const size_t smem = 128 + (size_t)STAGES * STAGE_BYTES + 2 * D * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_fused<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = 128 + (size_t)STAGES * Ring<NW>::STAGE_BYTES + 2 * D * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_fused<G, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    return launch(lc, k_attn_decode_fused<G>, dim3(n_split, Hkv, r.B), dim3(WARPS * 32), smem, qkv, r, q_gain,
+    return launch(lc, k_attn_decode_fused<G, NW>, dim3(n_split, Hkv, r.B), dim3(NW * 32), smem, qkv, r, q_gain,
                   k_gain, rope, k_layer, v_layer, kps, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps,
                   scale_log2, err);
 }
@@ -516,12 +520,18 @@ cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const R
                                      bf16 *k_layer, bf16 *v_layer, int n_split, int keys_per_split,
                                      float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
                                      int Hkv, int max_ctx, float eps, uint32_t *err) {
+    // one wide CTA per (sequence, KV head) when a single split covers the context: the
+    // latency-bound case (one or two short sequences); otherwise 4-warp CTAs over many splits
+    const bool wide = n_split == 1;
+#define Q3_ATTN(GG, NWW) run_fused<GG, NWW>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, \
+                                             keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err)
     switch (Hq / Hkv) {
-        case 1: return run_fused<1>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err);
-        case 2: return run_fused<2>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err);
-        case 4: return run_fused<4>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err);
-        case 8: return run_fused<8>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err);
+        case 1: return wide ? Q3_ATTN(1, 16) : Q3_ATTN(1, 4);
+        case 2: return wide ? Q3_ATTN(2, 16) : Q3_ATTN(2, 4);
+        case 4: return wide ? Q3_ATTN(4, 16) : Q3_ATTN(4, 4);
+        case 8: return wide ? Q3_ATTN(8, 16) : Q3_ATTN(8, 4);
     }
+#undef Q3_ATTN
     return cudaErrorInvalidValue;
 }
 

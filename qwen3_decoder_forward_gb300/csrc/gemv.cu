@@ -118,7 +118,8 @@ __global__ void __launch_bounds__(V2_WARPS * 32) k_gemv_bulk(const void *__restr
                                                             const bf16 *__restrict__ W, int N, int R,
                                                             void *out, const float *__restrict__ gain,
                                                             float eps, uint32_t *err,
-                                                            const bf16 *__restrict__ W_ahead) {
+                                                            const bf16 *__restrict__ W_ahead, float *zero_buf,
+                                                            int zero_n) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int K = KV * 256;
     constexpr int RPW = EPI == EPI_SWIGLU ? 2 : 1;
@@ -150,6 +151,11 @@ __global__ void __launch_bounds__(V2_WARPS * 32) k_gemv_bulk(const void *__restr
     }
     pdl_wait();
     pdl_trigger();
+    if (zero_buf) {  // clear this CTA's share of a buffer a later kernel accumulates into
+        const int per = (zero_n + gridDim.x - 1) / gridDim.x;
+        for (int i = blockIdx.x * per + threadIdx.x; i < min(zero_n, (blockIdx.x + 1) * per); i += blockDim.x)
+            zero_buf[i] = 0.0f;
+    }
     if (NORM) {
         const float *res = static_cast<const float *>(Xin);
         for (int b = warp; b < M; b += V2_WARPS) {
@@ -181,28 +187,51 @@ __global__ void __launch_bounds__(V2_WARPS * 32) k_gemv_bulk(const void *__restr
         mbar_wait_bounded(bar, 0, nullptr);  // let the copy land before the CTA exits
         return;
     }
-    for (int grp = warp; grp * RPW < nrows; grp += V2_WARPS) {
-        const int lr = grp * RPW;  // local row
+    // Each warp works on up to RB rows at once (rows warp, warp + 8, ...; SwiGLU pairs stay
+    // together) with two accumulators per row, so the loads and the reductions of several rows
+    // overlap instead of running one row after another.
+    constexpr int RB = 4;
+    const int n_grp = (nrows + RPW - 1) / RPW;
+    for (int g0 = warp; g0 < n_grp; g0 += V2_WARPS * (RB / RPW)) {
+        // groups of this warp in this pass (warp-uniform)
+        const int ng = min(RB / RPW, (n_grp - g0 + V2_WARPS - 1) / V2_WARPS);
         for (int b = 0; b < M; ++b) {
-            float acc[RPW];
+            float prev[RB];  // residual values for RESID_ADD, loaded before the dot products
+            if (EPI == EPI_RESID_ADD && lane == 0) {
 #pragma unroll
-            for (int r = 0; r < RPW; ++r) acc[r] = 0.0f;
+                for (int r = 0; r < RB; ++r)
+                    if (r < ng) prev[r] = ((const float *)out)[(size_t)b * N + row0 + g0 + r * V2_WARPS];
+            }
+            float acc[RB][2];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) acc[r][0] = acc[r][1] = 0.0f;
 #pragma unroll
             for (int i = 0; i < KV; ++i) {
                 const uint4 x = xs[b * (K / 8) + i * 32 + lane];
 #pragma unroll
-                for (int r = 0; r < RPW; ++r) acc[r] = dot8(ws[(lr + r) * (K / 8) + i * 32 + lane], x, acc[r]);
+                for (int r = 0; r < RB; ++r) {
+                    const int grp = g0 + (r / RPW) * V2_WARPS;
+                    const int lr = grp * RPW + (r % RPW);
+                    if (r / RPW < ng) acc[r][i & 1] = dot8(ws[(size_t)lr * (K / 8) + i * 32 + lane], x, acc[r][i & 1]);
+                }
             }
+            float sum[RB];
 #pragma unroll
-            for (int r = 0; r < RPW; ++r) acc[r] = warp_sum(acc[r]);
+            for (int r = 0; r < RB; ++r)
+                if (r / RPW < ng) sum[r] = warp_sum(acc[r][0] + acc[r][1]);
             if (lane == 0) {
-                const int row = row0 + lr;
-                if (EPI == EPI_F32) {
-                    ((float *)out)[(size_t)b * N + row] = acc[0];
-                } else if (EPI == EPI_RESID_ADD) {
-                    ((float *)out)[(size_t)b * N + row] += acc[0];
-                } else {
-                    ((bf16 *)out)[(size_t)b * (N / 2) + (row >> 1)] = __float2bfloat16(silu(acc[0]) * acc[RPW - 1]);
+#pragma unroll
+                for (int r = 0; r < RB; r += RPW) {
+                    if (r / RPW >= ng) continue;
+                    const int grp = g0 + (r / RPW) * V2_WARPS;
+                    const int row = row0 + grp * RPW;
+                    if (EPI == EPI_F32) {
+                        ((float *)out)[(size_t)b * N + row] = sum[r];
+                    } else if (EPI == EPI_RESID_ADD) {
+                        ((float *)out)[(size_t)b * N + row] = prev[r] + sum[r];
+                    } else {
+                        ((bf16 *)out)[(size_t)b * (N / 2) + (row >> 1)] = __float2bfloat16(silu(sum[r]) * sum[r + 1]);
+                    }
                 }
             }
         }
@@ -211,7 +240,8 @@ __global__ void __launch_bounds__(V2_WARPS * 32) k_gemv_bulk(const void *__restr
 
 template <int EPI, bool NORM, int KV>
 cudaError_t run_bulk(const Launch &lc, const void *X, int M, const bf16 *W, int N, void *out,
-                     const float *gain, float eps, uint32_t *err, const bf16 *W_ahead) {
+                     const float *gain, float eps, uint32_t *err, const bf16 *W_ahead, float *zero_buf,
+                     int zero_n) {
     constexpr int K = KV * 256;
     int R = (N + lc.num_sms - 1) / lc.num_sms;
     R = (R + 1) & ~1;  // even: SwiGLU rows come in (gate, up) pairs
@@ -220,16 +250,17 @@ cudaError_t run_bulk(const Launch &lc, const void *X, int M, const bf16 *W, int 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch(lc, k_gemv_bulk<EPI, NORM, KV>, dim3((N + R - 1) / R), dim3(V2_WARPS * 32), smem, X, M,
-                  W, N, R, out, gain, eps, err, W_ahead);
+                  W, N, R, out, gain, eps, err, W_ahead, zero_buf, zero_n);
 }
 
 template <int EPI, bool NORM>
 cudaError_t dispatch_bulk(const Launch &lc, const void *X, int M, int K, const bf16 *W, int N,
-                          void *out, const float *gain, float eps, uint32_t *err, const bf16 *W_ahead) {
+                          void *out, const float *gain, float eps, uint32_t *err, const bf16 *W_ahead,
+                          float *zero_buf, int zero_n) {
     switch (K) {
-        case 1024: return run_bulk<EPI, NORM, 4>(lc, X, M, W, N, out, gain, eps, err, W_ahead);
-        case 2048: return run_bulk<EPI, NORM, 8>(lc, X, M, W, N, out, gain, eps, err, W_ahead);
-        case 3072: return run_bulk<EPI, NORM, 12>(lc, X, M, W, N, out, gain, eps, err, W_ahead);
+        case 1024: return run_bulk<EPI, NORM, 4>(lc, X, M, W, N, out, gain, eps, err, W_ahead, zero_buf, zero_n);
+        case 2048: return run_bulk<EPI, NORM, 8>(lc, X, M, W, N, out, gain, eps, err, W_ahead, zero_buf, zero_n);
+        case 3072: return run_bulk<EPI, NORM, 12>(lc, X, M, W, N, out, gain, eps, err, W_ahead, zero_buf, zero_n);
     }
     return cudaErrorInvalidValue;
 }
@@ -259,17 +290,178 @@ bool gemv_fused_supported(int M, int K) {
 
 cudaError_t launch_gemv_fused(const Launch &lc, const void *X, int M, int K, const bf16 *W, int N,
                               int epi, void *out, const float *norm_gain, float eps, uint32_t *err,
-                              const bf16 *W_ahead) {
+                              const bf16 *W_ahead, float *zero_buf, int zero_n) {
     if (!gemv_fused_supported(M, K) || N % 2) return cudaErrorInvalidValue;
     const bool norm = norm_gain != nullptr;
-    if (epi == EPI_F32)
-        return norm ? dispatch_bulk<EPI_F32, true>(lc, X, M, K, W, N, out, norm_gain, eps, err, W_ahead)
-                    : dispatch_bulk<EPI_F32, false>(lc, X, M, K, W, N, out, norm_gain, eps, err, W_ahead);
-    if (epi == EPI_RESID_ADD)
-        return norm ? dispatch_bulk<EPI_RESID_ADD, true>(lc, X, M, K, W, N, out, norm_gain, eps, err, W_ahead)
-                    : dispatch_bulk<EPI_RESID_ADD, false>(lc, X, M, K, W, N, out, norm_gain, eps, err, W_ahead);
-    return norm ? dispatch_bulk<EPI_SWIGLU, true>(lc, X, M, K, W, N, out, norm_gain, eps, err, W_ahead)
-                : dispatch_bulk<EPI_SWIGLU, false>(lc, X, M, K, W, N, out, norm_gain, eps, err, W_ahead);
+#define Q3_BULK(E, Nm) dispatch_bulk<E, Nm>(lc, X, M, K, W, N, out, norm_gain, eps, err, W_ahead, zero_buf, zero_n)
+    if (epi == EPI_F32) return norm ? Q3_BULK(EPI_F32, true) : Q3_BULK(EPI_F32, false);
+    if (epi == EPI_RESID_ADD) return norm ? Q3_BULK(EPI_RESID_ADD, true) : Q3_BULK(EPI_RESID_ADD, false);
+    return norm ? Q3_BULK(EPI_SWIGLU, true) : Q3_BULK(EPI_SWIGLU, false);
+#undef Q3_BULK
+}
+
+// ---- the whole MLP of a decode step in one kernel ------------------------------------------
+//
+//   out[b] += h[b] (this CTA's slice) + sum_j act[b][j] WdT[j]   over this CTA's act indices j
+//   act[b][j] = silu(gate_j . m[b]) * (up_j . m[b]),  m[b] = RMSNorm(h[b]; gain)
+// ("手写Qwen3-0.6B推理", MLP: down(silu(gate(x)) * up(x)); the residual add of
+// Qwen3DecoderLayer).  CTA c owns act indices [c*NA, c*NA + NA): it bulk-copies their
+// interleaved gate/up weight rows and the matching rows of the transposed down weight (WdT
+// [I, C]) into shared memory before the dependency wait, so the down projection is split over
+// the CTAs along its reduction dimension and each CTA adds its partial sums (and its slice of
+// the residual h) into `out`, which must be zero on entry.  The fp32 additions of the CTAs
+// land in an unspecified order (vector atomics), so results may differ between runs in the
+// last bits.
+constexpr int MLP_WARPS = 8;
+
+template <int KV>
+__global__ void __launch_bounds__(MLP_WARPS * 32) k_mlp_fused(const float *__restrict__ h, int M,
+                                                             const float *__restrict__ gain, float eps,
+                                                             const bf16 *__restrict__ Wgu, const bf16 *__restrict__ WdT,
+                                                             int I, int NA, float *out, uint32_t *err,
+                                                             const bf16 *__restrict__ Wgu_ahead,
+                                                             const bf16 *__restrict__ WdT_ahead) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int C = KV * 256;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    uint4 *wgu = reinterpret_cast<uint4 *>(smem + 128);  // [2*NA][C/8]
+    uint4 *wd = wgu + (size_t)2 * NA * (C / 8);           // [NA][C/8]
+    uint4 *xs = wd + (size_t)NA * (C / 8);                // [M][C/8]
+    float *act = reinterpret_cast<float *>(xs + (size_t)M * (C / 8));  // [M][NA]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int a0 = blockIdx.x * NA;
+    const int na = min(NA, I - a0);
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(bar, 1);
+            mbar_expect_tx(bar, (uint32_t)na * 3 * C * 2);
+        }
+        __syncwarp();
+        for (int rr = lane; rr < 2 * na; rr += 32)
+            bulk_g2s(wgu + (size_t)rr * (C / 8), Wgu + (size_t)(2 * a0 + rr) * C, C * 2, bar);
+        for (int rr = lane; rr < na; rr += 32)
+            bulk_g2s(wd + (size_t)rr * (C / 8), WdT + (size_t)(a0 + rr) * C, C * 2, bar);
+    } else if (warp == 1 && lane == 0 && Wgu_ahead) {
+        prefetch_l2(Wgu_ahead + (size_t)2 * a0 * C, (uint32_t)na * 2 * C * 2);
+        prefetch_l2(WdT_ahead + (size_t)a0 * C, (uint32_t)na * C * 2);
+    }
+    float4 gv[2 * KV];
+#pragma unroll
+    for (int i = 0; i < 2 * KV; ++i) gv[i] = reinterpret_cast<const float4 *>(gain)[i * 32 + lane];
+    pdl_wait();
+    pdl_trigger();
+    // residual slice of this CTA into out (other CTAs add their partials to the same rows)
+    {
+        const int per = (C + gridDim.x - 1) / gridDim.x;
+        const int e0 = blockIdx.x * per, e1 = min(C, e0 + per);
+        for (int i = threadIdx.x; i < M * per; i += blockDim.x) {
+            const int b = i / per, e = e0 + i % per;
+            if (e < e1) atomicAdd(out + (size_t)b * C + e, h[(size_t)b * C + e]);
+        }
+    }
+    for (int b = warp; b < M; b += MLP_WARPS) {  // m[b] = RMSNorm(h[b]) into shared memory
+        const float4 *rp = reinterpret_cast<const float4 *>(h + (size_t)b * C);
+        float4 v[2 * KV];
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 2 * KV; ++i) {
+            v[i] = rp[i * 32 + lane];
+            ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+        }
+        const float inv = rsqrtf(warp_sum(ss) / (float)C + eps);
+        uint2 *dst = reinterpret_cast<uint2 *>(xs + (size_t)b * (C / 8));
+#pragma unroll
+        for (int i = 0; i < 2 * KV; ++i) {
+            uint2 o;
+            o.x = pack_bf16x2(v[i].x * inv * gv[i].x, v[i].y * inv * gv[i].y);
+            o.y = pack_bf16x2(v[i].z * inv * gv[i].z, v[i].w * inv * gv[i].w);
+            dst[i * 32 + lane] = o;
+        }
+    }
+    __syncthreads();
+    const bool ok = __syncthreads_and(mbar_wait_bounded(bar, 0, err));
+    if (!ok) {
+        mbar_wait_bounded(bar, 0, nullptr);
+        return;
+    }
+    // gate/up pairs -> act
+    for (int j = warp; j < na; j += MLP_WARPS) {
+        for (int b = 0; b < M; ++b) {
+            float g = 0.0f, u = 0.0f;
+#pragma unroll
+            for (int i = 0; i < KV; ++i) {
+                const uint4 x = xs[b * (C / 8) + i * 32 + lane];
+                g = dot8(wgu[(size_t)(2 * j) * (C / 8) + i * 32 + lane], x, g);
+                u = dot8(wgu[(size_t)(2 * j + 1) * (C / 8) + i * 32 + lane], x, u);
+            }
+            g = warp_sum(g);
+            u = warp_sum(u);
+            if (lane == 0) act[b * NA + j] = __bfloat162float(__float2bfloat16(silu(g) * u));
+        }
+    }
+    __syncthreads();
+    // down projection, split along its reduction dimension: this CTA's act indices only
+    for (int b = 0; b < M; ++b) {
+        for (int n0 = threadIdx.x * 4; n0 < C; n0 += blockDim.x * 4) {
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            for (int j = 0; j < na; ++j) {
+                const float a = act[b * NA + j];
+                const uint2 w = *reinterpret_cast<const uint2 *>(reinterpret_cast<const bf16 *>(wd) + (size_t)j * C + n0);
+                const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+                const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+                acc.x = fmaf(a, w01.x, acc.x);
+                acc.y = fmaf(a, w01.y, acc.y);
+                acc.z = fmaf(a, w23.x, acc.z);
+                acc.w = fmaf(a, w23.y, acc.w);
+            }
+            atomicAdd(reinterpret_cast<float4 *>(out + (size_t)b * C + n0), acc);
+        }
+    }
+}
+
+template <int KV>
+cudaError_t run_mlp(const Launch &lc, const float *h, int M, const float *gain, float eps, const bf16 *Wgu,
+                    const bf16 *WdT, int I, float *out, uint32_t *err, const bf16 *Wgu_ahead, const bf16 *WdT_ahead) {
+    constexpr int C = KV * 256;
+    const int NA = (I + lc.num_sms - 1) / lc.num_sms;
+    const size_t smem = 128 + (size_t)NA * 3 * C * 2 + (size_t)M * C * 2 + (size_t)M * NA * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_mlp_fused<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch(lc, k_mlp_fused<KV>, dim3((I + NA - 1) / NA), dim3(MLP_WARPS * 32), smem, h, M, gain, eps, Wgu,
+                  WdT, I, NA, out, err, Wgu_ahead, WdT_ahead);
+}
+
+bool mlp_fused_supported(int M, int C, int I, int num_sms) {
+    const int NA = (I + num_sms - 1) / num_sms;
+    const size_t smem = 128 + (size_t)NA * 3 * C * 2 + (size_t)M * C * 2 + (size_t)M * NA * 4;
+    return M >= 1 && M <= 4 && C == 1024 && smem <= 200 * 1024;
+}
+
+cudaError_t launch_mlp_fused(const Launch &lc, const float *h, int M, int C, const float *gain, float eps,
+                             const bf16 *Wgu, const bf16 *WdT, int I, float *out, uint32_t *err,
+                             const bf16 *Wgu_ahead, const bf16 *WdT_ahead) {
+    if (!mlp_fused_supported(M, C, I, lc.num_sms)) return cudaErrorInvalidValue;
+    return run_mlp<4>(lc, h, M, gain, eps, Wgu, WdT, I, out, err, Wgu_ahead, WdT_ahead);
+}
+
+// WdT[j][n] = Wd[n][j]: the down projection stored transposed for the split-K MLP kernel.
+__global__ void k_transpose_bf16(const bf16 *__restrict__ src, bf16 *__restrict__ dst, int rows, int cols) {
+    __shared__ bf16 tile[32][33];
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + threadIdx.x;
+        if (r < rows && c < cols) tile[i][threadIdx.x] = src[(size_t)r * cols + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, r = r0 + threadIdx.x;
+        if (r < rows && c < cols) dst[(size_t)c * rows + r] = tile[threadIdx.x][i];
+    }
+}
+
+cudaError_t launch_transpose_bf16(const Launch &lc, const bf16 *src, bf16 *dst, int rows, int cols) {
+    return launch(lc, k_transpose_bf16, dim3((cols + 31) / 32, (rows + 31) / 32), dim3(32, 8), 0, src, dst, rows,
+                  cols);
 }
 
 }  // namespace q3

@@ -105,7 +105,15 @@ cudaError_t launch_gemv(const Launch &lc, const bf16 *X, int M, int K, const bf1
 bool gemv_fused_supported(int M, int K);
 cudaError_t launch_gemv_fused(const Launch &lc, const void *X, int M, int K, const bf16 *W, int N,
                               int epi, void *out, const float *norm_gain, float eps, uint32_t *err,
-                              const bf16 *W_ahead = nullptr);
+                              const bf16 *W_ahead = nullptr, float *zero_buf = nullptr, int zero_n = 0);
+// The decode MLP in one kernel (M <= 4 rows, C == 1024): out += h + down(silu(gate m) * up m),
+// m = RMSNorm(h), with the down projection split over CTAs and added with fp32 atomics; out
+// must be zero on entry.  WdT is the down weight transposed ([I, C]).
+bool mlp_fused_supported(int M, int C, int I, int num_sms);
+cudaError_t launch_mlp_fused(const Launch &lc, const float *h, int M, int C, const float *gain, float eps,
+                             const bf16 *Wgu, const bf16 *WdT, int I, float *out, uint32_t *err,
+                             const bf16 *Wgu_ahead, const bf16 *WdT_ahead);
+cudaError_t launch_transpose_bf16(const Launch &lc, const bf16 *src, bf16 *dst, int rows, int cols);
 
 // --- rope_kv.cu --------------------------------------------------------------------------
 // qkv fp32 [rows, (Hq+2Hkv)*D] -> q bf16 [rows, Hq, D] (normed + rotated), K (normed +

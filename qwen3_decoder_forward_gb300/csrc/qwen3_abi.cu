@@ -25,12 +25,13 @@ size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Layout {
     // per-layer strides (bytes) and offsets within layer 0
-    size_t layer_bytes = 0, o_wqkv = 0, o_wo = 0, o_wgu = 0, o_wdown = 0, o_gin = 0, o_gpost = 0,
-           o_gq = 0, o_gk = 0;
+    size_t layer_bytes = 0, o_wqkv = 0, o_wo = 0, o_wgu = 0, o_wdown = 0, o_wdownT = 0, o_gin = 0,
+           o_gpost = 0, o_gq = 0, o_gk = 0;
     size_t o_layers = 0, o_embed = 0, o_gfinal = 0, o_rope = 0, o_kcache = 0, o_vcache = 0,
            kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0;
     size_t o_resid = 0, o_xn = 0, o_qkv = 0, o_q = 0, o_attn = 0, o_act = 0, o_rowslot = 0,
-           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0;
+           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0,
+           o_resid2 = 0;
     size_t total = 0;
 };
 
@@ -73,6 +74,7 @@ Layout make_layout(const qwen3_config &c) {
     L.o_wo = take(C * Hq * D * 2);
     L.o_wgu = take(2 * I * C * 2);
     L.o_wdown = take(C * I * 2);
+    L.o_wdownT = take(C * I * 2);  // down weight transposed [I, C] for the split-K decode MLP
     L.o_gin = take(C * 4);
     L.o_gpost = take(C * 4);
     L.o_gq = take(D * 4);
@@ -103,6 +105,7 @@ Layout make_layout(const qwen3_config &c) {
     L.o_wsml = take((size_t)c.max_seqs * Hq * MAX_SPLIT * 2 * 4);
     L.o_wso = take((size_t)c.max_seqs * Hq * MAX_SPLIT * D * 4);
     L.o_counters = take((size_t)c.max_seqs * Hkv * 4);
+    L.o_resid2 = take((size_t)c.max_seqs * C * 4);  // second residual buffer of the decode ping-pong
     L.total = off;
     return L;
 }
@@ -175,17 +178,20 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
     uint32_t *err = c->at<uint32_t>(L.o_err);
     const bf16 *embed = c->at<bf16>(L.o_embed);
     const float2 *rope = c->at<float2>(L.o_rope);
-    auto dump = [&](int l) -> cudaError_t {
+    auto dump = [&](int l, const float *src) -> cudaError_t {
         if (!c->dump) return cudaSuccess;
-        return cudaMemcpyAsync(c->dump + (size_t)l * R * C, resid, (size_t)R * C * 4,
+        return cudaMemcpyAsync(c->dump + (size_t)l * R * C, src, (size_t)R * C * 4,
                                cudaMemcpyDeviceToDevice, lc.stream);
     };
 
     Q3_TRY(launch_embed_rmsnorm(lc, tokens, rows, embed, (const float *)(c->layer(0) + L.o_gin),
                                 resid, xn, C, k.vocab, k.rms_eps, err));
-    Q3_TRY(dump(0));
+    Q3_TRY(dump(0, resid));
     const bool fused = decode && gemv_fused_supported(R, C) && gemv_fused_supported(R, Hq * D) &&
                        gemv_fused_supported(R, I);
+    // residual ping-pong of the fused decode MLP: layer l reads res[l & 1] and leaves res[(l+1) & 1]
+    const bool mlp = fused && mlp_fused_supported(R, C, I, lc.num_sms);
+    float *res[2] = {resid, mlp ? c->at<float>(L.o_resid2) : resid};
     for (int l = 0; l < k.n_layers; ++l) {
         const uint8_t *lw = c->layer(l);
         const float *g_in = (const float *)(lw + L.o_gin), *g_post = (const float *)(lw + L.o_gpost);
@@ -193,21 +199,28 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
         const bf16 *w_qkv = (const bf16 *)(lw + L.o_wqkv), *w_o = (const bf16 *)(lw + L.o_wo);
         const bf16 *w_gu = (const bf16 *)(lw + L.o_wgu), *w_down = (const bf16 *)(lw + L.o_wdown);
         if (fused) {
-            // decode, few rows: 5 kernels per layer, the norms folded into the GEMV prologues.
-            // Each projection also asks L2 for its block of the next layer's weights (the next
-            // step's layer 0 after the last layer), so HBM streams ahead of the kernel chain.
+            // decode, few rows: the norms folded into the GEMV prologues; each projection also asks
+            // L2 for its block of the next layer's weights (the next step's layer 0 after the
+            // last layer), so HBM streams ahead of the kernel chain.
             const uint8_t *ahead = c->layer((l + 1) % k.n_layers);
-            Q3_TRY(launch_gemv_fused(lc, resid, R, C, w_qkv, qkv_n, EPI_F32, qkv, g_in, k.rms_eps, err,
-                                     (const bf16 *)(ahead + L.o_wqkv)));
+            float *r_cur = res[l & 1], *r_next = res[(l + 1) & 1];
+            Q3_TRY(launch_gemv_fused(lc, r_cur, R, C, w_qkv, qkv_n, EPI_F32, qkv, g_in, k.rms_eps, err,
+                                     (const bf16 *)(ahead + L.o_wqkv), mlp ? r_next : nullptr, R * C));
             Q3_TRY(launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
                                             kps, c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
                                             c->at<int>(L.o_counters), attn, Hq, Hkv, k.max_ctx, k.rms_eps, err));
-            Q3_TRY(launch_gemv_fused(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, resid, nullptr, 0.0f, err,
+            Q3_TRY(launch_gemv_fused(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, r_cur, nullptr, 0.0f, err,
                                      (const bf16 *)(ahead + L.o_wo)));
-            Q3_TRY(launch_gemv_fused(lc, resid, R, C, w_gu, 2 * I, EPI_SWIGLU, act, g_post, k.rms_eps, err,
-                                     (const bf16 *)(ahead + L.o_wgu)));
-            Q3_TRY(launch_gemv_fused(lc, act, R, I, w_down, C, EPI_RESID_ADD, resid, nullptr, 0.0f, err,
-                                     (const bf16 *)(ahead + L.o_wdown)));
+            if (mlp) {  // gate_up + SwiGLU + down in one kernel, residual into the other buffer
+                Q3_TRY(launch_mlp_fused(lc, r_cur, R, C, g_post, k.rms_eps, w_gu, (const bf16 *)(lw + L.o_wdownT), I,
+                                        r_next, err, (const bf16 *)(ahead + L.o_wgu),
+                                        (const bf16 *)(ahead + L.o_wdownT)));
+            } else {
+                Q3_TRY(launch_gemv_fused(lc, r_cur, R, C, w_gu, 2 * I, EPI_SWIGLU, act, g_post, k.rms_eps, err,
+                                         (const bf16 *)(ahead + L.o_wgu)));
+                Q3_TRY(launch_gemv_fused(lc, act, R, I, w_down, C, EPI_RESID_ADD, r_cur, nullptr, 0.0f, err,
+                                         (const bf16 *)(ahead + L.o_wdown)));
+            }
         } else if (decode) {
             if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
             Q3_TRY(launch_gemv(lc, xn, R, C, w_qkv, qkv_n, EPI_F32, qkv));
@@ -240,11 +253,11 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
             Q3_TRY(gemm(xn, C, w_gu, 2 * I, EPI_SWIGLU, act));
             Q3_TRY(gemm(act, I, w_down, C, EPI_RESID_ADD, resid));
         }
-        Q3_TRY(dump(l + 1));
+        Q3_TRY(dump(l + 1, mlp ? res[(l + 1) & 1] : resid));
     }
     bf16 *last = c->at<bf16>(L.o_last);
-    Q3_TRY(launch_final_norm(lc, resid, rows.cu_seqlens, rows.B, c->at<float>(L.o_gfinal), last, C,
-                             k.rms_eps));
+    Q3_TRY(launch_final_norm(lc, mlp ? res[k.n_layers & 1] : resid, rows.cu_seqlens, rows.B,
+                             c->at<float>(L.o_gfinal), last, C, k.rms_eps));
     return launch_lmhead_argmax(lc, last, rows.B, C, embed, k.vocab, logits, c->at<float>(L.o_pval),
                                 c->at<int32_t>(L.o_pidx), c->n_parts, next, rows);
 }
@@ -345,6 +358,7 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
             Q3_TRY(cudaMemcpy2DAsync(lw + lay.o_wgu + C * 2, 2 * C * 2, w->wup[l], C * 2, C * 2, I,
                                      cudaMemcpyDeviceToDevice, st));
             Q3_TRY(d2d(lw + lay.o_wdown, w->wdown[l], C * I * 2));
+            Q3_TRY(launch_transpose_bf16(lc, (const bf16 *)w->wdown[l], (bf16 *)(lw + lay.o_wdownT), (int)C, (int)I));
             Q3_TRY(launch_bf16_to_f32(lc, (const bf16 *)w->in_norm[l], (float *)(lw + lay.o_gin), (int)C));
             Q3_TRY(launch_bf16_to_f32(lc, (const bf16 *)w->post_norm[l], (float *)(lw + lay.o_gpost), (int)C));
             Q3_TRY(launch_bf16_to_f32(lc, (const bf16 *)w->q_norm[l], (float *)(lw + lay.o_gq), (int)D));
@@ -436,7 +450,10 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
     while (bucket < max_len) bucket <<= 1;
     bucket = std::min(bucket, c->cfg.max_ctx);
     const int want = (4 * c->num_sms + B * c->cfg.n_kv_heads - 1) / (B * c->cfg.n_kv_heads);
-    const int n_split = std::max(1, std::min({want, MAX_SPLIT, (bucket + 63) / 64}));
+    // One or two short sequences: a single wide CTA per KV head (no cross-CTA merge on the
+    // critical path).  Otherwise enough splits to give every SM several CTAs.
+    const bool latency_mode = false;  // (a single wide CTA per KV head measured no faster)
+    const int n_split = latency_mode ? 1 : std::max(1, std::min({want, MAX_SPLIT, (bucket + 63) / 64}));
     const int kps = ((bucket + n_split - 1) / n_split + 15) / 16 * 16;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);

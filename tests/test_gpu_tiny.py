@@ -67,13 +67,19 @@ def test_teacher_forced_parity(setup):
 
 
 def test_graph_replay_matches_direct_launches(setup):
-    """The recorded decode graph and one-by-one launches give the same tokens and logits."""
+    """The recorded decode graph and one-by-one launches give the same tokens and logits.
+
+    The decode MLP adds its split-K partial sums with fp32 atomics in an unspecified order, so
+    two runs may differ in the last bits: logits must agree to 1e-5 and tokens wherever the
+    top-2 gap of the logits is clear."""
     w, prompt, ref = setup
     a, _ = run_gpu(w, prompt, ref["fed"], flags=0, dump=False)
     b, _ = run_gpu(w, prompt, ref["fed"], flags=binding.QWEN3_FLAG_NO_GRAPH, dump=False)
     for x, y in zip(a, b):
-        assert x["token"] == y["token"]
-        np.testing.assert_array_equal(x["logits"], y["logits"])
+        assert gc.rel_l2(x["logits"], y["logits"]) <= 1e-5
+        top2 = np.sort(y["logits"])[-2:]
+        if top2[1] - top2[0] > 1e-3:
+            assert x["token"] == y["token"]
 
 
 def test_free_running_greedy_feeds_itself(setup):
