@@ -222,9 +222,11 @@ __global__ void __launch_bounds__(NW * 32) k_attn_decode_fused(
     const int n_split = gridDim.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane & 7, kg = lane >> 3;
-    // Written by kernels that have completed (see above): safe before the dependency wait.
-    const int slot = r.row_slot[b];
-    const int pos = r.row_pos[b];
+    // Written by kernels that have completed (see above), so they may be read before the
+    // dependency wait -- but only from L2 (ld.global.cg): this SM's L1 may still hold the
+    // previous step's lines, and only the wait would invalidate them.
+    const int slot = __ldcg(r.row_slot + b);
+    const int pos = __ldcg(r.row_pos + b);
     const bool pos_ok = pos < max_ctx;
     const int k_begin = split * kps;
     const int k_end = pos_ok ? min(pos + 1, k_begin + kps) : k_begin;

@@ -444,6 +444,289 @@ cudaError_t launch_mlp_fused(const Launch &lc, const float *h, int M, int C, con
     return run_mlp<4>(lc, h, M, gain, eps, Wgu, WdT, I, out, err, Wgu_ahead, WdT_ahead);
 }
 
+// ---- tensor-core decode projection for 9..32 rows -------------------------------------------
+//
+// out[M,N] = X[M,K] . W[N,K]^T with the weights as the M side of mma.sync m16n8k16 and the
+// batch rows as the N side.  CTA = 16 weight rows x one K slice (K/KS): the rows are bulk-
+// copied into padded shared memory before the dependency wait, X (zero-padded to 32 rows) is
+// loaded after it, the 4 warps split the K slice, and their partial tiles are summed through
+// shared memory.  With KS > 1 (RESID_ADD only) the slices add into the output with atomics.
+constexpr int MMA_ROWS = 16, MMA_MPAD = 32, MMA_WARPS = 4;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t *r, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int EPI, int KS>
+__global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restrict__ X, int M, int K,
+                                                             const bf16 *__restrict__ W, int N, void *out,
+                                                             uint32_t *err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int Kc = K / KS;
+    const int stride = Kc * 2 + 16;  // padded row stride (bytes): conflict-free ldmatrix
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *ws = smem + 128;                      // [16][stride]
+    uint8_t *xs = ws + MMA_ROWS * stride;          // [32][stride]
+    float *red = reinterpret_cast<float *>(xs + MMA_MPAD * stride);  // [warps][16][32]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = blockIdx.x * MMA_ROWS, ks = blockIdx.y, k0 = ks * Kc;
+    uint64_t *xbar = bar + 1;
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(bar, 1);
+            mbar_init(xbar, 1);
+            mbar_expect_tx(bar, (uint32_t)MMA_ROWS * Kc * 2);
+        }
+        __syncwarp();
+        if (lane < MMA_ROWS) bulk_g2s(ws + lane * stride, W + (size_t)(row0 + lane) * K + k0, Kc * 2, bar);
+    }
+    // rows of X beyond M are zero
+    for (int i = threadIdx.x; i < (MMA_MPAD - M) * (Kc / 8); i += MMA_WARPS * 32)
+        *reinterpret_cast<uint4 *>(xs + (M + i / (Kc / 8)) * stride + (i % (Kc / 8)) * 16) = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    // X rows by bulk copies: one round trip for the whole operand
+    if (warp == 1) {
+        if (lane == 0) mbar_expect_tx(xbar, (uint32_t)M * Kc * 2);
+        __syncwarp();
+        if (lane < M) bulk_g2s(xs + lane * stride, X + (size_t)lane * K + k0, Kc * 2, xbar);
+    }
+    const bool ok = __syncthreads_and(mbar_wait_bounded(bar, 0, err) && mbar_wait_bounded(xbar, 0, err));
+    if (!ok) {
+        mbar_wait_bounded(bar, 0, nullptr);
+        mbar_wait_bounded(xbar, 0, nullptr);
+        return;
+    }
+    float acc[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    const int kq = Kc / MMA_WARPS;  // this warp's quarter of the slice
+    const uint32_t wsa = smem_addr(ws), xsa = smem_addr(xs);
+    for (int kk = warp * kq; kk < (warp + 1) * kq; kk += 16) {
+        uint32_t a[4];
+        ldsm_x4(a, wsa + (lane & 15) * stride + (kk + (lane >> 4) * 8) * 2);
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {  // two ldmatrix.x4 cover the 32 padded batch rows
+            uint32_t b[4];
+            const int n = nb * 16 + (lane & 7) + ((lane >> 4) << 3);
+            ldsm_x4(b, xsa + n * stride + (kk + ((lane >> 3) & 1) * 8) * 2);
+            mma16816(acc[nb * 2], a, b[0], b[1]);
+            mma16816(acc[nb * 2 + 1], a, b[2], b[3]);
+        }
+    }
+    // partial tiles of the 4 warps -> shared memory, then sum
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float *rw = red + warp * MMA_ROWS * MMA_MPAD;
+        rw[g * MMA_MPAD + j * 8 + 2 * t] = acc[j][0];
+        rw[g * MMA_MPAD + j * 8 + 2 * t + 1] = acc[j][1];
+        rw[(g + 8) * MMA_MPAD + j * 8 + 2 * t] = acc[j][2];
+        rw[(g + 8) * MMA_MPAD + j * 8 + 2 * t + 1] = acc[j][3];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < MMA_ROWS * MMA_MPAD; i += MMA_WARPS * 32) {
+        const int r = i / MMA_MPAD, b = i % MMA_MPAD;  // r: weight row, b: batch row
+        if (b >= M) continue;
+        float v = 0.0f;
+#pragma unroll
+        for (int w = 0; w < MMA_WARPS; ++w) v += red[w * MMA_ROWS * MMA_MPAD + i];
+        const int n = row0 + r;
+        if (EPI == EPI_F32) {
+            ((float *)out)[(size_t)b * N + n] = v;
+        } else if (EPI == EPI_RESID_ADD) {
+            if (KS == 1) ((float *)out)[(size_t)b * N + n] += v;
+            else atomicAdd((float *)out + (size_t)b * N + n, v);
+        } else if ((r & 1) == 0) {  // SwiGLU: rows (2j, 2j+1) = (gate_j, up_j)
+            float up = 0.0f;
+#pragma unroll
+            for (int w = 0; w < MMA_WARPS; ++w) up += red[w * MMA_ROWS * MMA_MPAD + i + MMA_MPAD];
+            ((bf16 *)out)[(size_t)b * (N / 2) + (n >> 1)] = __float2bfloat16(silu(v) * up);
+        }
+    }
+}
+
+// ---- tensor-core lm_head + argmax for 9..32 rows -----------------------------------------
+//
+// Persistent CTAs walk 16-row tiles of the (tied) embedding table through a 4-stage ring
+// filled by bulk copies; each tile is multiplied with the 32 (zero-padded) rows of x on the
+// tensor cores (mma.sync, 4 warps splitting K), its logits optionally stored, and the running
+// best (value, index) of every batch row updated -- lowest index on ties.  One partial per
+// CTA and row goes to part_val/part_idx for the reduction kernel.
+constexpr int LM_STAGES = 4;
+
+template <int KV>
+__global__ void __launch_bounds__(MMA_WARPS * 32) k_lmhead_mma(const bf16 *__restrict__ X, int M,
+                                                               const bf16 *__restrict__ E, int V,
+                                                               float *__restrict__ logits,
+                                                               float *__restrict__ part_val,
+                                                               int32_t *__restrict__ part_idx, uint32_t *err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int C = KV * 256;
+    constexpr int stride = C * 2 + 16;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [LM_STAGES]
+    uint64_t *xbar = full + LM_STAGES;
+    uint8_t *ring = smem + 128;                          // [LM_STAGES][16][stride]
+    uint8_t *xs = ring + LM_STAGES * MMA_ROWS * stride;  // [32][stride]
+    float *red = reinterpret_cast<float *>(xs + MMA_MPAD * stride);  // [warps][16][32]
+    __shared__ float best_v[MMA_MPAD];
+    __shared__ int best_i[MMA_MPAD];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = (V + MMA_ROWS - 1) / MMA_ROWS;
+    const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    auto issue = [&](int i) {  // local tile i into stage i % LM_STAGES (rows beyond V: not copied)
+        const int tile = blockIdx.x + i * gridDim.x, r0 = tile * MMA_ROWS;
+        const int nr = min(MMA_ROWS, V - r0);
+        uint64_t *b = &full[i % LM_STAGES];
+        if (lane == 0) mbar_expect_tx(b, (uint32_t)nr * C * 2);
+        __syncwarp();
+        if (lane < nr) bulk_g2s(ring + (i % LM_STAGES) * MMA_ROWS * stride + lane * stride, E + (size_t)(r0 + lane) * C, C * 2, b);
+    };
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < LM_STAGES; ++st) mbar_init(&full[st], 1);
+        mbar_init(xbar, 1);
+    }
+    if (threadIdx.x < MMA_MPAD) {
+        best_v[threadIdx.x] = -INFINITY;
+        best_i[threadIdx.x] = 0x7fffffff;
+    }
+    for (int i = threadIdx.x; i < (MMA_MPAD - M) * (C / 8); i += MMA_WARPS * 32)
+        *reinterpret_cast<uint4 *>(xs + (M + i / (C / 8)) * stride + (i % (C / 8)) * 16) = make_uint4(0, 0, 0, 0);
+    // stale rows of a partial last tile must be finite: zero every stage once
+    for (int i = threadIdx.x; i < LM_STAGES * MMA_ROWS * (C / 8); i += MMA_WARPS * 32)
+        *reinterpret_cast<uint4 *>(ring + (i / (C / 8)) * stride + (i % (C / 8)) * 16) = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    if (warp == 0)
+        for (int i = 0; i < min(LM_STAGES, my_tiles); ++i) issue(i);
+    pdl_wait();
+    pdl_trigger();
+    if (warp == 1) {
+        if (lane == 0) mbar_expect_tx(xbar, (uint32_t)M * C * 2);
+        __syncwarp();
+        if (lane < M) bulk_g2s(xs + lane * stride, X + (size_t)lane * C, C * 2, xbar);
+    }
+    bool ok = __syncthreads_and(mbar_wait_bounded(xbar, 0, err));
+    const uint32_t xsa = smem_addr(xs);
+    const int g = lane >> 2, t = lane & 3;
+    for (int i = 0; ok && i < my_tiles; ++i) {
+        const int st = i % LM_STAGES;
+        ok = __syncthreads_and(mbar_wait_bounded(&full[st], (i / LM_STAGES) & 1, err));
+        if (!ok) break;
+        const uint32_t wsa = smem_addr(ring + st * MMA_ROWS * stride);
+        float acc[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+#pragma unroll
+        for (int kk = warp * (C / MMA_WARPS); kk < (warp + 1) * (C / MMA_WARPS); kk += 16) {
+            uint32_t a[4];
+            ldsm_x4(a, wsa + (lane & 15) * stride + (kk + (lane >> 4) * 8) * 2);
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+                uint32_t b[4];
+                const int n = nb * 16 + (lane & 7) + ((lane >> 4) << 3);
+                ldsm_x4(b, xsa + n * stride + (kk + ((lane >> 3) & 1) * 8) * 2);
+                mma16816(acc[nb * 2], a, b[0], b[1]);
+                mma16816(acc[nb * 2 + 1], a, b[2], b[3]);
+            }
+        }
+        float *rw = red + warp * MMA_ROWS * MMA_MPAD;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            rw[g * MMA_MPAD + j * 8 + 2 * t] = acc[j][0];
+            rw[g * MMA_MPAD + j * 8 + 2 * t + 1] = acc[j][1];
+            rw[(g + 8) * MMA_MPAD + j * 8 + 2 * t] = acc[j][2];
+            rw[(g + 8) * MMA_MPAD + j * 8 + 2 * t + 1] = acc[j][3];
+        }
+        __syncthreads();  // partial tiles in place; the stage is free
+        if (warp == 0 && i + LM_STAGES < my_tiles) issue(i + LM_STAGES);
+        const int r0 = (blockIdx.x + i * gridDim.x) * MMA_ROWS;
+        // sum the warps' partials; thread handles 4 (row, batch) outputs
+        for (int o = threadIdx.x; o < MMA_ROWS * MMA_MPAD; o += MMA_WARPS * 32) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < MMA_WARPS; ++w) v += red[w * MMA_ROWS * MMA_MPAD + o];
+            red[o] = v;  // warp 0's slot holds the sum (each o read and written by one thread)
+            const int r = o / MMA_MPAD, b = o % MMA_MPAD;
+            if (logits && b < M && r0 + r < V) logits[(size_t)b * V + r0 + r] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x < MMA_MPAD && threadIdx.x < M) {  // running best of batch row b
+            const int b = threadIdx.x;
+            float bv = best_v[b];
+            int bi = best_i[b];
+            for (int r = 0; r < MMA_ROWS && r0 + r < V; ++r) {
+                const float v = red[r * MMA_MPAD + b];
+                if (v > bv) {  // rows increase within and across a CTA's tiles: strict > keeps the lowest
+                    bv = v;
+                    bi = r0 + r;
+                }
+            }
+            best_v[b] = bv;
+            best_i[b] = bi;
+        }
+        __syncthreads();  // red is rewritten by the next tile
+    }
+    if (!ok) {  // let issued copies land
+        for (int i = 0; i < min(LM_STAGES, my_tiles); ++i) mbar_wait_bounded(&full[i], 0, nullptr);
+        mbar_wait_bounded(xbar, 0, nullptr);
+        return;
+    }
+    if (threadIdx.x < M) {
+        part_val[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = best_v[threadIdx.x];
+        part_idx[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = best_i[threadIdx.x];
+    }
+}
+
+cudaError_t launch_lmhead_mma(const Launch &lc, const bf16 *X, int M, int C, const bf16 *E, int V, float *logits,
+                              float *part_val, int32_t *part_idx, int n_parts, uint32_t *err) {
+    if (C != 1024 || M < 1 || M > MMA_MPAD) return cudaErrorInvalidValue;
+    constexpr int KV = 4;
+    const size_t smem = 128 + (size_t)(LM_STAGES * MMA_ROWS + MMA_MPAD) * (KV * 256 * 2 + 16) +
+                        MMA_WARPS * MMA_ROWS * MMA_MPAD * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_lmhead_mma<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch(lc, k_lmhead_mma<KV>, dim3(n_parts), dim3(MMA_WARPS * 32), smem, X, M, E, V, logits, part_val,
+                  part_idx, err);
+}
+
+template <int EPI, int KS>
+cudaError_t run_mma(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N, void *out, uint32_t *err) {
+    const int Kc = K / KS;
+    const size_t smem = 128 + (size_t)(MMA_ROWS + MMA_MPAD) * (Kc * 2 + 16) + MMA_WARPS * MMA_ROWS * MMA_MPAD * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_gemv_mma<EPI, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch(lc, k_gemv_mma<EPI, KS>, dim3(N / MMA_ROWS, KS), dim3(MMA_WARPS * 32), smem, X, M, K, W, N, out,
+                  err);
+}
+
+bool gemv_mma_supported(int M, int K, int N) {
+    return M >= 1 && M <= MMA_MPAD && N % MMA_ROWS == 0 && K % 256 == 0 && K <= 3072;
+}
+
+cudaError_t launch_gemv_mma(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N, int epi,
+                            void *out, uint32_t *err) {
+    if (!gemv_mma_supported(M, K, N)) return cudaErrorInvalidValue;
+    // K above 2048 with 32 rows would not fit shared memory in one slice: split it (residual only)
+    if (K > 2048) {
+        if (epi != EPI_RESID_ADD) return cudaErrorInvalidValue;
+        return run_mma<EPI_RESID_ADD, 2>(lc, X, M, K, W, N, out, err);
+    }
+    if (epi == EPI_F32) return run_mma<EPI_F32, 1>(lc, X, M, K, W, N, out, err);
+    if (epi == EPI_RESID_ADD) return run_mma<EPI_RESID_ADD, 1>(lc, X, M, K, W, N, out, err);
+    return run_mma<EPI_SWIGLU, 1>(lc, X, M, K, W, N, out, err);
+}
+
 // WdT[j][n] = Wd[n][j]: the down projection stored transposed for the split-K MLP kernel.
 __global__ void k_transpose_bf16(const bf16 *__restrict__ src, bf16 *__restrict__ dst, int rows, int cols) {
     __shared__ bf16 tile[32][33];

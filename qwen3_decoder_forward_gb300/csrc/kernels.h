@@ -114,6 +114,15 @@ cudaError_t launch_mlp_fused(const Launch &lc, const float *h, int M, int C, con
                              const bf16 *Wgu, const bf16 *WdT, int I, float *out, uint32_t *err,
                              const bf16 *Wgu_ahead, const bf16 *WdT_ahead);
 cudaError_t launch_transpose_bf16(const Launch &lc, const bf16 *src, bf16 *dst, int rows, int cols);
+// Tensor-core (mma.sync) decode projection for up to 32 rows; K > 2048 only with EPI_RESID_ADD
+// (the K halves add into the output with atomics).
+bool gemv_mma_supported(int M, int K, int N);
+// lm_head + argmax pass 1 on the tensor cores for 1..32 rows (C == 1024): one partial (best
+// value, index) per CTA and row, as launch_lmhead_argmax's pass 1 writes them.
+cudaError_t launch_lmhead_mma(const Launch &lc, const bf16 *X, int M, int C, const bf16 *E, int V, float *logits,
+                              float *part_val, int32_t *part_idx, int n_parts, uint32_t *err);
+cudaError_t launch_gemv_mma(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N, int epi,
+                            void *out, uint32_t *err);
 
 // --- rope_kv.cu --------------------------------------------------------------------------
 // qkv fp32 [rows, (Hq+2Hkv)*D] -> q bf16 [rows, Hq, D] (normed + rotated), K (normed +
@@ -150,7 +159,7 @@ cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const R
 // Also sets ctx_len[slot] = position + 1 of each sequence's last row.
 cudaError_t launch_lmhead_argmax(const Launch &lc, const bf16 *X, int B, int C, const bf16 *E,
                                  int V, float *logits, float *part_val, int32_t *part_idx,
-                                 int n_parts, int32_t *next_tok, const Rows &r);
+                                 int n_parts, int32_t *next_tok, const Rows &r, uint32_t *err = nullptr);
 int lmhead_parts(int num_sms);
 
 }  // namespace q3

@@ -135,16 +135,27 @@ __global__ void __launch_bounds__(256) k_argmax_reduce(const float *__restrict__
 
 template <int KV>
 cudaError_t run(const Launch &lc, const bf16 *X, int B, const bf16 *E, int V, float *logits,
-                float *part_val, int32_t *part_idx, int n_parts, int32_t *next_tok, const Rows &r) {
-    cudaError_t e = cudaFuncSetAttribute(k_lmhead<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MAX_B * KV * 256 * (int)sizeof(bf16));
-    if (e != cudaSuccess) return e;
+                float *part_val, int32_t *part_idx, int n_parts, int32_t *next_tok, const Rows &r, uint32_t *err) {
+    cudaError_t e;
     constexpr int C = KV * 256;
-    for (int b0 = 0; b0 < B; b0 += MAX_B) {
-        const int bc = B - b0 < MAX_B ? B - b0 : MAX_B;
-        e = launch(lc, k_lmhead<KV>, dim3(n_parts), dim3(WARPS * 32), (size_t)bc * C * sizeof(bf16),
-                   X + (size_t)b0 * C, bc, E, V, logits, part_val, part_idx, b0, B);
+    if (B > 8 && C == 1024) {
+        // 9..32 rows per pass on the tensor cores (the SIMT pass is compute-bound there)
+        for (int b0 = 0; b0 < B; b0 += MAX_B) {
+            const int bc = B - b0 < MAX_B ? B - b0 : MAX_B;
+            e = launch_lmhead_mma(lc, X + (size_t)b0 * C, bc, C, E, V, logits ? logits + (size_t)b0 * V : nullptr,
+                                  part_val + (size_t)b0 * n_parts, part_idx + (size_t)b0 * n_parts, n_parts, err);
+            if (e != cudaSuccess) return e;
+        }
+    } else {
+        e = cudaFuncSetAttribute(k_lmhead<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 MAX_B * KV * 256 * (int)sizeof(bf16));
         if (e != cudaSuccess) return e;
+        for (int b0 = 0; b0 < B; b0 += MAX_B) {
+            const int bc = B - b0 < MAX_B ? B - b0 : MAX_B;
+            e = launch(lc, k_lmhead<KV>, dim3(n_parts), dim3(WARPS * 32), (size_t)bc * C * sizeof(bf16),
+                       X + (size_t)b0 * C, bc, E, V, logits, part_val, part_idx, b0, B);
+            if (e != cudaSuccess) return e;
+        }
     }
     return launch(lc, k_argmax_reduce, dim3(B), dim3(256), 0, (const float *)part_val,
                   (const int32_t *)part_idx, n_parts, next_tok, r);
@@ -156,17 +167,17 @@ int lmhead_parts(int num_sms) { return num_sms * 4; }
 
 cudaError_t launch_lmhead_argmax(const Launch &lc, const bf16 *X, int B, int C, const bf16 *E,
                                  int V, float *logits, float *part_val, int32_t *part_idx,
-                                 int n_parts, int32_t *next_tok, const Rows &r) {
+                                 int n_parts, int32_t *next_tok, const Rows &r, uint32_t *err) {
     switch (C) {
-        case 256: return run<1>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
-        case 512: return run<2>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
-        case 768: return run<3>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
-        case 1024: return run<4>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
-        case 1536: return run<6>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
-        case 2048: return run<8>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
-        case 2560: return run<10>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
-        case 3072: return run<12>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
-        case 4096: return run<16>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r);
+        case 256: return run<1>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
+        case 512: return run<2>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
+        case 768: return run<3>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
+        case 1024: return run<4>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
+        case 1536: return run<6>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
+        case 2048: return run<8>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
+        case 2560: return run<10>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
+        case 3072: return run<12>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
+        case 4096: return run<16>(lc, X, B, E, V, logits, part_val, part_idx, n_parts, next_tok, r, err);
     }
     return cudaErrorInvalidValue;
 }

@@ -222,15 +222,28 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
                                          (const bf16 *)(ahead + L.o_wdown)));
             }
         } else if (decode) {
+            // larger batches: RMSNorm kernels + tensor-core projections (32 rows at a time)
+            auto proj = [&](const bf16 *X, int Kd, const bf16 *W, int N, int epi, void *out) -> cudaError_t {
+                for (int m0 = 0; m0 < R; m0 += 32) {
+                    const int mc = std::min(32, R - m0);
+                    const bf16 *Xc = X + (size_t)m0 * Kd;
+                    void *oc = epi == EPI_SWIGLU ? (void *)((bf16 *)out + (size_t)m0 * (N / 2))
+                                                 : (void *)((float *)out + (size_t)m0 * N);
+                    cudaError_t e = gemv_mma_supported(mc, Kd, N) ? launch_gemv_mma(lc, Xc, mc, Kd, W, N, epi, oc, err)
+                                                                  : launch_gemv(lc, Xc, mc, Kd, W, N, epi, oc);
+                    if (e != cudaSuccess) return e;
+                }
+                return cudaSuccess;
+            };
             if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
-            Q3_TRY(launch_gemv(lc, xn, R, C, w_qkv, qkv_n, EPI_F32, qkv));
+            Q3_TRY(proj(xn, C, w_qkv, qkv_n, EPI_F32, qkv));
             Q3_TRY(launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
                                             kps, c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
                                             c->at<int>(L.o_counters), attn, Hq, Hkv, k.max_ctx, k.rms_eps, err));
-            Q3_TRY(launch_gemv(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, resid));
+            Q3_TRY(proj(attn, Hq * D, w_o, C, EPI_RESID_ADD, resid));
             Q3_TRY(launch_rmsnorm(lc, resid, R, g_post, xn, C, k.rms_eps));
-            Q3_TRY(launch_gemv(lc, xn, R, C, w_gu, 2 * I, EPI_SWIGLU, act));
-            Q3_TRY(launch_gemv(lc, act, R, I, w_down, C, EPI_RESID_ADD, resid));
+            Q3_TRY(proj(xn, C, w_gu, 2 * I, EPI_SWIGLU, act));
+            Q3_TRY(proj(act, I, w_down, C, EPI_RESID_ADD, resid));
         } else {
             // prefill: tensor-core GEMMs (tcgen05, TMA) where the shape allows, else mma.sync
             auto gemm = [&](const bf16 *X, int Kd, const bf16 *W, int N, int epi, void *out) {
@@ -585,9 +598,13 @@ int qwen3_op_gemv(const void *x, int32_t M, int32_t K, const void *w, int32_t N,
         return QWEN3_E_INVALID;
     }
     const Launch lc = op_launch(stream);
-    cudaError_t e = gemv_fused_supported(M, K)
-                        ? launch_gemv_fused(lc, x, M, K, (const bf16 *)w, N, epi, out, nullptr, 0.0f, nullptr)
-                        : launch_gemv(lc, (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out);
+    cudaError_t e;
+    if (gemv_fused_supported(M, K))
+        e = launch_gemv_fused(lc, x, M, K, (const bf16 *)w, N, epi, out, nullptr, 0.0f, nullptr);
+    else if (gemv_mma_supported(M, K, N) && (K <= 2048 || epi == EPI_RESID_ADD))
+        e = launch_gemv_mma(lc, (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out, nullptr);
+    else
+        e = launch_gemv(lc, (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out);
     if (e != cudaSuccess) {
         g_create_error = std::string("qwen3_op_gemv: ") + cudaGetErrorString(e);
         return QWEN3_E_CUDA;

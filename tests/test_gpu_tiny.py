@@ -70,13 +70,15 @@ def test_graph_replay_matches_direct_launches(setup):
     """The recorded decode graph and one-by-one launches give the same tokens and logits.
 
     The decode MLP adds its split-K partial sums with fp32 atomics in an unspecified order, so
-    two runs may differ in the last bits: logits must agree to 1e-5 and tokens wherever the
-    top-2 gap of the logits is clear."""
+    the residual of two runs may differ in the last bits (~5e-7 relative).  Such a difference
+    occasionally flips the bf16 rounding of one element of a later GEMM operand, which moves
+    the logits by ~1e-4 relative: logits must agree to 1e-3 (ten times inside the parity
+    gate) and tokens wherever the top-2 gap of the logits is clear."""
     w, prompt, ref = setup
     a, _ = run_gpu(w, prompt, ref["fed"], flags=0, dump=False)
     b, _ = run_gpu(w, prompt, ref["fed"], flags=binding.QWEN3_FLAG_NO_GRAPH, dump=False)
     for x, y in zip(a, b):
-        assert gc.rel_l2(x["logits"], y["logits"]) <= 1e-5
+        assert gc.rel_l2(x["logits"], y["logits"]) <= 1e-3
         top2 = np.sort(y["logits"])[-2:]
         if top2[1] - top2[0] > 1e-3:
             assert x["token"] == y["token"]
