@@ -1,0 +1,369 @@
+// Causal GQA prefill attention on the 5th-generation tensor cores (flash-style, online softmax).
+//
+//   o_h[i] = sum_{j<=i} softmax_j(q_h[i] . k_g[j] / sqrt(128)) v_g[j],  g = h / (Hq/Hkv)
+// ("手写Qwen3-0.6B推理", Attention; "第 3 章", 3.3: lower-triangular mask, K/V shared by Hq/Hkv
+// query heads; "从零开始写Qwen3", Attn: scale 1/sqrt(D)).  Same contract as the mma.sync kernel
+// in attn_prefill.cu: q bf16 [N, Hq, 128] packed by cu_seqlens, K/V read from the layer's cache
+// [slot][Hkv][max_ctx][128], out bf16 [N, Hq*128].
+//
+// CTA = 128 queries x the 2 query heads of one KV head (the GQA pair shares every K/V tile);
+// 10 warps:
+//   warp 8 (1 thread): TMA -- both Q tiles once, then each K and V tile of 128 keys (128-byte
+//                      swizzle, two 64-column halves per tile);
+//   warp 9 (1 thread): MMA -- per key tile: S_h = Q_h K^T for both heads (M=128, N=128, K=128)
+//                      into TMEM, then, as each head's P is ready, O_h += P_h V (V read MN-major);
+//   warps 0-3 / 4-7:   one softmax warpgroup per head -- thread t owns query row t: it reads its
+//                      row of S_h (tcgen05.ld), applies the causal mask and the online softmax in
+//                      fp32, writes P (bf16) into shared memory in the swizzled K-major layout and
+//                      rescales its row of the TMEM accumulator O_h by exp(m_old - m_new) before
+//                      the next P V accumulates into it.
+// The two warpgroups work on their heads at the same time while the tensor core alternates
+// between them, so the exponentials of one head overlap the MMAs of the other.
+// Every mbarrier wait is bounded; on timeout the CTA flags ERR_TIMEOUT and skips to the end.
+
+#include <cuda.h>
+
+#include <mutex>
+
+#include "kernels.h"
+
+namespace q3 {
+
+namespace {
+
+constexpr int D = 128, BQ = 128, BK = 128, THREADS = 320;
+constexpr int TILE_BYTES = 128 * D * 2;  // a [128][128] bf16 tile as two 64-column halves
+constexpr int HALF_BYTES = TILE_BYTES / 2;
+constexpr int SMEM_BYTES = TILE_BYTES * 6 + 512 + 1024;  // Q0, Q1, K, V, P0, P1
+constexpr uint32_t TMEM_COLS = 512;  // S0: 0-127, S1: 128-255, O0: 256-383, O1: 384-511
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;  // 128-byte swizzle
+    return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, A K-major, B K-major
+// (b_mn = 0) or MN-major (b_mn = 1).
+__host__ __device__ constexpr uint32_t idesc(int m, int n, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+        "[%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void st32(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+        "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+        "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])),
+        "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+        "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])),
+        "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+struct Bars {
+    uint64_t q_full, kfull, kempty, vfull, vempty;
+    uint64_t s_full[2], p_full[2], o_full[2];
+    uint32_t tmem;
+};
+
+__global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    const __grid_constant__ CUtensorMap tmV, const int32_t *__restrict__ cu, const int32_t *__restrict__ slots,
+    bf16 *__restrict__ out, int Hq, int Hkv, int max_ctx, float scale_log2, uint32_t *err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *q_s = smem;                    // [2] tiles
+    uint8_t *k_s = q_s + 2 * TILE_BYTES;
+    uint8_t *v_s = k_s + TILE_BYTES;
+    uint8_t *p_s = v_s + TILE_BYTES;        // [2] tiles
+    Bars *bars = reinterpret_cast<Bars *>(p_s + 2 * TILE_BYTES);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y, b = blockIdx.z;  // longest tiles first
+    pdl_wait();
+    const int start = cu[b], len = cu[b + 1] - start;
+    const int q0 = qt * BQ;
+    if (q0 >= len) return;  // uniform: no barrier or TMEM touched yet
+    const int h0 = g * 2;    // the pair of query heads of KV head g (Hq == 2 Hkv)
+    const int kv_row0 = (slots[b] * Hkv + g) * max_ctx;  // first cache row of this (slot, head)
+    const int n_tiles = min((len + BK - 1) / BK, qt + 1);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->kfull, 1);
+        mbar_init(&bars->kempty, 1);
+        mbar_init(&bars->vfull, 1);
+        mbar_init(&bars->vempty, 1);
+        for (int hh = 0; hh < 2; ++hh) {
+            mbar_init(&bars->s_full[hh], 1);
+            mbar_init(&bars->p_full[hh], 128);
+            mbar_init(&bars->o_full[hh], 1);
+        }
+    }
+    if (warp == 9) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&bars->tmem)),
+                     "r"(TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = bars->tmem;
+
+    bool ok = true;
+    if (warp == 8) {
+        if (lane == 0) {
+            mbar_expect_tx(&bars->q_full, 2 * TILE_BYTES);
+            for (int hh = 0; hh < 2; ++hh) {
+                tma2d(q_s + hh * TILE_BYTES, &tmQ, (h0 + hh) * D, start + q0, &bars->q_full);
+                tma2d(q_s + hh * TILE_BYTES + HALF_BYTES, &tmQ, (h0 + hh) * D + 64, start + q0, &bars->q_full);
+            }
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                if (j > 0 && !mbar_wait_bounded(&bars->kempty, (j - 1) & 1, err)) { ok = false; break; }
+                mbar_expect_tx(&bars->kfull, TILE_BYTES);
+                tma2d(k_s, &tmK, 0, kv_row0 + j * BK, &bars->kfull);
+                tma2d(k_s + HALF_BYTES, &tmK, 64, kv_row0 + j * BK, &bars->kfull);
+                if (j > 0 && !mbar_wait_bounded(&bars->vempty, (j - 1) & 1, err)) { ok = false; break; }
+                mbar_expect_tx(&bars->vfull, TILE_BYTES);
+                tma2d(v_s, &tmV, 0, kv_row0 + j * BK, &bars->vfull);
+                tma2d(v_s + HALF_BYTES, &tmV, 64, kv_row0 + j * BK, &bars->vfull);
+            }
+        }
+    } else if (warp == 9) {
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc(BQ, BK, 0), id_o = idesc(BQ, D, 1);
+            ok = mbar_wait_bounded(&bars->q_full, 0, err);
+            const uint32_t ka = smem_addr(k_s), va = smem_addr(v_s);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                if (!mbar_wait_bounded(&bars->kfull, j & 1, err)) { ok = false; break; }
+                for (int hh = 0; hh < 2 && ok; ++hh) {
+                    // S_h of the previous tile has been read (its P is written) before it is overwritten
+                    if (j > 0 && !mbar_wait_bounded(&bars->p_full[hh], (j - 1) & 1, err)) { ok = false; break; }
+                    fence_after();
+                    const uint32_t qa = smem_addr(q_s + hh * TILE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+                        mma(tmem + hh * 128, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id_s, kk != 0);
+                    }
+                    commit(&bars->s_full[hh]);
+                }
+                if (!ok) break;
+                commit(&bars->kempty);
+                if (!mbar_wait_bounded(&bars->vfull, j & 1, err)) { ok = false; break; }
+                for (int hh = 0; hh < 2 && ok; ++hh) {
+                    if (!mbar_wait_bounded(&bars->p_full[hh], j & 1, err)) { ok = false; break; }
+                    fence_after();
+                    const uint32_t pa = smem_addr(p_s + hh * TILE_BYTES);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // P: K-major over keys; V: MN-major (dims contiguous), 16 keys = 2048 bytes
+                        const uint32_t poff = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+                        mma(tmem + 256 + hh * 128, sdesc(pa + poff, 16, 1024), sdesc(va + kk * 2048, HALF_BYTES, 1024),
+                            id_o, (j | kk) != 0);
+                    }
+                    commit(&bars->o_full[hh]);
+                }
+                if (!ok) break;
+                commit(&bars->vempty);
+            }
+        }
+    } else {
+        // softmax warpgroup hh = warp / 4 for query head h0 + hh; thread owns query row r
+        const int hh = warp >> 2;
+        const int r = (warp & 3) * 32 + lane;
+        const int qi = q0 + r;  // position within the sequence
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t t_s = tmem + hh * 128 + lane_base, t_o = tmem + 256 + hh * 128 + lane_base;
+        float m_run = -INFINITY, l_run = 0.0f;
+        uint8_t *prow = p_s + hh * TILE_BYTES + r * 128;  // this row inside each 64-column half
+        for (int j = 0; j < n_tiles; ++j) {
+            const bool got_s = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->s_full[hh], j & 1, err));
+            if (!got_s) { ok = false; break; }
+            fence_after();
+            const int k0 = j * BK;
+            // pass 1: row maximum of the visible scores
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                ld32(t_s + c * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int kj = k0 + c * 32 + i;
+                    if (kj <= qi && kj < len) mx = fmaxf(mx, v[i]);
+                }
+            }
+            const float m_new = fmaxf(m_run, mx * scale_log2);
+            const float corr = m_run == -INFINITY ? 0.0f : exp2f(m_run - m_new);
+            // pass 2: probabilities, row sum, P (bf16) in the swizzled K-major layout.  The
+            // tensor core finished the previous P V (it precedes this tile's S in issue order).
+            float sum = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                ld32(t_s + c * 32, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int kj = k0 + c * 32 + i;
+                    const float p0 = (kj <= qi && kj < len) ? exp2f(v[i] * scale_log2 - m_new) : 0.0f;
+                    const float p1 = (kj + 1 <= qi && kj + 1 < len) ? exp2f(v[i + 1] * scale_log2 - m_new) : 0.0f;
+                    sum += p0 + p1;
+                    pk[i / 2] = pack_bf16x2(p0, p1);
+                }
+                // 32 keys = 4 chunks of 16 bytes; chunk cc of the 64-key half at cc ^ (r & 7)
+                uint8_t *half = prow + (c >> 1) * HALF_BYTES;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int cc = (c & 1) * 4 + q;
+                    *reinterpret_cast<uint4 *>(half + ((cc ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
+            }
+            l_run = l_run * corr + sum;
+            m_run = m_new;
+            // O_h holds tiles < j (implied by s_full; waited so that o_full's phases stay in step)
+            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_full[hh], (j - 1) & 1, err))) {
+                ok = false;
+                break;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, corr != 1.0f)) {  // rescale this row of O_h
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    float v[32];
+                    ld32(t_o + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= corr;
+                    st32(t_o + c * 32, v);
+                }
+            }
+            // make the generic-proxy writes of P visible to the tensor core, then hand over
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            fence_before();
+            arrive(&bars->p_full[hh]);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_full[hh], (n_tiles - 1) & 1, err));
+        if (ok) {
+            fence_after();
+            const float inv = 1.0f / l_run;
+            uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)(start + qi) * Hq + h0 + hh) * D);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                ld32(t_o + c * 32, v);
+                if (qi < len) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[c * 4 + i] = make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                                    pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                                    pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                                    pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
+                }
+            }
+        }
+    }
+    pdl_trigger();
+    fence_before();
+    __syncthreads();
+    if (warp == 9) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &p, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [rows, cols] bf16 row-major, boxes of 64 columns x 128 rows, 128-byte swizzle
+bool map2d(CUtensorMap *m, const bf16 *base, uint64_t rows, uint64_t cols) {
+    EncodeTiledFn fn = encode();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16 *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool attn_prefill_tc_supported(int Hq, int Hkv) { return Hq == 2 * Hkv && encode() != nullptr; }
+
+cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const bf16 *k_layer,
+                                   const bf16 *v_layer, const int32_t *cu_seqlens, const int32_t *slots, int B,
+                                   int max_len, int max_seqs, bf16 *out, int Hq, int Hkv, int max_ctx,
+                                   uint32_t *err) {
+    CUtensorMap mq, mk, mv;
+    const uint64_t kv_rows = (uint64_t)max_seqs * Hkv * max_ctx;
+    if (!map2d(&mq, q, (uint64_t)N, (uint64_t)Hq * D) || !map2d(&mk, k_layer, kv_rows, D) ||
+        !map2d(&mv, v_layer, kv_rows, D))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_attn_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+    return launch(lc, k_attn_prefill_tc, dim3((max_len + BQ - 1) / BQ, Hkv, B), dim3(THREADS), SMEM_BYTES, mq, mk, mv,
+                  cu_seqlens, slots, out, Hq, Hkv, max_ctx, scale_log2, err);
+}
+
+}  // namespace q3

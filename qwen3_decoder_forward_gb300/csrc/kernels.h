@@ -138,6 +138,13 @@ cudaError_t launch_attn_prefill(const Launch &lc, const bf16 *q, const bf16 *k_l
                                 const int32_t *slots, int B, int max_len, bf16 *out, int Hq,
                                 int Hkv, int max_ctx);
 
+// --- attn_prefill_tc.cu (tcgen05 flash attention; q has N rows) ----------------------------
+bool attn_prefill_tc_supported(int Hq, int Hkv);
+cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const bf16 *k_layer,
+                                   const bf16 *v_layer, const int32_t *cu_seqlens, const int32_t *slots, int B,
+                                   int max_len, int max_seqs, bf16 *out, int Hq, int Hkv, int max_ctx,
+                                   uint32_t *err);
+
 // --- attn_decode.cu ----------------------------------------------------------------------
 cudaError_t launch_attn_decode(const Launch &lc, const bf16 *q, const bf16 *k_layer,
                                const bf16 *v_layer, const Rows &r, int n_split,

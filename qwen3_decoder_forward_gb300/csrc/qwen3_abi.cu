@@ -259,8 +259,12 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
                 Q3_TRY(launch_qknorm_rope_kv(lc, qkv, rows, g_q, g_k, rope, q, c->kcache(l), c->vcache(l), Hq,
                                              Hkv, k.max_ctx, k.rms_eps, err));
             }
-            Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots, rows.B,
-                                       max_len, attn, Hq, Hkv, k.max_ctx));
+            if (attn_prefill_tc_supported(Hq, Hkv))
+                Q3_TRY(launch_attn_prefill_tc(lc, q, R, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots,
+                                              rows.B, max_len, k.max_seqs, attn, Hq, Hkv, k.max_ctx, err));
+            else
+                Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots, rows.B,
+                                           max_len, attn, Hq, Hkv, k.max_ctx));
             Q3_TRY(gemm(attn, Hq * D, w_o, C, EPI_RESID_ADD, resid));
             Q3_TRY(launch_rmsnorm(lc, resid, R, g_post, xn, C, k.rms_eps));
             Q3_TRY(gemm(xn, C, w_gu, 2 * I, EPI_SWIGLU, act));
@@ -389,6 +393,11 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
             }
         Q3_TRY(cudaMemcpyAsync(c->arena + lay.o_rope, tab.data(), tab.size() * sizeof(float2),
                                cudaMemcpyHostToDevice, st));
+        // The KV cache starts at zero: the tensor-core prefill attention multiplies whole
+        // 128-key tiles, so rows past a sequence's end (weight 0) must hold finite values --
+        // zeros, or an earlier sequence's keys and values.
+        Q3_TRY(cudaMemsetAsync(c->arena + lay.o_kcache, 0, lay.kv_layer_bytes * cfg->n_layers, st));
+        Q3_TRY(cudaMemsetAsync(c->arena + lay.o_vcache, 0, lay.kv_layer_bytes * cfg->n_layers, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_ctxlen, 0, (size_t)cfg->max_seqs * 4, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_err, 0, 16, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_counters, 0, (size_t)cfg->max_seqs * cfg->n_kv_heads * 4, st));
