@@ -6,12 +6,12 @@
 // Hq/Hkv query heads of one KV head are served by the same CTA so each K/V row is read
 // from HBM once ("手写Qwen3-0.6B推理", Attention: K/V shared by a group of query heads).
 //
-// Pass 1, grid (split, kv head, sequence): 8 lanes per key (16 dims each), 4 keys per warp
-// and step; dot products reduced with 3 warp shuffles; an online softmax (m, l, acc) per
-// 8-lane group, merged across groups with shuffles and across the 4 warps in shared
-// memory.  Writes (m, l) and the unnormalised acc of its key range to a workspace.
-// Pass 2, grid (query head, sequence): the log-sum-exp merge of the splits.
-// Scores are pre-scaled by log2(e)/sqrt(128) so exp2 is used throughout.
+// Grid (split, kv head, sequence): 8 lanes per key (16 dims each), 4 keys per warp and step;
+// dot products reduced with 3 warp shuffles; an online softmax (m, l, acc) per 8-lane group,
+// merged across groups with shuffles and across the warps in shared memory.  Each split
+// writes (m, l) and the unnormalised acc of its key range to a workspace and the last CTA of
+// a (sequence, KV head) takes the log-sum-exp merge of the splits.  Scores are pre-scaled by
+// log2(e)/sqrt(128) so exp2 is used throughout.
 
 #include "kernels.h"
 
@@ -20,160 +20,7 @@ namespace q3 {
 namespace {
 
 constexpr int D = 128;
-constexpr int WARPS = 4;
-
-template <int G>
-__global__ void __launch_bounds__(WARPS * 32) k_attn_decode_split(
-    const bf16 *__restrict__ q, const bf16 *__restrict__ k_layer, const bf16 *__restrict__ v_layer,
-    Rows r, int kps, float *__restrict__ ws_ml, float *__restrict__ ws_o, int Hq, int Hkv,
-    int max_ctx, float scale_log2) {
-    __shared__ float red_ml[WARPS][G][2];
-    __shared__ float red_o[WARPS][G][D];
-    pdl_wait();
-    pdl_trigger();
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int n_split = gridDim.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane & 7, kg = lane >> 3;
-    const int slot = r.row_slot[b];
-    const int ctx = min(r.row_pos[b] + 1, max_ctx);
-    const int k_begin = split * kps;
-    const int k_end = min(ctx, k_begin + kps);
-
-    float qv[G][16];
-#pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-        const bf16 *qp = q + ((size_t)b * Hq + g * G + gi) * D + sub * 16;
-        float t[8];
-        unpack8(*reinterpret_cast<const uint4 *>(qp), t);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qv[gi][e] = t[e] * scale_log2;
-        unpack8(*reinterpret_cast<const uint4 *>(qp + 8), t);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qv[gi][8 + e] = t[e] * scale_log2;
-    }
-    float m[G], l[G], acc[G][16];
-#pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-        m[gi] = -INFINITY;
-        l[gi] = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[gi][e] = 0.0f;
-    }
-
-    const bf16 *kb = k_layer + ((size_t)slot * Hkv + g) * max_ctx * D + sub * 16;
-    const bf16 *vb = v_layer + ((size_t)slot * Hkv + g) * max_ctx * D + sub * 16;
-    for (int j0 = k_begin; j0 < k_end; j0 += WARPS * 4) {
-        const int j = j0 + warp * 4 + kg;
-        const bool valid = j < k_end;
-        uint4 k0, k1, v0, v1;
-        if (valid) {
-            k0 = ld_stream(kb + (size_t)j * D);
-            k1 = ld_stream(kb + (size_t)j * D + 8);
-            v0 = ld_stream(vb + (size_t)j * D);
-            v1 = ld_stream(vb + (size_t)j * D + 8);
-        } else {
-            k0 = k1 = v0 = v1 = make_uint4(0, 0, 0, 0);
-        }
-        float kf[16], vf[16];
-        unpack8(k0, kf);
-        unpack8(k1, kf + 8);
-        unpack8(v0, vf);
-        unpack8(v1, vf + 8);
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            float s = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) s = fmaf(qv[gi][e], kf[e], s);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            s += __shfl_xor_sync(0xffffffffu, s, 4);
-            if (valid) {
-                const float mn = fmaxf(m[gi], s);
-                const float c = exp2f(m[gi] - mn);
-                const float p = exp2f(s - mn);
-                l[gi] = l[gi] * c + p;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) acc[gi][e] = fmaf(p, vf[e], acc[gi][e] * c);
-                m[gi] = mn;
-            }
-        }
-    }
-    // Merge the four 8-lane key groups of the warp.
-#pragma unroll
-    for (int off = 8; off <= 16; off <<= 1) {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m[gi], off);
-            const float lo = __shfl_xor_sync(0xffffffffu, l[gi], off);
-            const float mn = fmaxf(m[gi], mo);
-            const float c1 = mn == -INFINITY ? 0.0f : exp2f(m[gi] - mn);
-            const float c2 = mn == -INFINITY ? 0.0f : exp2f(mo - mn);
-            l[gi] = l[gi] * c1 + lo * c2;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float ao = __shfl_xor_sync(0xffffffffu, acc[gi][e], off);
-                acc[gi][e] = acc[gi][e] * c1 + ao * c2;
-            }
-            m[gi] = mn;
-        }
-    }
-    if (kg == 0) {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) {
-            if (sub == 0) {
-                red_ml[warp][gi][0] = m[gi];
-                red_ml[warp][gi][1] = l[gi];
-            }
-#pragma unroll
-            for (int e = 0; e < 16; ++e) red_o[warp][gi][sub * 16 + e] = acc[gi][e];
-        }
-    }
-    __syncthreads();
-    // Merge the warps: thread t handles dims t (and t+128*k) of every head of the group.
-    for (int idx = threadIdx.x; idx < G * D; idx += WARPS * 32) {
-        const int gi = idx / D, d = idx % D;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w) mx = fmaxf(mx, red_ml[w][gi][0]);
-        float lsum = 0.0f, o = 0.0f;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w) {
-            const float c = mx == -INFINITY ? 0.0f : exp2f(red_ml[w][gi][0] - mx);
-            lsum += red_ml[w][gi][1] * c;
-            o += red_o[w][gi][d] * c;
-        }
-        const size_t part = ((size_t)b * Hq + g * G + gi) * n_split + split;
-        ws_o[part * D + d] = o;
-        if (d == 0) {
-            ws_ml[part * 2] = mx;
-            ws_ml[part * 2 + 1] = lsum;
-        }
-    }
-}
-
-__global__ void __launch_bounds__(D) k_attn_decode_combine(const float *__restrict__ ws_ml,
-                                                           const float *__restrict__ ws_o,
-                                                           int n_split, bf16 *__restrict__ out,
-                                                           int Hq) {
-    pdl_wait();
-    pdl_trigger();
-    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-    const size_t base = ((size_t)b * Hq + h) * n_split;
-    float mx = -INFINITY;
-    for (int s = 0; s < n_split; ++s) mx = fmaxf(mx, ws_ml[(base + s) * 2]);
-    float lsum = 0.0f, o = 0.0f;
-    for (int s = 0; s < n_split; ++s) {
-        const float ms = ws_ml[(base + s) * 2];
-        if (ms == -INFINITY) continue;
-        const float c = exp2f(ms - mx);
-        lsum += ws_ml[(base + s) * 2 + 1] * c;
-        o += ws_o[(base + s) * D + d] * c;
-    }
-    out[((size_t)b * Hq + h) * D + d] = __float2bfloat16(o / lsum);
-}
-
-// ---- fused variant: QK-norm + RoPE + KV write in the prologue, split merge by the last CTA --
+// QK-norm + RoPE + KV write in the prologue, split merge by the last CTA.
 //
 // Reads the new row's q/k/v straight from the QKV projection (fp32 [B, (Hq+2Hkv)*128]).
 // Each CTA normalises and rotates its query heads and the new key in registers (lane `sub`
@@ -189,33 +36,39 @@ __global__ void __launch_bounds__(D) k_attn_decode_combine(const float *__restri
 // are final, and the first stages are requested before the wait.  Only q/k/v of the new
 // row come from the immediately preceding kernel.
 //
+// Split s of n covers keys [s*per, min((s+1)*per, p+1)) with per = ceil((p+1)/n), taken from
+// the sequence's own position on the device: the ranges stay balanced for every length that
+// a recorded launch (a fixed n) serves.
+//
 // The CTA that finishes last for a (sequence, KV head) merges all splits (a counter per
 // pair, incremented after a memory fence and reset by that CTA): no second kernel and no
 // waiting on other CTAs.
 
-constexpr int STAGES = 4;
-// keys per ring stage for NW warps: at least 32, and one step of 4 keys per warp
-template <int NW> struct Ring {
-    static constexpr int CHUNK = NW * 4 > 32 ? NW * 4 : 32;
-    static constexpr int STAGE_BYTES = CHUNK * D * 2 * 2;  // K and V rows of one chunk
-};
+constexpr int STAGES = 3;
+constexpr int NW = 4;                        // warps per CTA
+constexpr int KPG = 4;                       // keys per 8-lane group and step
+constexpr int CHUNK = NW * 4 * KPG;          // keys per ring stage: one step of the CTA
+constexpr int STAGE_BYTES = CHUNK * D * 2 * 2;  // K and V rows of one chunk
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16(x)); }
 
-template <int G, int NW>
-__global__ void __launch_bounds__(NW * 32) k_attn_decode_fused(
+template <int G>
+__global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
     const float *__restrict__ qkv, Rows r, const float *__restrict__ q_gain,
     const float *__restrict__ k_gain, const float2 *__restrict__ rope, bf16 *__restrict__ k_layer,
-    bf16 *__restrict__ v_layer, int kps, float *__restrict__ ws_ml, float *__restrict__ ws_o,
+    bf16 *__restrict__ v_layer, float *__restrict__ ws_ml, float *__restrict__ ws_o,
     int *__restrict__ counters, bf16 *__restrict__ out, int Hq, int Hkv, int max_ctx, float eps,
     float scale_log2, uint32_t *err) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int CHUNK = Ring<NW>::CHUNK, STAGE_BYTES = Ring<NW>::STAGE_BYTES;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);              // [STAGES]
     uint8_t *ring = smem + 128;                                        // [STAGES][K | V]
     float *s_new = reinterpret_cast<float *>(ring + STAGES * STAGE_BYTES);  // new K, new V [2][D]
-    __shared__ float red_ml[NW][G][2];
-    __shared__ float red_o[NW][G][D];
+    // after the key loop the ring is free: the cross-warp and cross-split merges reuse it
+    float(*red_o)[G][D] = reinterpret_cast<float(*)[G][D]>(ring);                         // [NW]
+    float(*red_ml)[G][2] = reinterpret_cast<float(*)[G][2]>(ring + NW * G * D * 4);       // [NW]
+    float(*sp_w)[ATTN_DECODE_MAX_SPLIT] =
+        reinterpret_cast<float(*)[ATTN_DECODE_MAX_SPLIT]>(ring + NW * G * (D + 2) * 4);  // [G]
+    __shared__ float s_lsum[G];
     __shared__ int s_last;
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -228,8 +81,9 @@ __global__ void __launch_bounds__(NW * 32) k_attn_decode_fused(
     const int slot = __ldcg(r.row_slot + b);
     const int pos = __ldcg(r.row_pos + b);
     const bool pos_ok = pos < max_ctx;
-    const int k_begin = split * kps;
-    const int k_end = pos_ok ? min(pos + 1, k_begin + kps) : k_begin;
+    const int per = (pos + n_split) / n_split;  // ceil((pos + 1) / n_split)
+    const int k_begin = split * per;
+    const int k_end = pos_ok ? min(pos + 1, k_begin + per) : k_begin;
     const int cache_end = max(k_begin, min(k_end, pos));  // cached keys [k_begin, cache_end)
     const int n_chunks = (cache_end - k_begin + CHUNK - 1) / CHUNK;
     const size_t head_base = ((size_t)slot * Hkv + g) * max_ctx * D;
@@ -330,28 +184,52 @@ __global__ void __launch_bounds__(NW * 32) k_attn_decode_fused(
 #pragma unroll
         for (int e = 0; e < 16; ++e) acc[gi][e] = 0.0f;
     }
-    auto update = [&](const float *kf, const float *vf, bool valid) {
+    // KPG keys of this 8-lane group: scores, one max and one rescale for all of them
+    auto update = [&](const float (*kf)[16], const float (*vf)[16], const bool *valid) {
 #pragma unroll
         for (int gi = 0; gi < G; ++gi) {
-            float s = 0.0f;
+            float sc[KPG];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) s = fmaf(qv[gi][e], kf[e], s);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            s += __shfl_xor_sync(0xffffffffu, s, 2);
-            s += __shfl_xor_sync(0xffffffffu, s, 4);
-            if (valid) {
-                const float mn = fmaxf(m[gi], s);
+            for (int kk = 0; kk < KPG; ++kk) {
+                float t = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) t = fmaf(qv[gi][e], kf[kk][e], t);
+                sc[kk] = t;
+            }
+#pragma unroll
+            for (int kk = 0; kk < KPG; ++kk) sc[kk] += __shfl_xor_sync(0xffffffffu, sc[kk], 1);
+#pragma unroll
+            for (int kk = 0; kk < KPG; ++kk) sc[kk] += __shfl_xor_sync(0xffffffffu, sc[kk], 2);
+#pragma unroll
+            for (int kk = 0; kk < KPG; ++kk) sc[kk] += __shfl_xor_sync(0xffffffffu, sc[kk], 4);
+            float mn = m[gi];
+#pragma unroll
+            for (int kk = 0; kk < KPG; ++kk)
+                if (valid[kk]) mn = fmaxf(mn, sc[kk]);
+            if (mn != -INFINITY) {  // some key of the group seen so far
                 const float c = exp2f(m[gi] - mn);
-                const float p = exp2f(s - mn);
-                l[gi] = l[gi] * c + p;
+                float p[KPG];
+                float ps = 0.0f;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) acc[gi][e] = fmaf(p, vf[e], acc[gi][e] * c);
+                for (int kk = 0; kk < KPG; ++kk) {
+                    p[kk] = valid[kk] ? exp2f(sc[kk] - mn) : 0.0f;
+                    ps += p[kk];
+                }
+                l[gi] = l[gi] * c + ps;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float a = acc[gi][e] * c;
+#pragma unroll
+                    for (int kk = 0; kk < KPG; ++kk) a = fmaf(p[kk], vf[kk][e], a);
+                    acc[gi][e] = a;
+                }
                 m[gi] = mn;
             }
         }
     };
 
     bool ok = true;
+    const int j0 = (warp * 4 + kg) * KPG;  // this group's first key in each chunk
     for (int c = 0; c < n_chunks; ++c) {
         const int st = c % STAGES;
         const bool late = !mbar_wait_bounded(&full[st], (c / STAGES) & 1, err);
@@ -362,20 +240,20 @@ __global__ void __launch_bounds__(NW * 32) k_attn_decode_fused(
         const uint8_t *ks = ring + st * STAGE_BYTES;
         const uint8_t *vs = ks + CHUNK * D * 2;
         const int n = min(CHUNK, cache_end - (k_begin + c * CHUNK));
+        float kf[KPG][16], vf[KPG][16];
+        bool valid[KPG];
 #pragma unroll
-        for (int it = 0; it < CHUNK / (NW * 4); ++it) {
-            const int jj = it * NW * 4 + warp * 4 + kg;
-            const bool valid = jj < n;
-            const int js = valid ? jj : 0;
+        for (int kk = 0; kk < KPG; ++kk) {
+            valid[kk] = j0 + kk < n;
+            const int js = valid[kk] ? j0 + kk : 0;
             const uint4 *kp = reinterpret_cast<const uint4 *>(ks + (size_t)js * D * 2 + sub * 32);
             const uint4 *vp = reinterpret_cast<const uint4 *>(vs + (size_t)js * D * 2 + sub * 32);
-            float kf[16], vf[16];
-            unpack8(kp[0], kf);
-            unpack8(kp[1], kf + 8);
-            unpack8(vp[0], vf);
-            unpack8(vp[1], vf + 8);
-            update(kf, vf, valid);
+            unpack8(kp[0], kf[kk]);
+            unpack8(kp[1], kf[kk] + 8);
+            unpack8(vp[0], vf[kk]);
+            unpack8(vp[1], vf[kk] + 8);
         }
+        update(kf, vf, valid);
         __syncthreads();  // every warp is done with stage st
         if (threadIdx.x == 0 && c + STAGES < n_chunks) issue(c + STAGES);
     }
@@ -386,13 +264,18 @@ __global__ void __launch_bounds__(NW * 32) k_attn_decode_fused(
     }
     __syncthreads();  // s_new is visible
     if (warp == 0 && k_begin <= pos && pos < k_end) {  // the new key, from shared memory
-        float kf[16], vf[16];
+        float kf[KPG][16], vf[KPG][16];
+        bool valid[KPG];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            kf[e] = s_new[sub * 16 + e];
-            vf[e] = s_new[D + sub * 16 + e];
+        for (int kk = 0; kk < KPG; ++kk) {
+            valid[kk] = kk == 0 && kg == 0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                kf[kk][e] = s_new[sub * 16 + e];
+                vf[kk][e] = s_new[D + sub * 16 + e];
+            }
         }
-        update(kf, vf, kg == 0);
+        update(kf, vf, valid);
     }
 
 #pragma unroll
@@ -456,85 +339,91 @@ __global__ void __launch_bounds__(NW * 32) k_attn_decode_fused(
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    // weights of the splits: exp2(m_s - max) per query head, and the merged denominator
+    if (threadIdx.x < G) {
+        const int gi = threadIdx.x;
+        const size_t base = ((size_t)b * Hq + g * G + gi) * n_split;
+        float mx = -INFINITY;
+        for (int sp = 0; sp < n_split; ++sp) mx = fmaxf(mx, __ldcg(ws_ml + (base + sp) * 2));
+        float lsum = 0.0f;
+        for (int sp = 0; sp < n_split; ++sp) {
+            const float ms = __ldcg(ws_ml + (base + sp) * 2);
+            const float w = ms == -INFINITY ? 0.0f : exp2f(ms - mx);
+            sp_w[gi][sp] = w;
+            lsum += __ldcg(ws_ml + (base + sp) * 2 + 1) * w;
+        }
+        s_lsum[gi] = lsum;
+    }
+    __syncthreads();
     for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
         const int gi = idx / D, d = idx % D;
         const int h = g * G + gi;
-        const size_t base = ((size_t)b * Hq + h) * n_split;
-        float mx = -INFINITY;
-        for (int sp = 0; sp < n_split; ++sp) mx = fmaxf(mx, __ldcg(ws_ml + (base + sp) * 2));
-        float lsum = 0.0f, o = 0.0f;
-        for (int sp = 0; sp < n_split; ++sp) {
-            const float ms = __ldcg(ws_ml + (base + sp) * 2);
-            if (ms == -INFINITY) continue;
-            const float c = exp2f(ms - mx);
-            lsum += __ldcg(ws_ml + (base + sp) * 2 + 1) * c;
-            o += __ldcg(ws_o + (base + sp) * D + d) * c;
-        }
-        out[((size_t)b * Hq + h) * D + d] = __float2bfloat16(o / lsum);
+        const float *po = ws_o + ((size_t)b * Hq + h) * n_split * D + d;
+        float o = 0.0f;
+#pragma unroll 8
+        for (int sp = 0; sp < n_split; ++sp) o = fmaf(__ldcg(po + (size_t)sp * D), sp_w[gi][sp], o);
+        out[((size_t)b * Hq + h) * D + d] = __float2bfloat16(o / s_lsum[gi]);
     }
     if (threadIdx.x == 0) counters[b * Hkv + g] = 0;
 }
 
-template <int G, int NW>
+constexpr size_t SMEM_BYTES = 128 + (size_t)STAGES * STAGE_BYTES + 2 * D * sizeof(float);
+
+template <int G>
 cudaError_t run_fused(const Launch &lc, const float *qkv, const Rows &r, const float *q_gain,
                       const float *k_gain, const float2 *rope, bf16 *k_layer, bf16 *v_layer, int n_split,
-                      int kps, float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq, int Hkv,
+                      float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq, int Hkv,
                       int max_ctx, float eps, uint32_t *err) {
+    static_assert(NW * G * (D + 2) * 4 + G * ATTN_DECODE_MAX_SPLIT * 4 <= STAGES * STAGE_BYTES,
+                  "merge scratch fits in the ring");
+    if (n_split < 1 || n_split > ATTN_DECODE_MAX_SPLIT) return cudaErrorInvalidValue;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-    const size_t smem = 128 + (size_t)STAGES * Ring<NW>::STAGE_BYTES + 2 * D * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_fused<G, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_fused<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    return launch(lc, k_attn_decode_fused<G, NW>, dim3(n_split, Hkv, r.B), dim3(NW * 32), smem, qkv, r, q_gain,
-                  k_gain, rope, k_layer, v_layer, kps, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps,
+    return launch(lc, k_attn_decode_fused<G>, dim3(n_split, Hkv, r.B), dim3(NW * 32), SMEM_BYTES, qkv, r, q_gain,
+                  k_gain, rope, k_layer, v_layer, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps,
                   scale_log2, err);
 }
 
 template <int G>
-cudaError_t run(const Launch &lc, const bf16 *q, const bf16 *k_layer, const bf16 *v_layer,
-                const Rows &r, int n_split, int kps, float *ws_ml, float *ws_o, bf16 *out, int Hq,
-                int Hkv, int max_ctx) {
-    const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-    cudaError_t e = launch(lc, k_attn_decode_split<G>, dim3(n_split, Hkv, r.B), dim3(WARPS * 32), 0,
-                           q, k_layer, v_layer, r, kps, ws_ml, ws_o, Hq, Hkv, max_ctx, scale_log2);
-    if (e != cudaSuccess) return e;
-    return launch(lc, k_attn_decode_combine, dim3(Hq, r.B), dim3(D), 0, (const float *)ws_ml,
-                  (const float *)ws_o, n_split, out, Hq);
+int ctas_per_sm() {
+    int n = 0;
+    if (cudaFuncSetAttribute(k_attn_decode_fused<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn_decode_fused<G>, NW * 32, SMEM_BYTES) !=
+            cudaSuccess)
+        return 1;
+    return n < 1 ? 1 : n;
 }
 
 }  // namespace
 
-cudaError_t launch_attn_decode(const Launch &lc, const bf16 *q, const bf16 *k_layer,
-                               const bf16 *v_layer, const Rows &r, int n_split,
-                               int keys_per_split, float *ws_ml, float *ws_o, bf16 *out, int Hq,
-                               int Hkv, int max_ctx) {
-    switch (Hq / Hkv) {
-        case 1: return run<1>(lc, q, k_layer, v_layer, r, n_split, keys_per_split, ws_ml, ws_o, out, Hq, Hkv, max_ctx);
-        case 2: return run<2>(lc, q, k_layer, v_layer, r, n_split, keys_per_split, ws_ml, ws_o, out, Hq, Hkv, max_ctx);
-        case 4: return run<4>(lc, q, k_layer, v_layer, r, n_split, keys_per_split, ws_ml, ws_o, out, Hq, Hkv, max_ctx);
-        case 8: return run<8>(lc, q, k_layer, v_layer, r, n_split, keys_per_split, ws_ml, ws_o, out, Hq, Hkv, max_ctx);
-    }
-    return cudaErrorInvalidValue;
-}
-
 cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const Rows &r,
                                      const float *q_gain, const float *k_gain, const float2 *rope,
-                                     bf16 *k_layer, bf16 *v_layer, int n_split, int keys_per_split,
+                                     bf16 *k_layer, bf16 *v_layer, int n_split,
                                      float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
                                      int Hkv, int max_ctx, float eps, uint32_t *err) {
-    // one wide CTA per (sequence, KV head) when a single split covers the context: the
-    // latency-bound case (one or two short sequences); otherwise 4-warp CTAs over many splits
-    const bool wide = n_split == 1;
-#define Q3_ATTN(GG, NWW) run_fused<GG, NWW>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, \
-                                             keys_per_split, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, err)
+#define Q3_ATTN(GG) run_fused<GG>(lc, qkv, r, q_gain, k_gain, rope, k_layer, v_layer, n_split, ws_ml, ws_o, \
+                                  counters, out, Hq, Hkv, max_ctx, eps, err)
     switch (Hq / Hkv) {
-        case 1: return wide ? Q3_ATTN(1, 16) : Q3_ATTN(1, 4);
-        case 2: return wide ? Q3_ATTN(2, 16) : Q3_ATTN(2, 4);
-        case 4: return wide ? Q3_ATTN(4, 16) : Q3_ATTN(4, 4);
-        case 8: return wide ? Q3_ATTN(8, 16) : Q3_ATTN(8, 4);
+        case 1: return Q3_ATTN(1);
+        case 2: return Q3_ATTN(2);
+        case 4: return Q3_ATTN(4);
+        case 8: return Q3_ATTN(8);
     }
 #undef Q3_ATTN
     return cudaErrorInvalidValue;
+}
+
+int attn_decode_ctas_per_sm(int Hq, int Hkv) {
+    switch (Hq / Hkv) {
+        case 1: return ctas_per_sm<1>();
+        case 2: return ctas_per_sm<2>();
+        case 4: return ctas_per_sm<4>();
+        case 8: return ctas_per_sm<8>();
+    }
+    return 1;
 }
 
 }  // namespace q3

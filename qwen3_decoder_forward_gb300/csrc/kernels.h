@@ -146,18 +146,19 @@ cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const
                                    uint32_t *err);
 
 // --- attn_decode.cu ----------------------------------------------------------------------
-cudaError_t launch_attn_decode(const Launch &lc, const bf16 *q, const bf16 *k_layer,
-                               const bf16 *v_layer, const Rows &r, int n_split,
-                               int keys_per_split, float *ws_ml, float *ws_o, bf16 *out, int Hq,
-                               int Hkv, int max_ctx);
+// Most key ranges per (sequence, KV head) of the decode attention.
+constexpr int ATTN_DECODE_MAX_SPLIT = 64;
+// CTAs of the decode attention that one SM holds at once.
+int attn_decode_ctas_per_sm(int Hq, int Hkv);
 
 // Decode attention fed directly by the QKV projection (fp32 [B, (Hq+2Hkv)*D]): per-head
 // QK-norm + RoPE + KV-cache write of the new row, attention over keys 0..pos, and the
-// merge of the n_split key ranges by the last CTA of each (sequence, KV head).  counters
+// merge of the n_split key ranges (balanced over keys 0..pos on the device) by the last CTA
+// of each (sequence, KV head).  counters
 // [max_seqs * Hkv] must be zero on entry and are left zero.
 cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const Rows &r,
                                      const float *q_gain, const float *k_gain, const float2 *rope,
-                                     bf16 *k_layer, bf16 *v_layer, int n_split, int keys_per_split,
+                                     bf16 *k_layer, bf16 *v_layer, int n_split,
                                      float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
                                      int Hkv, int max_ctx, float eps, uint32_t *err);
 

@@ -18,7 +18,7 @@ using namespace q3;
 namespace {
 
 constexpr size_t ALIGN = 1024;
-constexpr int MAX_SPLIT = 64;   // decode attention: key ranges per (sequence, head)
+constexpr int MAX_SPLIT = ATTN_DECODE_MAX_SPLIT;  // decode attention: key ranges per (sequence, head)
 constexpr int MAX_PARTS = 1024; // lm_head partial results per row
 
 size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
@@ -119,7 +119,7 @@ void set_last_error(const std::string &msg) { g_create_error = msg; }
 }  // namespace q3
 
 struct GraphEntry {
-    int B, n_split, kps;
+    int B, n_split;
     const void *tokens, *slots;
     void *logits, *next;
     cudaGraphExec_t exec;
@@ -131,7 +131,7 @@ struct qwen3_ctx {
     Layout lay;
     uint8_t *arena = nullptr;
     std::vector<int32_t> len_host;
-    int num_sms = 0, n_parts = 0;
+    int num_sms = 0, n_parts = 0, attn_ctas_per_sm = 1;
     float *dump = nullptr;
     size_t dump_bytes = 0;
     cudaStream_t cap_stream = nullptr;
@@ -165,7 +165,7 @@ namespace {
 // Everything one call runs, in stream order.  `decode` selects the GEMV projections and the
 // split-KV attention; prefill uses the tiled GEMM and the flash prefill attention.
 cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, const Rows &rows,
-                        bool decode, int max_len, int n_split, int kps, float *logits,
+                        bool decode, int max_len, int n_split, float *logits,
                         int32_t *next) {
     const qwen3_config &k = c->cfg;
     const Layout &L = c->lay;
@@ -207,7 +207,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
             Q3_TRY(launch_gemv_fused(lc, r_cur, R, C, w_qkv, qkv_n, EPI_F32, qkv, g_in, k.rms_eps, err,
                                      (const bf16 *)(ahead + L.o_wqkv), mlp ? r_next : nullptr, R * C));
             Q3_TRY(launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
-                                            kps, c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
+                                            c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
                                             c->at<int>(L.o_counters), attn, Hq, Hkv, k.max_ctx, k.rms_eps, err));
             Q3_TRY(launch_gemv_fused(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, r_cur, nullptr, 0.0f, err,
                                      (const bf16 *)(ahead + L.o_wo)));
@@ -238,7 +238,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
             if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
             Q3_TRY(proj(xn, C, w_qkv, qkv_n, EPI_F32, qkv));
             Q3_TRY(launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
-                                            kps, c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
+                                            c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
                                             c->at<int>(L.o_counters), attn, Hq, Hkv, k.max_ctx, k.rms_eps, err));
             Q3_TRY(proj(attn, Hq * D, w_o, C, EPI_RESID_ADD, resid));
             Q3_TRY(launch_rmsnorm(lc, resid, R, g_post, xn, C, k.rms_eps));
@@ -349,6 +349,7 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
     c->len_host.assign(cfg->max_seqs, 0);
     c->num_sms = prop.multiProcessorCount;
     c->n_parts = std::min(lmhead_parts(c->num_sms), MAX_PARTS);
+    c->attn_ctas_per_sm = attn_decode_ctas_per_sm(cfg->n_q_heads, cfg->n_kv_heads);
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);
     Launch lc;
     lc.stream = st;
@@ -441,7 +442,7 @@ int qwen3_prefill(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev
     lc.num_sms = c->num_sms;
     lc.counter = &c->launches;
     const Rows rows = make_rows(c, cu_dev, slots_dev, B, N);
-    cudaError_t e = run_forward(c, lc, tokens_dev, rows, false, max_len, 0, 0, logits_dev, next_tok_dev);
+    cudaError_t e = run_forward(c, lc, tokens_dev, rows, false, max_len, 0, logits_dev, next_tok_dev);
     if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_prefill");
     for (int b = 0; b < B; ++b) c->len_host[slots_host[b]] = cu_host[b + 1] - cu_host[b];
     return QWEN3_OK;
@@ -471,12 +472,12 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
     int bucket = 64;
     while (bucket < max_len) bucket <<= 1;
     bucket = std::min(bucket, c->cfg.max_ctx);
-    const int want = (4 * c->num_sms + B * c->cfg.n_kv_heads - 1) / (B * c->cfg.n_kv_heads);
-    // One or two short sequences: a single wide CTA per KV head (no cross-CTA merge on the
-    // critical path).  Otherwise enough splits to give every SM several CTAs.
-    const bool latency_mode = false;  // (a single wide CTA per KV head measured no faster)
-    const int n_split = latency_mode ? 1 : std::max(1, std::min({want, MAX_SPLIT, (bucket + 63) / 64}));
-    const int kps = ((bucket + n_split - 1) / n_split + 15) / 16 * 16;
+    // One wave of the decode attention: as many key ranges per (sequence, KV head) as the SMs
+    // hold CTAs for all pairs at once, ranges of at least 64 keys.  The kernel divides the
+    // actual keys 0..pos of each sequence evenly over the ranges.
+    const int pairs = B * c->cfg.n_kv_heads;
+    const int slots = c->num_sms * c->attn_ctas_per_sm;
+    const int n_split = std::max(1, std::min({slots / pairs, MAX_SPLIT, (bucket + 63) / 64}));
 
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);
     const Rows rows = make_rows(c, nullptr, slots_dev, B, B);
@@ -487,12 +488,12 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
         lc.pdl = !(c->cfg.flags & QWEN3_FLAG_NO_PDL);
         lc.num_sms = c->num_sms;
         lc.counter = &c->launches;
-        cudaError_t e = run_forward(c, lc, tokens_dev, rows, true, 0, n_split, kps, logits_dev, next_tok_dev);
+        cudaError_t e = run_forward(c, lc, tokens_dev, rows, true, 0, n_split, logits_dev, next_tok_dev);
         if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_decode_step");
     } else {
         GraphEntry *g = nullptr;
         for (auto &x : c->graphs)
-            if (x.B == B && x.n_split == n_split && x.kps == kps && x.tokens == tokens_dev &&
+            if (x.B == B && x.n_split == n_split && x.tokens == tokens_dev &&
                 x.slots == slots_dev && x.logits == logits_dev && x.next == next_tok_dev)
                 g = &x;
         if (!g) {
@@ -502,7 +503,7 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
             lc.num_sms = c->num_sms;
             cudaError_t e = cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal);
             if (e != cudaSuccess) return c->cuda_fail(e, "cudaStreamBeginCapture");
-            e = run_forward(c, lc, tokens_dev, rows, true, 0, n_split, kps, logits_dev, next_tok_dev);
+            e = run_forward(c, lc, tokens_dev, rows, true, 0, n_split, logits_dev, next_tok_dev);
             cudaGraph_t graph = nullptr;
             const cudaError_t e2 = cudaStreamEndCapture(c->cap_stream, &graph);
             if (e != cudaSuccess || e2 != cudaSuccess) {
@@ -526,7 +527,7 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
                 if (exec) cudaGraphExecDestroy(exec);
                 return c->cuda_fail(e, "decode graph instantiate");
             }
-            c->graphs.push_back(GraphEntry{B, n_split, kps, tokens_dev, slots_dev, logits_dev,
+            c->graphs.push_back(GraphEntry{B, n_split, tokens_dev, slots_dev, logits_dev,
                                            next_tok_dev, exec, kernels});
             g = &c->graphs.back();
         }
