@@ -46,8 +46,10 @@ def parse_args():
     p.add_argument("--workload", default="decode_b1")
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--launch", default="graph", choices=["graph", "graph-nopdl", "direct"],
-                   help="direct: decode steps launched kernel by kernel, without PDL (for profilers)")
+    p.add_argument("--launch", default="graph", choices=["graph", "graph-nopdl", "direct", "persistent"],
+                   help="graph: decode steps as a CUDA graph of the kernel chain; direct: kernel by kernel "
+                        "without PDL (for profilers); persistent: steps of up to 8 sequences as one "
+                        "persistent kernel")
     p.add_argument("--decode-steps", type=int, default=None,
                    help="override the workload's decode steps (shorter runs for profilers)")
     return p.parse_args()
@@ -398,7 +400,8 @@ def gpu_arm(args, wl):
     device = torch.device("cuda", local_rank)
     peaks, peak_kind = load_peaks()
     flags = {"graph": 0, "graph-nopdl": binding.QWEN3_FLAG_NO_PDL,
-             "direct": binding.QWEN3_FLAG_NO_GRAPH | binding.QWEN3_FLAG_NO_PDL}[args.launch]
+             "direct": binding.QWEN3_FLAG_NO_GRAPH | binding.QWEN3_FLAG_NO_PDL,
+             "persistent": binding.QWEN3_FLAG_PERSISTENT}[args.launch]
     runner = GpuRunner(wl, device, flags)
     units, unit = units_per_step(wl)
 

@@ -54,6 +54,8 @@ extern "C" {
 /* qwen3_config.flags */
 #define QWEN3_FLAG_NO_GRAPH 1u   /* launch decode steps one kernel at a time instead of a CUDA graph */
 #define QWEN3_FLAG_NO_PDL 2u     /* launch kernels without programmatic dependent launch (for profilers) */
+#define QWEN3_FLAG_PERSISTENT 4u /* decode steps of up to 8 sequences as one persistent kernel
+                                    (Qwen3-0.6B widths only; see qwen3_decode_step) */
 
 /* Model and capacity.  Supported: head_dim == 128; n_q_heads a multiple of n_kv_heads with
  * n_q_heads / n_kv_heads <= 8; hidden, n_q_heads*head_dim and intermediate multiples of 256;
@@ -127,10 +129,13 @@ int qwen3_prefill(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *cu_s
  * slots[b] at position = the slot's current length, attends to keys 0..position, and
  * next_tok_dev[b] receives the greedy next token (logits_dev[B, V] too if not NULL).  Each
  * slot's length grows by one.  next_tok_dev may be passed as the next step's tokens_dev.
- * Unless QWEN3_FLAG_NO_GRAPH is set, the step is recorded once per (B, pointers, split
- * plan) as a CUDA graph and replayed.  Errors: E_INVALID (NULL, B < 1, repeated slot, slot
- * never prefilled), E_CAPACITY (B > max_seqs, a slot already holding max_ctx tokens),
- * E_CUDA. */
+ * With QWEN3_FLAG_PERSISTENT, B <= 8 and the Qwen3-0.6B widths (hidden 1024, 16/8 heads,
+ * head_dim 128) the whole step is one persistent kernel with one CTA per SM (cooperative
+ * launch; it needs the whole GPU, so other work on the device waits for it).  Otherwise,
+ * unless QWEN3_FLAG_NO_GRAPH is set, the step's kernel chain is recorded once per (B,
+ * pointers, split plan) as a CUDA graph and replayed.  Errors: E_INVALID (NULL, B < 1,
+ * repeated slot, slot never prefilled), E_CAPACITY (B > max_seqs, a slot already holding
+ * max_ctx tokens), E_CUDA. */
 int qwen3_decode_step(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *slots_dev,
                       const int32_t *slots_host, int32_t B, float *logits_dev,
                       int32_t *next_tok_dev, void *stream);

@@ -20,17 +20,18 @@ namespace {
 constexpr size_t ALIGN = 1024;
 constexpr int MAX_SPLIT = ATTN_DECODE_MAX_SPLIT;  // decode attention: key ranges per (sequence, head)
 constexpr int MAX_PARTS = 1024; // lm_head partial results per row
+constexpr int PFLAG_WORDS = 64;  // persistent decode: [0] all-CTA arrivals, [1] argmax counter, [8, 8+Hkv) groups
 
 size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
 struct Layout {
     // per-layer strides (bytes) and offsets within layer 0
-    size_t layer_bytes = 0, o_wqkv = 0, o_wo = 0, o_wgu = 0, o_wdown = 0, o_wdownT = 0, o_gin = 0,
+    size_t layer_bytes = 0, o_wqkv = 0, o_wo = 0, o_wog = 0, o_wgu = 0, o_wdown = 0, o_wdownT = 0, o_gin = 0,
            o_gpost = 0, o_gq = 0, o_gk = 0;
     size_t o_layers = 0, o_embed = 0, o_gfinal = 0, o_rope = 0, o_kcache = 0, o_vcache = 0,
            kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0;
     size_t o_resid = 0, o_xn = 0, o_qkv = 0, o_q = 0, o_attn = 0, o_act = 0, o_rowslot = 0,
-           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0,
+           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0, o_pflags = 0, o_pres = 0,
            o_resid2 = 0;
     size_t total = 0;
 };
@@ -72,6 +73,7 @@ Layout make_layout(const qwen3_config &c) {
     // one layer's block
     L.o_wqkv = take(qkv_n * C * 2);
     L.o_wo = take(C * Hq * D * 2);
+    L.o_wog = take(C * Hq * D * 2);  // o_proj regrouped by KV head [Hkv][C][Hq/Hkv*D] (persistent decode)
     L.o_wgu = take(2 * I * C * 2);
     L.o_wdown = take(C * I * 2);
     L.o_wdownT = take(C * I * 2);  // down weight transposed [I, C] for the split-K decode MLP
@@ -106,6 +108,8 @@ Layout make_layout(const qwen3_config &c) {
     L.o_wso = take((size_t)c.max_seqs * Hq * MAX_SPLIT * D * 4);
     L.o_counters = take((size_t)c.max_seqs * Hkv * 4);
     L.o_resid2 = take((size_t)c.max_seqs * C * 4);  // second residual buffer of the decode ping-pong
+    L.o_pflags = take(PFLAG_WORDS * 4);  // persistent decode: arrival counters, argmax counter
+    L.o_pres = take((size_t)3 * c.max_seqs * C * 4);  // persistent decode: three residual buffers
     L.total = off;
     return L;
 }
@@ -370,6 +374,12 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
             Q3_TRY(d2d(lw + lay.o_wqkv + Hq * D * C * 2, w->wk[l], Hkv * D * C * 2));
             Q3_TRY(d2d(lw + lay.o_wqkv + (Hq + Hkv) * D * C * 2, w->wv[l], Hkv * D * C * 2));
             Q3_TRY(d2d(lw + lay.o_wo, w->wo[l], C * Hq * D * 2));
+            // the same o_proj with the columns of each KV head's query heads stored together
+            const size_t gcols = Hq / Hkv * D;
+            for (size_t g = 0; g < Hkv; ++g)
+                Q3_TRY(cudaMemcpy2DAsync(lw + lay.o_wog + g * C * gcols * 2, gcols * 2,
+                                         (const bf16 *)w->wo[l] + g * gcols, Hq * D * 2, gcols * 2, C,
+                                         cudaMemcpyDeviceToDevice, st));
             // gate/up interleaved row by row: row 2j = gate_j, row 2j+1 = up_j
             Q3_TRY(cudaMemcpy2DAsync(lw + lay.o_wgu, 2 * C * 2, w->wgate[l], C * 2, C * 2, I,
                                      cudaMemcpyDeviceToDevice, st));
@@ -402,6 +412,8 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_ctxlen, 0, (size_t)cfg->max_seqs * 4, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_err, 0, 16, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_counters, 0, (size_t)cfg->max_seqs * cfg->n_kv_heads * 4, st));
+        Q3_TRY(cudaMemsetAsync(c->arena + lay.o_pflags, 0, PFLAG_WORDS * 4, st));
+        Q3_TRY(cudaMemsetAsync(c->arena + lay.o_pres, 0, (size_t)3 * cfg->max_seqs * C * 4, st));
         Q3_TRY(cudaStreamSynchronize(st));
         return cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
     };
@@ -480,6 +492,48 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
     const int n_split = std::max(1, std::min({slots / pairs, MAX_SPLIT, (bucket + 63) / 64}));
 
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+    const qwen3_config &k = c->cfg;
+    if ((k.flags & QWEN3_FLAG_PERSISTENT) && c->num_sms <= MAX_PARTS && k.n_kv_heads <= PFLAG_WORDS - 8 &&
+        decode_persistent_supported(k.hidden, k.n_q_heads, k.n_kv_heads, k.head_dim, k.intermediate, B, c->num_sms)) {
+        const Layout &L = c->lay;
+        DecodePersistentArgs p;
+        p.L = k.n_layers; p.C = k.hidden; p.Hq = k.n_q_heads; p.Hkv = k.n_kv_heads; p.head_dim = k.head_dim;
+        p.I = k.intermediate; p.V = k.vocab; p.max_ctx = k.max_ctx; p.B = B;
+        p.eps = k.rms_eps;
+        p.layers = c->layer(0);
+        p.layer_bytes = L.layer_bytes;
+        p.o_wqkv = L.o_wqkv; p.o_wog = L.o_wog; p.o_wgu = L.o_wgu; p.o_wdownT = L.o_wdownT;
+        p.o_gin = L.o_gin; p.o_gpost = L.o_gpost; p.o_gq = L.o_gq; p.o_gk = L.o_gk;
+        p.embed = c->at<bf16>(L.o_embed);
+        p.g_final = c->at<float>(L.o_gfinal);
+        p.rope = c->at<float2>(L.o_rope);
+        p.kcache = c->kcache(0);
+        p.vcache = c->vcache(0);
+        p.kv_layer_elems = L.kv_layer_bytes / 2;
+        p.tokens = tokens_dev; p.slots = slots_dev;
+        p.ctx_len = c->at<int32_t>(L.o_ctxlen);
+        p.next_tok = next_tok_dev;
+        p.logits = logits_dev;
+        p.dump = c->dump;
+        for (int i = 0; i < 3; ++i) p.res[i] = c->at<float>(L.o_pres) + (size_t)i * k.max_seqs * k.hidden;
+        p.qkv = c->at<float>(L.o_qkv);
+        p.part_val = c->at<float>(L.o_pval);
+        p.part_idx = c->at<int32_t>(L.o_pidx);
+        uint32_t *pf = c->at<uint32_t>(L.o_pflags);
+        p.arrive = pf;
+        p.counter = pf + 1;
+        p.grp = pf + 8;
+        p.err = c->at<uint32_t>(L.o_err);
+        Launch lc;
+        lc.stream = st;
+        lc.pdl = false;
+        lc.num_sms = c->num_sms;
+        lc.counter = &c->launches;
+        cudaError_t e = launch_decode_persistent(lc, p);
+        if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_decode_step (persistent)");
+        for (int b = 0; b < B; ++b) c->len_host[slots_host[b]] += 1;
+        return QWEN3_OK;
+    }
     const Rows rows = make_rows(c, nullptr, slots_dev, B, B);
     const bool use_graph = !(c->cfg.flags & QWEN3_FLAG_NO_GRAPH) && !c->dump;
     if (!use_graph) {

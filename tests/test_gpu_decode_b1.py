@@ -14,14 +14,22 @@ pytestmark = pytest.mark.gpu
 WL = synth.WORKLOADS["decode_b1"]
 
 
-def test_decode_b1_teacher_forced_parity():
+@pytest.fixture(scope="module")
+def setup():
     gc.ensure_library()
     s = WL.shape
     w = synth.make_weights(s)
     prompt = WL.prompts()[0]
     ref = oracle.generate(gc.oracle_config(s), gc.oracle_weights(w), prompt.tolist(), WL.decode_steps)
+    return w, prompt, ref
 
-    m = binding.Model(s, w, max_seqs=1, max_ctx=WL.max_ctx, max_prefill_tokens=WL.lengths[0])
+
+@pytest.mark.parametrize("flags", [0, binding.QWEN3_FLAG_PERSISTENT], ids=["chain", "persistent"])
+def test_decode_b1_teacher_forced_parity(setup, flags):
+    """Decode steps as the single persistent kernel and as the chain of kernels."""
+    w, prompt, ref = setup
+    s = WL.shape
+    m = binding.Model(s, w, max_seqs=1, max_ctx=WL.max_ctx, max_prefill_tokens=WL.lengths[0], flags=flags)
     n = prompt.numel()
     buf = torch.zeros((s.n_layers + 1) * n * s.hidden, dtype=torch.float32, device="cuda")
     m.set_debug_dump(buf)
