@@ -229,20 +229,35 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
             if (!got_s) { ok = false; break; }
             fence_after();
             const int k0 = j * BK;
+            // Only the diagonal tile (j == qt) masks: every key of an earlier tile is below the
+            // first query of this CTA (BQ == BK), hence visible and inside the sequence.
+            const bool diag = j == qt;
             // pass 1: row maximum of the visible scores
             float mx = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 float v[32];
                 ld32(t_s + c * 32, v);
+                if (diag) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int kj = k0 + c * 32 + i;
-                    if (kj <= qi && kj < len) mx = fmaxf(mx, v[i]);
+                    for (int i = 0; i < 32; ++i) {
+                        const int kj = k0 + c * 32 + i;
+                        if (kj <= qi && kj < len) mx = fmaxf(mx, v[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
                 }
             }
-            const float m_new = fmaxf(m_run, mx * scale_log2);
-            const float corr = m_run == -INFINITY ? 0.0f : exp2f(m_run - m_new);
+            // The reference maximum moves only when the tile's maximum exceeds it by more than
+            // 2^8: softmax does not depend on the reference, P stays below 256 (exact enough in
+            // bf16, far from overflow) and the rescale of O through TMEM becomes rare.
+            const float m_tile = mx * scale_log2;
+            float m_new = m_run, corr = 1.0f;
+            if (m_run == -INFINITY || m_tile > m_run + 8.0f) {
+                m_new = m_tile;
+                corr = m_run == -INFINITY ? 0.0f : exp2f(m_run - m_tile);
+            }
             // pass 2: probabilities, row sum, P (bf16) in the swizzled K-major layout.  The
             // tensor core finished the previous P V (it precedes this tile's S in issue order).
             float sum = 0.0f;
@@ -251,13 +266,24 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
                 float v[32];
                 ld32(t_s + c * 32, v);
                 uint32_t pk[16];
+                if (diag) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int kj = k0 + c * 32 + i;
-                    const float p0 = (kj <= qi && kj < len) ? exp2f(v[i] * scale_log2 - m_new) : 0.0f;
-                    const float p1 = (kj + 1 <= qi && kj + 1 < len) ? exp2f(v[i + 1] * scale_log2 - m_new) : 0.0f;
-                    sum += p0 + p1;
-                    pk[i / 2] = pack_bf16x2(p0, p1);
+                    for (int i = 0; i < 32; i += 2) {
+                        const int kj = k0 + c * 32 + i;
+                        const float p0 = (kj <= qi && kj < len) ? exp2f(fmaf(v[i], scale_log2, -m_new)) : 0.0f;
+                        const float p1 =
+                            (kj + 1 <= qi && kj + 1 < len) ? exp2f(fmaf(v[i + 1], scale_log2, -m_new)) : 0.0f;
+                        sum += p0 + p1;
+                        pk[i / 2] = pack_bf16x2(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float p0 = exp2f(fmaf(v[i], scale_log2, -m_new));
+                        const float p1 = exp2f(fmaf(v[i + 1], scale_log2, -m_new));
+                        sum += p0 + p1;
+                        pk[i / 2] = pack_bf16x2(p0, p1);
+                    }
                 }
                 // 32 keys = 4 chunks of 16 bytes; chunk cc of the 64-key half at cc ^ (r & 7)
                 uint8_t *half = prow + (c >> 1) * HALF_BYTES;
