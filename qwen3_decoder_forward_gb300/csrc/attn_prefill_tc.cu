@@ -7,16 +7,21 @@
 // [slot][Hkv][max_ctx][128], out bf16 [N, Hq*128].
 //
 // CTA = 128 queries x the 2 query heads of one KV head (the GQA pair shares every K/V tile);
-// 10 warps:
-//   warp 8 (1 thread): TMA -- both Q tiles once, then each K and V tile of 128 keys (128-byte
+// 18 warps:
+//   warp 16 (1 thread): TMA -- both Q tiles once, then each K and V tile of 128 keys (128-byte
 //                      swizzle, two 64-column halves per tile);
-//   warp 9 (1 thread): MMA -- per key tile: S_h = Q_h K^T for both heads (M=128, N=128, K=128)
-//                      into TMEM, then, as each head's P is ready, O_h += P_h V (V read MN-major);
-//   warps 0-3 / 4-7:   one softmax warpgroup per head -- thread t owns query row t: it reads its
-//                      row of S_h (tcgen05.ld), applies the causal mask and the online softmax in
-//                      fp32, writes P (bf16) into shared memory in the swizzled K-major layout and
-//                      rescales its row of the TMEM accumulator O_h by exp(m_old - m_new) before
-//                      the next P V accumulates into it.
+//   warp 17 (1 thread): MMA -- S_h = Q_h K^T (M=128, N=128, K=128) into TMEM and, as each head's
+//                      P is ready, O_h += P_h V (V read MN-major), issued per head in the order
+//                      P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): the scores of one head's next tile
+//                      are computed while the other head's softmax runs;
+//   warps 0-7 / 8-15:  eight softmax warps per head -- warps w and w+4 of a head read the same
+//                      32 TMEM lanes (query rows) and split the 128 columns (keys) in halves:
+//                      each thread takes 64 scores of its row (tcgen05.ld), the two halves
+//                      exchange their row maxima through shared memory (one named barrier per
+//                      tile and head), apply the causal mask and the online softmax in fp32,
+//                      write P (bf16) into shared memory in the swizzled K-major layout and
+//                      rescale their half of the row of the TMEM accumulator O_h when the
+//                      reference maximum moves; the two partial row sums meet at the end.
 // The two warpgroups work on their heads at the same time while the tensor core alternates
 // between them, so the exponentials of one head overlap the MMAs of the other.
 // Every mbarrier wait is bounded; on timeout the CTA flags ERR_TIMEOUT and skips to the end.
@@ -31,10 +36,11 @@ namespace q3 {
 
 namespace {
 
-constexpr int D = 128, BQ = 128, BK = 128, THREADS = 320;
+constexpr int D = 128, BQ = 128, BK = 128, THREADS = 576;
+constexpr int SM_WARPS = 16, TMA_WARP = 16, MMA_WARP = 17;
 constexpr int TILE_BYTES = 128 * D * 2;  // a [128][128] bf16 tile as two 64-column halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
-constexpr int SMEM_BYTES = TILE_BYTES * 6 + 512 + 1024;  // Q0, Q1, K, V, P0, P1
+constexpr int SMEM_BYTES = TILE_BYTES * 6 + 6144 + 1024;  // Q0, Q1, K, V, P0, P1, barriers
 constexpr uint32_t TMEM_COLS = 512;  // S0: 0-127, S1: 128-255, O0: 256-383, O1: 384-511
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -111,6 +117,9 @@ struct Bars {
     uint64_t q_full, kfull, kempty, vfull, vempty;
     uint64_t s_full[2], p_full[2], o_full[2];
     uint32_t tmem;
+    float xmax[2][2][2][BQ];  // [tile parity][head][column half][row]: partial row maxima
+    float xsum[2][2][BQ];     // [head][column half][row]: partial row sums at the end
+    int fail[2];              // [head]: a wait gave up (read by every warp of the head after a barrier)
 };
 
 __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
@@ -143,11 +152,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
         mbar_init(&bars->vempty, 1);
         for (int hh = 0; hh < 2; ++hh) {
             mbar_init(&bars->s_full[hh], 1);
-            mbar_init(&bars->p_full[hh], 128);
+            mbar_init(&bars->p_full[hh], 8 * 32);
             mbar_init(&bars->o_full[hh], 1);
+            bars->fail[hh] = 0;
         }
     }
-    if (warp == 9) {
+    if (warp == MMA_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&bars->tmem)),
                      "r"(TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -158,7 +168,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
     const uint32_t tmem = bars->tmem;
 
     bool ok = true;
-    if (warp == 8) {
+    if (warp == TMA_WARP) {
         if (lane == 0) {
             mbar_expect_tx(&bars->q_full, 2 * TILE_BYTES);
             for (int hh = 0; hh < 2; ++hh) {
@@ -176,139 +186,169 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
                 tma2d(v_s + HALF_BYTES, &tmV, 64, kv_row0 + j * BK, &bars->vfull);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == MMA_WARP) {
         if (lane == 0) {
             constexpr uint32_t id_s = idesc(BQ, BK, 0), id_o = idesc(BQ, D, 1);
             ok = mbar_wait_bounded(&bars->q_full, 0, err);
-            const uint32_t ka = smem_addr(k_s), va = smem_addr(v_s);
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                if (!mbar_wait_bounded(&bars->kfull, j & 1, err)) { ok = false; break; }
-                for (int hh = 0; hh < 2 && ok; ++hh) {
-                    // S_h of the previous tile has been read (its P is written) before it is overwritten
-                    if (j > 0 && !mbar_wait_bounded(&bars->p_full[hh], (j - 1) & 1, err)) { ok = false; break; }
-                    fence_after();
-                    const uint32_t qa = smem_addr(q_s + hh * TILE_BYTES);
+            // Descriptors built once; a byte offset o moves the start-address field by o >> 4
+            // (shared-memory addresses stay below 2^18, so the 14-bit field never carries).
+            const uint64_t dq[2] = {sdesc(smem_addr(q_s), 16, 1024), sdesc(smem_addr(q_s + TILE_BYTES), 16, 1024)};
+            const uint64_t dk = sdesc(smem_addr(k_s), 16, 1024);
+            const uint64_t dp[2] = {sdesc(smem_addr(p_s), 16, 1024), sdesc(smem_addr(p_s + TILE_BYTES), 16, 1024)};
+            const uint64_t dv = sdesc(smem_addr(v_s), HALF_BYTES, 1024);
+            auto issue_s = [&](int hh, int j) {  // S_hh = Q_hh K(j)^T
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-                        mma(tmem + hh * 128, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), id_s, kk != 0);
-                    }
-                    commit(&bars->s_full[hh]);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
+                    mma(tmem + hh * 128, dq[hh] + off, dk + off, id_s, kk != 0);
                 }
-                if (!ok) break;
-                commit(&bars->kempty);
+                commit(&bars->s_full[hh]);
+                if (hh == 1) commit(&bars->kempty);  // both heads have read K(j)
+            };
+            if (ok && mbar_wait_bounded(&bars->kfull, 0, err)) {
+                fence_after();
+                issue_s(0, 0);
+                issue_s(1, 0);
+            } else {
+                ok = false;
+            }
+            for (int j = 0; j < n_tiles && ok; ++j) {
                 if (!mbar_wait_bounded(&bars->vfull, j & 1, err)) { ok = false; break; }
                 for (int hh = 0; hh < 2 && ok; ++hh) {
+                    // P_hh(j) is written (and S_hh(j) read): O_hh += P_hh V(j), then S_hh(j+1)
                     if (!mbar_wait_bounded(&bars->p_full[hh], j & 1, err)) { ok = false; break; }
                     fence_after();
-                    const uint32_t pa = smem_addr(p_s + hh * TILE_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         // P: K-major over keys; V: MN-major (dims contiguous), 16 keys = 2048 bytes
-                        const uint32_t poff = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-                        mma(tmem + 256 + hh * 128, sdesc(pa + poff, 16, 1024), sdesc(va + kk * 2048, HALF_BYTES, 1024),
-                            id_o, (j | kk) != 0);
+                        const uint64_t poff = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
+                        mma(tmem + 256 + hh * 128, dp[hh] + poff, dv + (uint64_t)(kk * 2048 >> 4), id_o, (j | kk) != 0);
                     }
                     commit(&bars->o_full[hh]);
+                    if (hh == 1) commit(&bars->vempty);  // both heads have read V(j)
+                    if (j + 1 < n_tiles) {
+                        if (hh == 0 && !mbar_wait_bounded(&bars->kfull, (j + 1) & 1, err)) {
+                            ok = false;
+                            break;
+                        }
+                        fence_after();
+                        issue_s(hh, j + 1);
+                    }
                 }
-                if (!ok) break;
-                commit(&bars->vempty);
             }
         }
     } else {
-        // softmax warpgroup hh = warp / 4 for query head h0 + hh; thread owns query row r
-        const int hh = warp >> 2;
-        const int r = (warp & 3) * 32 + lane;
+        // softmax: head hh = warp / 8; warps w and w + 4 of the head share query rows
+        // r = 32 (w % 4) + lane and take the column halves ch = (w % 8) / 4
+        const int hh = warp >> 3, wl = warp & 7, ch = wl >> 2;
+        const int r = (wl & 3) * 32 + lane;
         const int qi = q0 + r;  // position within the sequence
-        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t t_s = tmem + hh * 128 + lane_base, t_o = tmem + 256 + hh * 128 + lane_base;
+        const uint32_t lane_base = (uint32_t)((wl & 3) * 32) << 16;
+        const uint32_t t_s = tmem + hh * 128 + ch * 64 + lane_base, t_o = tmem + 256 + hh * 128 + ch * 64 + lane_base;
+        auto head_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + hh), "r"(8 * 32) : "memory"); };
         float m_run = -INFINITY, l_run = 0.0f;
-        uint8_t *prow = p_s + hh * TILE_BYTES + r * 128;  // this row inside each 64-column half
+        uint8_t *prow = p_s + hh * TILE_BYTES + ch * HALF_BYTES + r * 128;  // this row in its 64-key half
         for (int j = 0; j < n_tiles; ++j) {
-            const bool got_s = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->s_full[hh], j & 1, err));
-            if (!got_s) { ok = false; break; }
+            // A wait that gives up is reported through fail[hh] and acted on after the head's
+            // barrier, so that all eight warps leave the loop at the same barrier.
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars->s_full[hh], j & 1, err)) && lane == 0)
+                bars->fail[hh] = 1;
             fence_after();
-            const int k0 = j * BK;
+            const int k0 = j * BK + ch * 64;  // first key of this thread's half
             // Only the diagonal tile (j == qt) masks: every key of an earlier tile is below the
             // first query of this CTA (BQ == BK), hence visible and inside the sequence.
             const bool diag = j == qt;
-            // pass 1: row maximum of the visible scores
-            float mx = -INFINITY;
+            float v[2][32];
+            ld32(t_s, v[0]);
+            ld32(t_s + 32, v[1]);
+            // pass 1: maximum of the visible scores of this half (eight partial maxima)
+            float mxp[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                ld32(t_s + c * 32, v);
+            for (int i = 0; i < 8; ++i) mxp[i] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 if (diag) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int kj = k0 + c * 32 + i;
-                        if (kj <= qi && kj < len) mx = fmaxf(mx, v[i]);
+                        if (kj <= qi && kj < len) mxp[i & 7] = fmaxf(mxp[i & 7], v[c][i]);
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
+                    for (int i = 0; i < 32; ++i) mxp[i & 7] = fmaxf(mxp[i & 7], v[c][i]);
                 }
+            }
+            const float mh = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                   fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+            bars->xmax[j & 1][hh][ch][r] = mh;
+            head_sync();
+            const float mx = fmaxf(mh, bars->xmax[j & 1][hh][ch ^ 1][r]);
+            if (*reinterpret_cast<volatile int *>(&bars->fail[hh])) {
+                ok = false;
+                break;
             }
             // The reference maximum moves only when the tile's maximum exceeds it by more than
             // 2^8: softmax does not depend on the reference, P stays below 256 (exact enough in
-            // bf16, far from overflow) and the rescale of O through TMEM becomes rare.
+            // bf16, far from overflow) and the rescale of O through TMEM becomes rare.  Both
+            // halves of a row see the same maximum, so they take the same decision.
             const float m_tile = mx * scale_log2;
             float m_new = m_run, corr = 1.0f;
             if (m_run == -INFINITY || m_tile > m_run + 8.0f) {
                 m_new = m_tile;
                 corr = m_run == -INFINITY ? 0.0f : exp2f(m_run - m_tile);
             }
-            // pass 2: probabilities, row sum, P (bf16) in the swizzled K-major layout.  The
-            // tensor core finished the previous P V (it precedes this tile's S in issue order).
-            float sum = 0.0f;
+            // pass 2: probabilities, partial row sum, P (bf16) in the swizzled K-major layout.
+            // The tensor core finished the previous P V (it precedes this tile's S in issue order).
+            float sp[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                ld32(t_s + c * 32, v);
+            for (int i = 0; i < 8; ++i) sp[i] = 0.0f;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
                 uint32_t pk[16];
                 if (diag) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
                         const int kj = k0 + c * 32 + i;
-                        const float p0 = (kj <= qi && kj < len) ? exp2f(fmaf(v[i], scale_log2, -m_new)) : 0.0f;
+                        const float p0 = (kj <= qi && kj < len) ? exp2f(fmaf(v[c][i], scale_log2, -m_new)) : 0.0f;
                         const float p1 =
-                            (kj + 1 <= qi && kj + 1 < len) ? exp2f(fmaf(v[i + 1], scale_log2, -m_new)) : 0.0f;
-                        sum += p0 + p1;
+                            (kj + 1 <= qi && kj + 1 < len) ? exp2f(fmaf(v[c][i + 1], scale_log2, -m_new)) : 0.0f;
+                        sp[(i >> 1) & 7] += p0 + p1;
                         pk[i / 2] = pack_bf16x2(p0, p1);
                     }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
-                        const float p0 = exp2f(fmaf(v[i], scale_log2, -m_new));
-                        const float p1 = exp2f(fmaf(v[i + 1], scale_log2, -m_new));
-                        sum += p0 + p1;
+                        const float p0 = exp2f(fmaf(v[c][i], scale_log2, -m_new));
+                        const float p1 = exp2f(fmaf(v[c][i + 1], scale_log2, -m_new));
+                        sp[(i >> 1) & 7] += p0 + p1;
                         pk[i / 2] = pack_bf16x2(p0, p1);
                     }
                 }
                 // 32 keys = 4 chunks of 16 bytes; chunk cc of the 64-key half at cc ^ (r & 7)
-                uint8_t *half = prow + (c >> 1) * HALF_BYTES;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const int cc = (c & 1) * 4 + q;
-                    *reinterpret_cast<uint4 *>(half + ((cc ^ (r & 7)) << 4)) =
+                    const int cc = c * 4 + q;
+                    *reinterpret_cast<uint4 *>(prow + ((cc ^ (r & 7)) << 4)) =
                         make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
                 }
             }
+            const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l_run = l_run * corr + sum;
             m_run = m_new;
             // O_h holds tiles < j (implied by s_full; waited so that o_full's phases stay in step)
+            bool o_ok = true;
             if (j > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_full[hh], (j - 1) & 1, err))) {
-                ok = false;
-                break;
+                o_ok = false;
+                if (lane == 0) bars->fail[hh] = 1;  // the loop ends at the next barrier
             }
-            if (j > 0 && __any_sync(0xffffffffu, corr != 1.0f)) {  // rescale this row of O_h
+            if (o_ok && j > 0 && __any_sync(0xffffffffu, corr != 1.0f)) {  // rescale this half-row of O_h
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    float v[32];
-                    ld32(t_o + c * 32, v);
+                for (int c = 0; c < 2; ++c) {
+                    float o[32];
+                    ld32(t_o + c * 32, o);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= corr;
-                    st32(t_o + c * 32, v);
+                    for (int i = 0; i < 32; ++i) o[i] *= corr;
+                    st32(t_o + c * 32, o);
                 }
             }
             // make the generic-proxy writes of P visible to the tensor core, then hand over
@@ -316,13 +356,17 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
             fence_before();
             arrive(&bars->p_full[hh]);
         }
+        // the two halves' row sums; the output row is then written in two halves
+        bars->xsum[hh][ch][r] = l_run;
+        head_sync();
+        const float l_tot = l_run + bars->xsum[hh][ch ^ 1][r];
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_full[hh], (n_tiles - 1) & 1, err));
         if (ok) {
             fence_after();
-            const float inv = 1.0f / l_run;
-            uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)(start + qi) * Hq + h0 + hh) * D);
+            const float inv = 1.0f / l_tot;
+            uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)(start + qi) * Hq + h0 + hh) * D + ch * 64);
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 float v[32];
                 ld32(t_o + c * 32, v);
                 if (qi < len) {
@@ -339,7 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
     pdl_trigger();
     fence_before();
     __syncthreads();
-    if (warp == 9) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
+    if (warp == MMA_WARP) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS));
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
