@@ -35,7 +35,12 @@ L2_BYTES = 129 * 2 ** 20
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the
 # capture summarised in profiles/ (None until taken for the current kernel).
-TRAFFIC_BYTES = {"gemv_gate_up": None}
+# DRAM bytes (read + write) per launch of the roofline kernels, medians of ncu captures of the
+# kernels as they stand (dram__bytes_read.sum + dram__bytes_write.sum): the decode gate_up GEMV
+# at one row reads exactly its 12.6 MB of weights; the prefill gate_up GEMM at 23,460 rows reads
+# A (48 MB) and W (12.6 MB) once and writes 86 MB of its 144 MB output before the kernel ends
+# (the rest leaves L2 later).
+TRAFFIC_BYTES = {"gemv_gate_up": 12609536, "gemm_gate_up": 146652416}
 
 
 def parse_args():
@@ -283,6 +288,53 @@ def measure_gemv_roofline(torch, binding, wl, peaks, peak_kind):
             else "fallback 6.8 TB/s"}
 
 
+def measure_gemm_roofline(torch, binding, wl, peaks, peak_kind):
+    """Average duration of the prefill gate_up projection GEMM (tcgen05, SwiGLU epilogue), the
+    largest prefill GEMM, at the workload's packed token count N, timed with CUDA events on the
+    launching stream.  At N = 23,460 the activations and the output (48 MB + 144 MB) exceed L2;
+    the 12.6 MB of weights may stay in it."""
+    s = wl.shape
+    dev = torch.device("cuda")
+    M, K, N = wl.n_prompt_tokens, s.hidden, 2 * s.intermediate
+    g = torch.Generator(device="cpu").manual_seed(6)
+    x = (torch.randn(M, K, generator=g)).to(torch.bfloat16).to(dev)
+    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).to(dev)
+    out = torch.empty(M, N // 2, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(3):
+        binding.qwen3_op_gemm(x.data_ptr(), M, K, w.data_ptr(), N, binding.QWEN3_EPI_SWIGLU, out.data_ptr(), stream)
+    reps = 10
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        binding.qwen3_op_gemm(x.data_ptr(), M, K, w.data_ptr(), N, binding.QWEN3_EPI_SWIGLU, out.data_ptr(), stream)
+    e1.record()
+    torch.cuda.synchronize()
+    avg_s = e0.elapsed_time(e1) / 1e3 / reps
+    flops = 2 * M * N * K
+    achieved = flops / avg_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    return {"kernel": f"k_gemm_tcp (prefill gate_up GEMM + SwiGLU, tcgen05, [{M},{K}] x [{N},{K}]^T)",
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": TRAFFIC_BYTES["gemm_gate_up"],
+            "algorithmic_flops_per_launch": flops, "avg_launch_us": round(avg_s * 1e6, 3),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, burst: kernel timed alone)"
+            if peak_kind == "measured" else "fallback 1.9 PFLOP/s"}
+
+
+def prefill_flops(wl):
+    """Algorithmic FLOPs of one prefill call: every linear projection for each packed token,
+    causal attention (the lower triangle only, QK^T and PV) and the tied head at each
+    sequence's last row."""
+    s = wl.shape
+    lin = 2 * wl.n_prompt_tokens * s.n_layers * ((s.q_dim + 2 * s.kv_dim) * s.hidden + s.hidden * s.q_dim +
+                                                3 * s.intermediate * s.hidden)
+    attn = s.n_layers * sum(4 * s.n_q_heads * s.head_dim * n * (n + 1) // 2 for n in wl.lengths)
+    head = 2 * s.hidden * s.vocab * wl.n_seqs
+    return lin + attn + head
+
+
 # --------------------------------------------------------------------------------------
 # CPU oracle timing (reference arm and the cpu_baseline object)
 # --------------------------------------------------------------------------------------
@@ -456,7 +508,8 @@ def gpu_arm(args, wl):
     e2e_s_max, e2e_units = reduce_over_ranks(torch, world, e2e_s * 1e3, units * args.steps)
     e2e_value = e2e_units / (e2e_s_max / 1e3)
 
-    roofline = measure_gemv_roofline(torch, binding, wl, peaks, peak_kind) if wl.decode_steps else None
+    roofline = (measure_gemv_roofline(torch, binding, wl, peaks, peak_kind) if wl.decode_steps
+                else measure_gemm_roofline(torch, binding, wl, peaks, peak_kind))
     assert runner.model.status() == 0, binding.qwen3_last_error(runner.model.ctx)
     runner.model.close()
     del runner
@@ -499,6 +552,9 @@ def gpu_arm(args, wl):
             step_bytes = decode_step_bytes(wl)
             dec_s = dec_ms / 1e3 / args.steps / wl.decode_steps
             line["breakdown"]["decode_step_hbm_frac"] = round(step_bytes / dec_s / 1e9 / float(peaks["hbm_gbs"]), 4)
+        pre_s = pre_ms / 1e3 / args.steps
+        line["breakdown"]["prefill_tflops"] = round(prefill_flops(wl) / pre_s / 1e12, 1)
+        line["breakdown"]["prefill_tensor_frac"] = round(prefill_flops(wl) / pre_s / 1e12 / float(peaks["bf16_tflops"]), 4)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
