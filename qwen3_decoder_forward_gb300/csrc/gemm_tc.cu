@@ -87,8 +87,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *v) {
 // major, so CTAs running together share A rows).  Two TMEM accumulators of 256 columns: the
 // MMA thread fills one while the epilogue warps drain the other.
 //   warp 0 (1 thread) TMA producer; warp 1 (1 thread) MMA issuer and TMEM owner;
-//   warps 2-5 epilogue, warp w reading TMEM lanes 32*(w%4) .. 32*(w%4)+31.
-constexpr int TCP_THREADS = 192;
+//   warps 2-9 epilogue, warp w reading TMEM lanes 32*(w%4) .. 32*(w%4)+31 and the columns
+//   128*((w-2)/4) .. +127 of the tile (for QKV: one head of the tile's two).
+constexpr int TCP_THREADS = 320, TCP_EPI_WARPS = 8;
 constexpr uint32_t TCP_TMEM_COLS = 512;
 
 struct EpiArgs {
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tm_full[a], 1);
-            mbar_init(&tm_empty[a], 4);  // one arrival per epilogue warp
+            mbar_init(&tm_empty[a], TCP_EPI_WARPS);  // one arrival per epilogue warp
         }
     }
     if (warp == 1) {
@@ -231,8 +232,9 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
             }
         }
     } else {
-        // epilogue warps 2..5
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // epilogue warps 2..9
+        const int q = warp & 3;         // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;  // 128-column half of the tile
         int local = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
             const int a = local & 1;
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
             const uint32_t t_row = tmem + a * TC_BN + ((uint32_t)(q * 32) << 16);
             if (EPI != EPI_QKV) {
 #pragma unroll 1
-                for (int c = 0; c < TC_BN / 32; ++c) {
+                for (int c = half * 4; c < half * 4 + 4; ++c) {
                     uint32_t v[32];
                     tmem_ld32(t_row + c * 32, v);
                     if (row < M) store_chunk(EPI, v, row, n0 + c * 32, N, ea.out);
@@ -253,8 +255,8 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                 // two heads of 128 columns per tile: head index within [q | k | v]
                 const int slot = row < M ? ea.row_slot[row] : 0;
                 const int pos = row < M ? ea.row_pos[row] : 0;
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
+                {
+                    const int hh = half;
                     const int head = n0 / 128 + hh;
                     const uint32_t th = t_row + hh * 128;
                     const bool is_v = head >= ea.Hq + ea.Hkv;
