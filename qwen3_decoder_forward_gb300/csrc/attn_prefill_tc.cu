@@ -8,8 +8,8 @@
 //
 // CTA = 128 queries x the 2 query heads of one KV head (the GQA pair shares every K/V tile);
 // 18 warps:
-//   warp 16 (1 thread): TMA -- both Q tiles once, then each K and V tile of 128 keys (128-byte
-//                      swizzle, two 64-column halves per tile);
+//   warp 16 (1 thread): TMA -- both Q tiles once, then each K tile (two-stage ring) and V tile
+//                      of 128 keys (128-byte swizzle, two 64-column halves per tile);
 //   warp 17 (1 thread): MMA -- S_h = Q_h K^T (M=128, N=128, K=128) into TMEM and, as each head's
 //                      P is ready, O_h += P_h V (V read MN-major), issued per head in the order
 //                      P_0 V(j), S_0(j+1), P_1 V(j), S_1(j+1): the scores of one head's next tile
@@ -19,8 +19,9 @@
 //                      each thread takes 64 scores of its row (tcgen05.ld), the two halves
 //                      exchange their row maxima through shared memory (one named barrier per
 //                      tile and head), apply the causal mask and the online softmax in fp32,
-//                      write P (bf16) into shared memory in the swizzled K-major layout and
-//                      rescale their half of the row of the TMEM accumulator O_h when the
+//                      write P (bf16) into tensor memory over the first 64 columns of S_h
+//                      (the P V MMA reads its A operand from there, not from shared memory)
+//                      and rescale their half of the row of the TMEM accumulator O_h when the
 //                      reference maximum moves; the two partial row sums meet at the end.
 // The two warpgroups work on their heads at the same time while the tensor core alternates
 // between them, so the exponentials of one head overlap the MMAs of the other.
@@ -40,7 +41,7 @@ constexpr int D = 128, BQ = 128, BK = 128, THREADS = 576;
 constexpr int SM_WARPS = 16, TMA_WARP = 16, MMA_WARP = 17;
 constexpr int TILE_BYTES = 128 * D * 2;  // a [128][128] bf16 tile as two 64-column halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
-constexpr int SMEM_BYTES = TILE_BYTES * 6 + 6144 + 1024;  // Q0, Q1, K, V, P0, P1, barriers
+constexpr int SMEM_BYTES = TILE_BYTES * 5 + 6144 + 1024;  // Q0, Q1, K ring (2), V, barriers
 constexpr uint32_t TMEM_COLS = 512;  // S0: 0-127, S1: 128-255, O0: 256-383, O1: 384-511
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -75,6 +76,13 @@ __device__ __forceinline__ void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
         "l"(a), "l"(b), "r"(id), "r"(acc));
 }
+// O += A B with A (M x K, bf16, two elements per 32-bit column, row = TMEM lane) in tensor memory.
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
 __device__ __forceinline__ void commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                  : "memory");
@@ -97,6 +105,16 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float *v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 columns of this thread's TMEM lane (no wait: the caller issues tcgen05.wait::st).
+__device__ __forceinline__ void st16_nowait(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void st32(uint32_t taddr, const float *v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -114,7 +132,7 @@ __device__ __forceinline__ void st32(uint32_t taddr, const float *v) {
 }
 
 struct Bars {
-    uint64_t q_full, kfull, kempty, vfull, vempty;
+    uint64_t q_full, kfull[2], kempty[2], vfull, vempty;
     uint64_t s_full[2], p_full[2], o_full[2];
     uint32_t tmem;
     float xmax[2][2][2][BQ];  // [tile parity][head][column half][row]: partial row maxima
@@ -129,10 +147,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_s = smem;                    // [2] tiles
-    uint8_t *k_s = q_s + 2 * TILE_BYTES;
-    uint8_t *v_s = k_s + TILE_BYTES;
-    uint8_t *p_s = v_s + TILE_BYTES;        // [2] tiles
-    Bars *bars = reinterpret_cast<Bars *>(p_s + 2 * TILE_BYTES);
+    uint8_t *k_s = q_s + 2 * TILE_BYTES;    // [2] tiles: K ring
+    uint8_t *v_s = k_s + 2 * TILE_BYTES;
+    Bars *bars = reinterpret_cast<Bars *>(v_s + TILE_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qt = gridDim.x - 1 - blockIdx.x, g = blockIdx.y, b = blockIdx.z;  // longest tiles first
@@ -146,8 +163,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
-        mbar_init(&bars->kfull, 1);
-        mbar_init(&bars->kempty, 1);
+        for (int st = 0; st < 2; ++st) {
+            mbar_init(&bars->kfull[st], 1);
+            mbar_init(&bars->kempty[st], 1);
+        }
         mbar_init(&bars->vfull, 1);
         mbar_init(&bars->vempty, 1);
         for (int hh = 0; hh < 2; ++hh) {
@@ -176,10 +195,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
                 tma2d(q_s + hh * TILE_BYTES + HALF_BYTES, &tmQ, (h0 + hh) * D + 64, start + q0, &bars->q_full);
             }
             for (int j = 0; j < n_tiles && ok; ++j) {
-                if (j > 0 && !mbar_wait_bounded(&bars->kempty, (j - 1) & 1, err)) { ok = false; break; }
-                mbar_expect_tx(&bars->kfull, TILE_BYTES);
-                tma2d(k_s, &tmK, 0, kv_row0 + j * BK, &bars->kfull);
-                tma2d(k_s + HALF_BYTES, &tmK, 64, kv_row0 + j * BK, &bars->kfull);
+                const int st = j & 1;  // K tile j into ring stage j % 2, once tile j - 2 has been used
+                if (j >= 2 && !mbar_wait_bounded(&bars->kempty[st], ((j - 2) >> 1) & 1, err)) { ok = false; break; }
+                mbar_expect_tx(&bars->kfull[st], TILE_BYTES);
+                tma2d(k_s + st * TILE_BYTES, &tmK, 0, kv_row0 + j * BK, &bars->kfull[st]);
+                tma2d(k_s + st * TILE_BYTES + HALF_BYTES, &tmK, 64, kv_row0 + j * BK, &bars->kfull[st]);
                 if (j > 0 && !mbar_wait_bounded(&bars->vempty, (j - 1) & 1, err)) { ok = false; break; }
                 mbar_expect_tx(&bars->vfull, TILE_BYTES);
                 tma2d(v_s, &tmV, 0, kv_row0 + j * BK, &bars->vfull);
@@ -193,19 +213,18 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
             // Descriptors built once; a byte offset o moves the start-address field by o >> 4
             // (shared-memory addresses stay below 2^18, so the 14-bit field never carries).
             const uint64_t dq[2] = {sdesc(smem_addr(q_s), 16, 1024), sdesc(smem_addr(q_s + TILE_BYTES), 16, 1024)};
-            const uint64_t dk = sdesc(smem_addr(k_s), 16, 1024);
-            const uint64_t dp[2] = {sdesc(smem_addr(p_s), 16, 1024), sdesc(smem_addr(p_s + TILE_BYTES), 16, 1024)};
+            const uint64_t dk[2] = {sdesc(smem_addr(k_s), 16, 1024), sdesc(smem_addr(k_s + TILE_BYTES), 16, 1024)};
             const uint64_t dv = sdesc(smem_addr(v_s), HALF_BYTES, 1024);
             auto issue_s = [&](int hh, int j) {  // S_hh = Q_hh K(j)^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
-                    mma(tmem + hh * 128, dq[hh] + off, dk + off, id_s, kk != 0);
+                    mma(tmem + hh * 128, dq[hh] + off, dk[j & 1] + off, id_s, kk != 0);
                 }
                 commit(&bars->s_full[hh]);
-                if (hh == 1) commit(&bars->kempty);  // both heads have read K(j)
+                if (hh == 1) commit(&bars->kempty[j & 1]);  // both heads have read K(j)
             };
-            if (ok && mbar_wait_bounded(&bars->kfull, 0, err)) {
+            if (ok && mbar_wait_bounded(&bars->kfull[0], 0, err)) {
                 fence_after();
                 issue_s(0, 0);
                 issue_s(1, 0);
@@ -220,14 +239,14 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
                     fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        // P: K-major over keys; V: MN-major (dims contiguous), 16 keys = 2048 bytes
-                        const uint64_t poff = (uint64_t)(((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4);
-                        mma(tmem + 256 + hh * 128, dp[hh] + poff, dv + (uint64_t)(kk * 2048 >> 4), id_o, (j | kk) != 0);
+                        // P from TMEM (16 keys = 8 columns, over S_hh); V: MN-major, 16 keys = 2048 bytes
+                        mma_ts(tmem + 256 + hh * 128, tmem + hh * 128 + kk * 8, dv + (uint64_t)(kk * 2048 >> 4), id_o,
+                               (j | kk) != 0);
                     }
                     commit(&bars->o_full[hh]);
                     if (hh == 1) commit(&bars->vempty);  // both heads have read V(j)
                     if (j + 1 < n_tiles) {
-                        if (hh == 0 && !mbar_wait_bounded(&bars->kfull, (j + 1) & 1, err)) {
+                        if (hh == 0 && !mbar_wait_bounded(&bars->kfull[(j + 1) & 1], ((j + 1) >> 1) & 1, err)) {
                             ok = false;
                             break;
                         }
@@ -247,7 +266,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
         const uint32_t t_s = tmem + hh * 128 + ch * 64 + lane_base, t_o = tmem + 256 + hh * 128 + ch * 64 + lane_base;
         auto head_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + hh), "r"(8 * 32) : "memory"); };
         float m_run = -INFINITY, l_run = 0.0f;
-        uint8_t *prow = p_s + hh * TILE_BYTES + ch * HALF_BYTES + r * 128;  // this row in its 64-key half
+        // P (bf16, two keys per column) overwrites the first 64 columns of S_hh: keys
+        // ch*64 + c*32 .. +31 of this row go to columns ch*32 + c*16 .. +15 of its lane.  Both
+        // halves of the row hold their scores in registers past the head's barrier, so no
+        // score is overwritten before it is read.
+        const uint32_t t_p = tmem + hh * 128 + ch * 32 + lane_base;
         for (int j = 0; j < n_tiles; ++j) {
             // A wait that gives up is reported through fail[hh] and acted on after the head's
             // barrier, so that all eight warps leave the loop at the same barrier.
@@ -297,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
                 m_new = m_tile;
                 corr = m_run == -INFINITY ? 0.0f : exp2f(m_run - m_tile);
             }
-            // pass 2: probabilities, partial row sum, P (bf16) in the swizzled K-major layout.
+            // pass 2: probabilities, partial row sum, P (bf16) into tensor memory.
             // The tensor core finished the previous P V (it precedes this tile's S in issue order).
             float sp[8];
 #pragma unroll
@@ -324,13 +347,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
                         pk[i / 2] = pack_bf16x2(p0, p1);
                     }
                 }
-                // 32 keys = 4 chunks of 16 bytes; chunk cc of the 64-key half at cc ^ (r & 7)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int cc = c * 4 + q;
-                    *reinterpret_cast<uint4 *>(prow + ((cc ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                }
+                st16_nowait(t_p + c * 16, pk);
             }
             const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
             l_run = l_run * corr + sum;
@@ -351,8 +368,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
                     st32(t_o + c * 32, o);
                 }
             }
-            // make the generic-proxy writes of P visible to the tensor core, then hand over
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // P is in tensor memory: complete the stores, then hand over
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             fence_before();
             arrive(&bars->p_full[hh]);
         }
