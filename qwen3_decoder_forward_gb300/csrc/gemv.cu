@@ -717,13 +717,17 @@ bool gemv_mma_supported(int M, int K, int N) {
 cudaError_t launch_gemv_mma(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N, int epi,
                             void *out, uint32_t *err) {
     if (!gemv_mma_supported(M, K, N)) return cudaErrorInvalidValue;
-    // K above 2048 with 32 rows would not fit shared memory in one slice: split it (residual only)
-    if (K > 2048) {
-        if (epi != EPI_RESID_ADD) return cudaErrorInvalidValue;
-        return run_mma<EPI_RESID_ADD, 2>(lc, X, M, K, W, N, out, err);
+    // Residual adds split K over 2 or 4 CTAs (fp32 atomics; order unspecified): o_proj and down
+    // have only N/16 = 64 weight-row tiles, and K above 2048 with 32 rows would not fit shared
+    // memory in one slice.  The other epilogues need whole sums and keep K in one slice.
+    if (epi == EPI_RESID_ADD) {
+        if (K >= 2048 && (K / 4) % 256 == 0) return run_mma<EPI_RESID_ADD, 4>(lc, X, M, K, W, N, out, err);
+        if ((K / 2) % 256 == 0) return run_mma<EPI_RESID_ADD, 2>(lc, X, M, K, W, N, out, err);
+        if (K <= 2048) return run_mma<EPI_RESID_ADD, 1>(lc, X, M, K, W, N, out, err);
+        return cudaErrorInvalidValue;
     }
+    if (K > 2048) return cudaErrorInvalidValue;
     if (epi == EPI_F32) return run_mma<EPI_F32, 1>(lc, X, M, K, W, N, out, err);
-    if (epi == EPI_RESID_ADD) return run_mma<EPI_RESID_ADD, 1>(lc, X, M, K, W, N, out, err);
     return run_mma<EPI_SWIGLU, 1>(lc, X, M, K, W, N, out, err);
 }
 

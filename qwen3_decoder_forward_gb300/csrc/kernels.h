@@ -114,8 +114,9 @@ cudaError_t launch_mlp_fused(const Launch &lc, const float *h, int M, int C, con
                              const bf16 *Wgu, const bf16 *WdT, int I, float *out, uint32_t *err,
                              const bf16 *Wgu_ahead, const bf16 *WdT_ahead);
 cudaError_t launch_transpose_bf16(const Launch &lc, const bf16 *src, bf16 *dst, int rows, int cols);
-// Tensor-core (mma.sync) decode projection for up to 32 rows; K > 2048 only with EPI_RESID_ADD
-// (the K halves add into the output with atomics).
+// Tensor-core (mma.sync) decode projection for up to 32 rows.  With EPI_RESID_ADD the K range is
+// split over 2 or 4 CTAs whose partial sums add into the output with fp32 atomics (order
+// unspecified); the other epilogues keep K in one slice (K <= 2048).
 bool gemv_mma_supported(int M, int K, int N);
 // lm_head + argmax pass 1 on the tensor cores for 1..32 rows (C == 1024): one partial (best
 // value, index) per CTA and row, as launch_lmhead_argmax's pass 1 writes them.
