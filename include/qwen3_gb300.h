@@ -125,6 +125,19 @@ int qwen3_prefill(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *cu_s
                   const int32_t *slots_host, int32_t B, float *logits_dev,
                   int32_t *next_tok_dev, void *stream);
 
+/* Prefill that continues its slots ("从零开始写Qwen3", Attn: the causal mask of a query block
+ * that follows cached keys; "古法手撕简易LLM推理器", prefill与predict: offset = the cache length):
+ * the len_b tokens of sequence b are appended to slot slots[b] after the n_b tokens it holds
+ * (n_b = 0 is allowed), at positions n_b .. n_b+len_b-1, each attending to keys 0 .. its own
+ * position -- the cached prefix included -- and the slot then holds n_b + len_b tokens.
+ * Chunked prefill: one long prompt can be fed in several calls, and prompts can be extended
+ * after decode steps.  Arguments, outputs and errors as qwen3_prefill; E_CAPACITY when
+ * n_b + len_b > max_ctx, E_UNSUPPORTED for head ratios other than Hq = 2 Hkv. */
+int qwen3_prefill_append(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *cu_seqlens_dev,
+                         const int32_t *cu_seqlens_host, const int32_t *slots_dev,
+                         const int32_t *slots_host, int32_t B, float *logits_dev,
+                         int32_t *next_tok_dev, void *stream);
+
 /* One decode step ("古法手撕简易LLM推理器", predict): token tokens_dev[b] is appended to slot
  * slots[b] at position = the slot's current length, attends to keys 0..position, and
  * next_tok_dev[b] receives the greedy next token (logits_dev[B, V] too if not NULL).  Each

@@ -72,6 +72,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_create": (ctypes.c_int, [ctypes.POINTER(qwen3_config), ctypes.POINTER(qwen3_weights), _P, sz, _P,
                                         ctypes.POINTER(_P)]),
         "qwen3_prefill": (ctypes.c_int, [_P, _P, _P, pi32, _P, pi32, i32, _P, _P, _P]),
+        "qwen3_prefill_append": (ctypes.c_int, [_P, _P, _P, pi32, _P, pi32, i32, _P, _P, _P]),
         "qwen3_decode_step": (ctypes.c_int, [_P, _P, _P, pi32, i32, _P, _P, _P]),
         "qwen3_set_debug_dump": (ctypes.c_int, [_P, _P, sz]),
         "qwen3_get_status": (ctypes.c_int, [_P]),
@@ -129,6 +130,13 @@ def qwen3_prefill(ctx, tokens_ptr: int, cu_dev_ptr: int, cu_host: Sequence[int],
                   slots_host: Sequence[int], B: int, logits_ptr: Optional[int], next_ptr: int, stream: int = 0):
     _check(load_library().qwen3_prefill(ctx, tokens_ptr, cu_dev_ptr, _i32_array(cu_host), slots_dev_ptr,
                                         _i32_array(slots_host), B, logits_ptr, next_ptr, stream), ctx)
+
+
+def qwen3_prefill_append(ctx, tokens_ptr: int, cu_dev_ptr: int, cu_host: Sequence[int], slots_dev_ptr: int,
+                         slots_host: Sequence[int], B: int, logits_ptr: Optional[int], next_ptr: int,
+                         stream: int = 0):
+    _check(load_library().qwen3_prefill_append(ctx, tokens_ptr, cu_dev_ptr, _i32_array(cu_host), slots_dev_ptr,
+                                               _i32_array(slots_host), B, logits_ptr, next_ptr, stream), ctx)
 
 
 def qwen3_decode_step(ctx, tokens_ptr: int, slots_dev_ptr: int, slots_host: Sequence[int], B: int,
@@ -246,8 +254,9 @@ class Model:
         return self.torch.cuda.current_stream(self.device).cuda_stream
 
     def prefill(self, tokens, lengths: Sequence[int], slots: Sequence[int], want_logits: bool = False,
-                next_out=None):
-        """tokens: int32 CUDA tensor [N]; returns (next_tok int32 [B], logits fp32 [B, V] or None)."""
+                next_out=None, append: bool = False):
+        """tokens: int32 CUDA tensor [N]; returns (next_tok int32 [B], logits fp32 [B, V] or None).
+        append=True continues each slot after the tokens it holds (qwen3_prefill_append)."""
         torch = self.torch
         B = len(lengths)
         cu = [0]
@@ -257,8 +266,9 @@ class Model:
         slots_d = torch.tensor(list(slots), dtype=torch.int32, device=self.device)
         nxt = next_out if next_out is not None else torch.empty(B, dtype=torch.int32, device=self.device)
         logits = torch.empty(B, self.shape.vocab, dtype=torch.float32, device=self.device) if want_logits else None
-        qwen3_prefill(self.ctx, tokens.data_ptr(), cu_d.data_ptr(), cu, slots_d.data_ptr(), list(slots), B,
-                      logits.data_ptr() if logits is not None else None, nxt.data_ptr(), self._stream())
+        fn = qwen3_prefill_append if append else qwen3_prefill
+        fn(self.ctx, tokens.data_ptr(), cu_d.data_ptr(), cu, slots_d.data_ptr(), list(slots), B,
+           logits.data_ptr() if logits is not None else None, nxt.data_ptr(), self._stream())
         self._keep = (cu_d, slots_d)
         return nxt, logits
 

@@ -143,7 +143,8 @@ struct Bars {
 __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
     const __grid_constant__ CUtensorMap tmV, const int32_t *__restrict__ cu, const int32_t *__restrict__ slots,
-    bf16 *__restrict__ out, int Hq, int Hkv, int max_ctx, float scale_log2, uint32_t *err) {
+    const int32_t *__restrict__ row_pos, bf16 *__restrict__ out, int Hq, int Hkv, int max_ctx, float scale_log2,
+    uint32_t *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_s = smem;                    // [2] tiles
@@ -159,7 +160,13 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
     if (q0 >= len) return;  // uniform: no barrier or TMEM touched yet
     const int h0 = g * 2;    // the pair of query heads of KV head g (Hq == 2 Hkv)
     const int kv_row0 = (slots[b] * Hkv + g) * max_ctx;  // first cache row of this (slot, head)
-    const int n_tiles = min((len + BK - 1) / BK, qt + 1);
+    // The sequence's rows are positions off .. off+len-1 of its slot (off > 0 when the call
+    // continues a slot that already holds off tokens): query off+i sees keys 0 .. off+i, the
+    // bottom-right alignment of the causal mask.
+    const int off = row_pos[start];
+    const int n_tiles = (off + min(len, q0 + BQ) + BK - 1) / BK;
+    // tiles j >= first_masked hold a key above this CTA's first query and need the mask
+    const int first_masked = (off + q0 + 1) / BK;
 
     if (threadIdx.x == 0) {
         mbar_init(&bars->q_full, 1);
@@ -261,7 +268,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
         // r = 32 (w % 4) + lane and take the column halves ch = (w % 8) / 4
         const int hh = warp >> 3, wl = warp & 7, ch = wl >> 2;
         const int r = (wl & 3) * 32 + lane;
-        const int qi = q0 + r;  // position within the sequence
+        const int qi = q0 + r;        // row within this call's part of the sequence
+        const int qa = off + qi;      // its position (keys 0..qa are visible)
+        const int kend = off + len;   // keys at or beyond kend do not exist yet
         const uint32_t lane_base = (uint32_t)((wl & 3) * 32) << 16;
         const uint32_t t_s = tmem + hh * 128 + ch * 64 + lane_base, t_o = tmem + 256 + hh * 128 + ch * 64 + lane_base;
         auto head_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + hh), "r"(8 * 32) : "memory"); };
@@ -278,9 +287,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
                 bars->fail[hh] = 1;
             fence_after();
             const int k0 = j * BK + ch * 64;  // first key of this thread's half
-            // Only the diagonal tile (j == qt) masks: every key of an earlier tile is below the
-            // first query of this CTA (BQ == BK), hence visible and inside the sequence.
-            const bool diag = j == qt;
+            // Only tiles reaching above the CTA's first query mask: every key of an earlier
+            // tile is below it, hence visible and inside the sequence.
+            const bool diag = j >= first_masked;
             float v[2][32];
             ld32(t_s, v[0]);
             ld32(t_s + 32, v[1]);
@@ -294,7 +303,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int kj = k0 + c * 32 + i;
-                        if (kj <= qi && kj < len) mxp[i & 7] = fmaxf(mxp[i & 7], v[c][i]);
+                        if (kj <= qa && kj < kend) mxp[i & 7] = fmaxf(mxp[i & 7], v[c][i]);
                     }
                 } else {
 #pragma unroll
@@ -332,9 +341,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
 #pragma unroll
                     for (int i = 0; i < 32; i += 2) {
                         const int kj = k0 + c * 32 + i;
-                        const float p0 = (kj <= qi && kj < len) ? exp2f(fmaf(v[c][i], scale_log2, -m_new)) : 0.0f;
+                        const float p0 = (kj <= qa && kj < kend) ? exp2f(fmaf(v[c][i], scale_log2, -m_new)) : 0.0f;
                         const float p1 =
-                            (kj + 1 <= qi && kj + 1 < len) ? exp2f(fmaf(v[c][i + 1], scale_log2, -m_new)) : 0.0f;
+                            (kj + 1 <= qa && kj + 1 < kend) ? exp2f(fmaf(v[c][i + 1], scale_log2, -m_new)) : 0.0f;
                         sp[(i >> 1) & 7] += p0 + p1;
                         pk[i / 2] = pack_bf16x2(p0, p1);
                     }
@@ -438,9 +447,9 @@ bool map2d(CUtensorMap *m, const bf16 *base, uint64_t rows, uint64_t cols) {
 bool attn_prefill_tc_supported(int Hq, int Hkv) { return Hq == 2 * Hkv && encode() != nullptr; }
 
 cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const bf16 *k_layer,
-                                   const bf16 *v_layer, const int32_t *cu_seqlens, const int32_t *slots, int B,
-                                   int max_len, int max_seqs, bf16 *out, int Hq, int Hkv, int max_ctx,
-                                   uint32_t *err) {
+                                   const bf16 *v_layer, const int32_t *cu_seqlens, const int32_t *slots,
+                                   const int32_t *row_pos, int B, int max_len, int max_seqs, bf16 *out, int Hq,
+                                   int Hkv, int max_ctx, uint32_t *err) {
     CUtensorMap mq, mk, mv;
     const uint64_t kv_rows = (uint64_t)max_seqs * Hkv * max_ctx;
     if (!map2d(&mq, q, (uint64_t)N, (uint64_t)Hq * D) || !map2d(&mk, k_layer, kv_rows, D) ||
@@ -450,7 +459,7 @@ cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const
     if (e != cudaSuccess) return e;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     return launch(lc, k_attn_prefill_tc, dim3((max_len + BQ - 1) / BQ, Hkv, B), dim3(THREADS), SMEM_BYTES, mq, mk, mv,
-                  cu_seqlens, slots, out, Hq, Hkv, max_ctx, scale_log2, err);
+                  cu_seqlens, slots, row_pos, out, Hq, Hkv, max_ctx, scale_log2, err);
 }
 
 }  // namespace q3

@@ -60,6 +60,7 @@ struct Rows {
     int32_t *row_slot = nullptr;          // [rows] written by the embedding kernel
     int32_t *row_pos = nullptr;           // [rows]
     int32_t *ctx_len = nullptr;           // [max_seqs] tokens cached per slot (nullptr: no bookkeeping)
+    bool append = false;                  // prefill rows continue their slot: positions start at ctx_len
     int32_t B = 0;
     int32_t rows = 0;
 };
@@ -141,10 +142,12 @@ cudaError_t launch_attn_prefill(const Launch &lc, const bf16 *q, const bf16 *k_l
 
 // --- attn_prefill_tc.cu (tcgen05 flash attention; q has N rows) ----------------------------
 bool attn_prefill_tc_supported(int Hq, int Hkv);
+// Rows of sequence b are positions row_pos[cu[b]] .. of its slot (non-zero when a call
+// continues a slot); keys come from the cache, causal mask aligned bottom-right.
 cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const bf16 *k_layer,
-                                   const bf16 *v_layer, const int32_t *cu_seqlens, const int32_t *slots, int B,
-                                   int max_len, int max_seqs, bf16 *out, int Hq, int Hkv, int max_ctx,
-                                   uint32_t *err);
+                                   const bf16 *v_layer, const int32_t *cu_seqlens, const int32_t *slots,
+                                   const int32_t *row_pos, int B, int max_len, int max_seqs, bf16 *out, int Hq,
+                                   int Hkv, int max_ctx, uint32_t *err);
 
 // --- attn_decode.cu ----------------------------------------------------------------------
 // Most key ranges per (sequence, KV head) of the decode attention.

@@ -56,7 +56,7 @@ __global__ void k_embed_rmsnorm(const int32_t *__restrict__ tokens, Rows r,
                 if (r.cu_seqlens[mid] <= row) lo = mid; else hi = mid - 1;
             }
             slot = r.slots[lo];
-            pos = row - r.cu_seqlens[lo];
+            pos = row - r.cu_seqlens[lo] + (r.append ? r.ctx_len[slot] : 0);
         } else {  // decode: one row per sequence, appended after the cached tokens
             slot = r.slots[row];
             pos = r.ctx_len[slot];

@@ -265,7 +265,8 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
             }
             if (attn_prefill_tc_supported(Hq, Hkv))
                 Q3_TRY(launch_attn_prefill_tc(lc, q, R, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots,
-                                              rows.B, max_len, k.max_seqs, attn, Hq, Hkv, k.max_ctx, err));
+                                              rows.row_pos, rows.B, max_len, k.max_seqs, attn, Hq, Hkv, k.max_ctx,
+                                              err));
             else
                 Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots, rows.B,
                                            max_len, attn, Hq, Hkv, k.max_ctx));
@@ -426,25 +427,32 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
     return QWEN3_OK;
 }
 
-int qwen3_prefill(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev,
-                  const int32_t *cu_host, const int32_t *slots_dev, const int32_t *slots_host,
-                  int32_t B, float *logits_dev, int32_t *next_tok_dev, void *stream_v) {
+namespace {
+
+// qwen3_prefill (append = false: every slot restarts at position 0) and qwen3_prefill_append
+// (the rows continue each slot after the tokens it holds).
+int prefill_impl(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev, const int32_t *cu_host,
+                 const int32_t *slots_dev, const int32_t *slots_host, int32_t B, float *logits_dev,
+                 int32_t *next_tok_dev, void *stream_v, bool append) {
     if (!c) return QWEN3_E_INVALID;
     if (!tokens_dev || !cu_dev || !cu_host || !slots_dev || !slots_host || !next_tok_dev)
         return c->fail(QWEN3_E_INVALID, "NULL argument");
     if (B < 1) return c->fail(QWEN3_E_INVALID, "B must be >= 1");
     if (B > c->cfg.max_seqs) return c->fail(QWEN3_E_CAPACITY, "B exceeds max_seqs");
     if (cu_host[0] != 0) return c->fail(QWEN3_E_INVALID, "cu_seqlens[0] must be 0");
+    if (int rc = check_slots(c, slots_host, B)) return rc;
     int max_len = 0;
     for (int b = 0; b < B; ++b) {
         const int n = cu_host[b + 1] - cu_host[b];
         if (n < 1) return c->fail(QWEN3_E_INVALID, "cu_seqlens must be strictly increasing");
-        if (n > c->cfg.max_ctx) return c->fail(QWEN3_E_CAPACITY, "sequence longer than max_ctx");
+        const int held = append ? c->len_host[slots_host[b]] : 0;
+        if (held + n > c->cfg.max_ctx) return c->fail(QWEN3_E_CAPACITY, "sequence longer than max_ctx");
         max_len = std::max(max_len, n);
     }
     const int N = cu_host[B];
     if (N > c->cfg.max_prefill_tokens) return c->fail(QWEN3_E_CAPACITY, "N exceeds max_prefill_tokens");
-    if (int rc = check_slots(c, slots_host, B)) return rc;
+    if (append && !attn_prefill_tc_supported(c->cfg.n_q_heads, c->cfg.n_kv_heads))
+        return c->fail(QWEN3_E_UNSUPPORTED, "appending to a slot needs the tensor-core prefill attention");
     if (c->dump && c->dump_bytes < (size_t)(c->cfg.n_layers + 1) * N * c->cfg.hidden * 4)
         return c->fail(QWEN3_E_CAPACITY, "debug dump buffer too small for this call");
 
@@ -453,11 +461,29 @@ int qwen3_prefill(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev
     lc.pdl = !(c->cfg.flags & QWEN3_FLAG_NO_PDL);
     lc.num_sms = c->num_sms;
     lc.counter = &c->launches;
-    const Rows rows = make_rows(c, cu_dev, slots_dev, B, N);
+    Rows rows = make_rows(c, cu_dev, slots_dev, B, N);
+    rows.append = append;
     cudaError_t e = run_forward(c, lc, tokens_dev, rows, false, max_len, 0, logits_dev, next_tok_dev);
-    if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_prefill");
-    for (int b = 0; b < B; ++b) c->len_host[slots_host[b]] = cu_host[b + 1] - cu_host[b];
+    if (e != cudaSuccess) return c->cuda_fail(e, append ? "qwen3_prefill_append" : "qwen3_prefill");
+    for (int b = 0; b < B; ++b)
+        c->len_host[slots_host[b]] = (append ? c->len_host[slots_host[b]] : 0) + cu_host[b + 1] - cu_host[b];
     return QWEN3_OK;
+}
+
+}  // namespace
+
+int qwen3_prefill(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev,
+                  const int32_t *cu_host, const int32_t *slots_dev, const int32_t *slots_host,
+                  int32_t B, float *logits_dev, int32_t *next_tok_dev, void *stream_v) {
+    return prefill_impl(c, tokens_dev, cu_dev, cu_host, slots_dev, slots_host, B, logits_dev, next_tok_dev, stream_v,
+                        false);
+}
+
+int qwen3_prefill_append(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev,
+                         const int32_t *cu_host, const int32_t *slots_dev, const int32_t *slots_host,
+                         int32_t B, float *logits_dev, int32_t *next_tok_dev, void *stream_v) {
+    return prefill_impl(c, tokens_dev, cu_dev, cu_host, slots_dev, slots_host, B, logits_dev, next_tok_dev, stream_v,
+                        true);
 }
 
 int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *slots_dev,
