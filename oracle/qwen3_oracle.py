@@ -299,6 +299,43 @@ def greedy(logits: np.ndarray):
     return tok, float(top2[1] - top2[0])
 
 
+# Candidates considered by the sampler: the most likely tokens, at most this many.
+SAMPLE_CANDIDATES = 1024
+
+
+def sample(logits: np.ndarray, temperature: float, top_k: int, top_p: float, u: float,
+           candidates: int = SAMPLE_CANDIDATES) -> int:
+    """Next token drawn from the logits of one row ([P2] 4.3 Sampler: argmax when no
+    temperature, otherwise temperature and Top-k/Top-p sampling; [P4] softmax with a
+    temperature).  The pages name the steps but not their exact rule; the reading taken:
+
+      temperature <= 0: the greedy choice (lowest index on ties).
+      Otherwise z = logits / temperature; tokens ordered by z descending, index ascending;
+      the first min(candidates, V) of that order are the candidates; top_k in [1, V) keeps
+      the first top_k of them; p_i proportional to exp(z_i - z_max) over the kept tokens;
+      top_p < 1 keeps the shortest prefix whose cumulative probability reaches top_p; the
+      token is the first kept one whose cumulative probability exceeds u * (the kept total),
+      u in [0, 1) a uniform draw supplied by the caller.
+    """
+    z = np.asarray(logits, dtype=DTYPE)
+    if temperature <= 0:
+        return greedy(z)[0]
+    z = z / DTYPE(temperature)
+    order = np.lexsort((np.arange(z.shape[0]), -z))  # z descending, then index ascending
+    n = min(int(candidates), z.shape[0])
+    if 1 <= top_k < n:
+        n = int(top_k)
+    kept = order[:n]
+    p = np.exp(z[kept] - z[kept[0]])
+    cum = np.cumsum(p)
+    if top_p < 1.0:
+        n = int(np.searchsorted(cum, DTYPE(top_p) * cum[-1], side="left")) + 1
+        n = min(n, len(kept))
+    target = DTYPE(u) * cum[n - 1]
+    i = int(np.searchsorted(cum[:n], target, side="right"))
+    return int(kept[min(i, n - 1)])
+
+
 def generate(cfg: Config, w: Weights, prompt: Sequence[int], steps: int,
              forced: Optional[Sequence[int]] = None) -> dict:
     """Prefill the prompt, then run ``steps`` single-token decode steps.

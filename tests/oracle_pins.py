@@ -360,6 +360,66 @@ def check_greedy_ties_and_margin(o):
     assert tok == 2 and abs(margin - 1.75) < 1e-15
 
 
+def _sample_brute(logits, temperature, top_k, top_p, candidates):
+    """Kept tokens and their probabilities, written independently with Python's sorted and math
+    (the reading of "第 3 章", 4.3 stated in the oracle's sample docstring)."""
+    z = [float(x) / temperature for x in logits]
+    order = sorted(range(len(z)), key=lambda i: (-z[i], i))[:candidates]
+    if 1 <= top_k < len(order):
+        order = order[:top_k]
+    w = [math.exp(z[i] - z[order[0]]) for i in order]
+    total = sum(w)
+    if top_p < 1.0:
+        acc, n = 0.0, 0
+        while n < len(order):
+            acc += w[n] / total
+            n += 1
+            if acc >= top_p - 1e-15:
+                break
+        order, w = order[:n], w[:n]
+        total = sum(w)
+    return order, [x / total for x in w]
+
+
+def check_sample_frequencies_brute_force(o):
+    """Draws on a fine grid of u reproduce the kept tokens' renormalised probabilities."""
+    rng = np.random.default_rng(11)
+    for temperature, top_k, top_p, v, cand in [(0.7, 0, 1.0, 9, 1024), (1.3, 4, 1.0, 9, 1024),
+                                              (0.9, 0, 0.8, 9, 1024), (1.1, 6, 0.7, 12, 1024),
+                                              (0.8, 0, 1.0, 12, 5), (1.0, 3, 0.9, 12, 8)]:
+        logits = rng.normal(0.0, 1.5, v)
+        logits[3] = logits[7]  # a tie, resolved by the lower index
+        kept, probs = _sample_brute(logits, temperature, top_k, top_p, cand)
+        grid = 20000
+        counts = {}
+        for j in range(grid):
+            t = o.sample(logits, temperature, top_k, top_p, (j + 0.5) / grid, candidates=cand)
+            counts[t] = counts.get(t, 0) + 1
+        assert set(counts) <= set(kept), (set(counts), kept)
+        for tok, pr in zip(kept, probs):
+            assert abs(counts.get(tok, 0) / grid - pr) < 2e-4, (temperature, top_k, top_p, tok, pr)
+        # the inverse CDF walks the kept tokens in order: low u gives the first kept token
+        assert o.sample(logits, temperature, top_k, top_p, 0.0, candidates=cand) == kept[0]
+
+
+def check_sample_limits_and_invariance(o):
+    rng = np.random.default_rng(12)
+    logits = rng.normal(0.0, 2.0, 50)
+    logits[17] = logits.max()  # tie with the maximum: argmax takes the lower index
+    best = int(np.argmax(logits))
+    for u in (0.0, 0.37, 0.999):
+        assert o.sample(logits, 0.0, 0, 1.0, u) == best          # no temperature: greedy
+        assert o.sample(logits, 0.8, 1, 1.0, u) == best          # top-1
+        assert o.sample(logits, 0.8, 0, 1e-9, u) == best         # nucleus of one token
+        # softmax(z / T) is unchanged by adding a constant, and by scaling z and T together
+        assert o.sample(logits, 0.8, 5, 0.9, u) == o.sample(logits + 3.25, 0.8, 5, 0.9, u)
+        assert o.sample(logits, 0.8, 5, 0.9, u) == o.sample(logits * 2.0, 1.6, 5, 0.9, u)
+    # flat logits over more tokens than candidates: only the first `candidates` indices are drawn
+    flat = np.zeros(3000)
+    assert o.sample(flat, 1.0, 0, 1.0, 0.99999, candidates=1024) == 1023
+    assert o.sample(flat, 1.0, 0, 1.0, 0.5, candidates=1024) == 512
+
+
 def check_shapes_worked_example(o):
     """The shape table of "第 3 章 前向与生成", section 5 (B=1, T=3, C=32, Hq=4, Hkv=2, D=8, V=64)."""
     import json
@@ -453,6 +513,8 @@ ALL_CHECKS = [
     check_causality_prefix,
     check_cache_consistency,
     check_greedy_ties_and_margin,
+    check_sample_frequencies_brute_force,
+    check_sample_limits_and_invariance,
     check_shapes_worked_example,
     check_model_vs_torch_composition,
 ]

@@ -45,6 +45,11 @@ MUTANTS = {
     "wq_transposed_heads": ('q = (u @ w["wq"].T).reshape(t, hq, d)',
                             'q = (u @ w["wq"].T).reshape(t, d, hq).transpose(0, 2, 1)'),
     "o_proj_head_order": ("h = h + o.reshape(t, hq * d)", "h = h + o.transpose(0, 2, 1).reshape(t, hq * d)"),
+    "sample_ascending_order": ("np.lexsort((np.arange(z.shape[0]), -z))", "np.lexsort((np.arange(z.shape[0]), z))"),
+    "sample_no_temperature": ("z = z / DTYPE(temperature)", "z = z"),
+    "sample_top_p_one_short": ("side=\"left\")) + 1", "side=\"left\"))"),
+    "sample_cdf_left": ("np.searchsorted(cum[:n], target, side=\"right\")", "np.searchsorted(cum[:n], target, side=\"left\")"),
+    "sample_ties_high_index": ("np.lexsort((np.arange(z.shape[0]), -z))", "np.lexsort((-np.arange(z.shape[0]), -z))"),
 }
 
 
