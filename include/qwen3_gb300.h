@@ -160,6 +160,28 @@ int qwen3_decode_step(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *
  * Decode steps run without a graph while the dump is on.  NULL turns it off. */
 int qwen3_set_debug_dump(qwen3_ctx *ctx, float *hidden_dev, size_t bytes);
 
+/* Per-sequence sampling settings: device arrays indexed by the row of a call (row b of a
+ * decode step is the sequence in slots[b]; row b of a prefill is sequence b).  The rule is
+ * qwen3_sample's (below).  The library reads them on the stream when each call runs, so the
+ * caller may rewrite the values (a fresh uniform draw per step, say) between calls in
+ * stream order; the pointers themselves are captured into the decode graphs. */
+typedef struct qwen3_sampling {
+    const float *temperature;  /* fp32 [max_seqs]; <= 0 selects the argmax for that row */
+    const int32_t *top_k;      /* int32 [max_seqs] */
+    const float *top_p;        /* fp32 [max_seqs] */
+    const float *uniform;      /* fp32 [max_seqs], each in [0, 1) */
+} qwen3_sampling;
+
+/* Next tokens drawn by sampling ("第 3 章", 4.3 Sampler): while set, every qwen3_prefill,
+ * qwen3_prefill_append and qwen3_decode_step writes its logits and then replaces the greedy
+ * next_tok_dev[b] by the qwen3_sample draw from them, in the same stream (inside the decode
+ * graph).  Those calls then need a logits_dev buffer (E_INVALID otherwise), and the
+ * persistent decode kernel is followed by one more launch.  sampling == NULL, or a NULL
+ * temperature, returns to greedy next tokens.  The structure is copied; the arrays are
+ * borrowed until the setting is replaced.  Errors: E_INVALID (a NULL array),
+ * E_UNSUPPORTED (a vocabulary the sampler cannot hold). */
+int qwen3_set_sampling(qwen3_ctx *ctx, const qwen3_sampling *sampling);
+
 /* Synchronises the device, then returns QWEN3_OK, E_CUDA (a pending CUDA error) or E_DEVICE
  * (the device error word was set; the word is cleared). */
 int qwen3_get_status(qwen3_ctx *ctx);
@@ -240,6 +262,32 @@ int qwen3_op_lmhead_argmax(const void *x_dev, int32_t B, int32_t C, const void *
 int qwen3_op_lmhead_argmax_noalloc(const void *x_dev, int32_t B, int32_t C,
                                    const void *embed_dev, int32_t V, float *logits_dev,
                                    int32_t *next_tok_dev, void *stream);
+
+/* Candidates qwen3_sample draws from: the most likely tokens of a row, at most this many. */
+#define QWEN3_SAMPLE_CANDIDATES 1024
+
+/* Next-token sampling ("第 3 章", 4.3 Sampler: argmax without a temperature, otherwise
+ * temperature with Top-k / Top-p; "手写Qwen3-0.6B推理", softmax with a temperature).
+ *
+ * logits_dev fp32 [B, V] row-major (as qwen3_decode_step / qwen3_prefill write them); per row b
+ * temperature_dev[b] (fp32), top_k_dev[b] (int32), top_p_dev[b] (fp32) and uniform_dev[b]
+ * (fp32, a uniform draw in [0, 1) the caller makes); next_tok_dev[b] (int32) receives the token.
+ * All are device pointers; nothing is allocated; the call is asynchronous on `stream`.
+ *
+ * Rule per row.  temperature <= 0: the argmax (lowest index on ties), the other arguments
+ * unused.  Otherwise: tokens ordered by logit descending, index ascending; the first
+ * min(QWEN3_SAMPLE_CANDIDATES, V) are the candidates; top_k in [1, candidates) keeps the first
+ * top_k of them (any other top_k keeps all); p_i = exp((l_i - l_max) / temperature) over the kept
+ * tokens; top_p < 1 keeps the shortest prefix whose cumulative p reaches top_p times their total
+ * (top_p >= 1 keeps all); the token is the first kept one whose cumulative p exceeds
+ * uniform * (the total of what is left).  Arithmetic is fp32: a draw within about 1e-6
+ * (relative) of a cumulative boundary may land on the neighbouring token of an fp64 evaluation.
+ *
+ * Errors: E_INVALID (NULL pointer, B outside [1, 65535], V < 1), E_CUDA (launch); the message
+ * is returned by qwen3_last_error(NULL). */
+int qwen3_sample(const float *logits_dev, int32_t B, int32_t V, const float *temperature_dev,
+                 const int32_t *top_k_dev, const float *top_p_dev, const float *uniform_dev,
+                 int32_t *next_tok_dev, void *stream);
 
 /* Releases the context and its graphs.  Does not free the arena or any caller memory. */
 void qwen3_free(qwen3_ctx *ctx);

@@ -31,6 +31,10 @@ QWEN3_EPI_SWIGLU = 2
 _P = ctypes.c_void_p
 
 
+class qwen3_sampling(ctypes.Structure):
+    _fields_ = [("temperature", _P), ("top_k", _P), ("top_p", _P), ("uniform", _P)]
+
+
 class qwen3_config(ctypes.Structure):
     _fields_ = [
         ("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
@@ -75,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_prefill_append": (ctypes.c_int, [_P, _P, _P, pi32, _P, pi32, i32, _P, _P, _P]),
         "qwen3_decode_step": (ctypes.c_int, [_P, _P, _P, pi32, i32, _P, _P, _P]),
         "qwen3_set_debug_dump": (ctypes.c_int, [_P, _P, sz]),
+        "qwen3_set_sampling": (ctypes.c_int, [_P, ctypes.POINTER(qwen3_sampling)]),
         "qwen3_get_status": (ctypes.c_int, [_P]),
         "qwen3_last_error": (ctypes.c_char_p, [_P]),
         "qwen3_slot_length": (i32, [_P, i32]),
@@ -86,6 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_op_lmhead_workspace_bytes": (sz, [i32]),
         "qwen3_op_lmhead_argmax": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P, sz, _P]),
         "qwen3_op_lmhead_argmax_noalloc": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P]),
+        "qwen3_sample": (ctypes.c_int, [_P, i32, i32, _P, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -149,6 +155,17 @@ def qwen3_set_debug_dump(ctx, hidden_ptr: Optional[int], nbytes: int):
     _check(load_library().qwen3_set_debug_dump(ctx, hidden_ptr, nbytes), ctx)
 
 
+def qwen3_set_sampling(ctx, temperature_ptr: Optional[int], top_k_ptr: Optional[int] = None,
+                       top_p_ptr: Optional[int] = None, uniform_ptr: Optional[int] = None):
+    """Per-row sampling arrays (device pointers) for the context's next tokens; a None
+    temperature returns to greedy next tokens."""
+    if temperature_ptr is None:
+        _check(load_library().qwen3_set_sampling(ctx, None), ctx)
+        return
+    sp = qwen3_sampling(temperature_ptr, top_k_ptr, top_p_ptr, uniform_ptr)
+    _check(load_library().qwen3_set_sampling(ctx, ctypes.byref(sp)), ctx)
+
+
 def qwen3_get_status(ctx) -> int:
     return int(load_library().qwen3_get_status(ctx))
 
@@ -199,6 +216,37 @@ def qwen3_op_lmhead_argmax_noalloc(x_ptr: int, B: int, C: int, embed_ptr: int, V
     """lm_head + argmax with the library's fixed scratch instead of a caller workspace (B <= 32)."""
     _check(load_library().qwen3_op_lmhead_argmax_noalloc(x_ptr, B, C, embed_ptr, V, logits_ptr, next_ptr,
                                                          stream), None)
+
+
+QWEN3_SAMPLE_CANDIDATES = 1024
+
+
+def qwen3_sample(logits_ptr: int, B: int, V: int, temperature_ptr: int, top_k_ptr: int, top_p_ptr: int,
+                 uniform_ptr: int, next_ptr: int, stream: int = 0):
+    """Temperature / top-k / top-p draw of one token per row from fp32 logits [B, V]; the per-row
+    parameters and the uniform draws are device arrays of B values."""
+    _check(load_library().qwen3_sample(logits_ptr, B, V, temperature_ptr, top_k_ptr, top_p_ptr, uniform_ptr,
+                                       next_ptr, stream), None)
+
+
+def sample(logits, temperature, top_k, top_p, uniform, out=None):
+    """qwen3_sample on CUDA tensors: logits fp32 [B, V]; temperature, top_p, uniform fp32 [B];
+    top_k int32 [B]; returns (or fills) int32 [B] on the current stream."""
+    import torch
+
+    B, V = logits.shape
+    for t, dt in ((logits, torch.float32), (temperature, torch.float32), (top_k, torch.int32),
+                  (top_p, torch.float32), (uniform, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise Qwen3Error(QWEN3_E_INVALID, "sample: expected contiguous CUDA tensors of the documented dtypes")
+    for t in (temperature, top_k, top_p, uniform):
+        if t.numel() != B:
+            raise Qwen3Error(QWEN3_E_INVALID, "sample: one parameter per row")
+    if out is None:
+        out = torch.empty(B, dtype=torch.int32, device=logits.device)
+    qwen3_sample(logits.data_ptr(), B, V, temperature.data_ptr(), top_k.data_ptr(), top_p.data_ptr(),
+                 uniform.data_ptr(), out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    return out
 
 
 # --- device-memory owner -------------------------------------------------------------------
@@ -281,6 +329,22 @@ class Model:
     def set_debug_dump(self, buf):
         qwen3_set_debug_dump(self.ctx, buf.data_ptr() if buf is not None else None,
                              buf.numel() * 4 if buf is not None else 0)
+
+    def set_sampling(self, temperature=None, top_k=None, top_p=None, uniform=None):
+        """Per-row sampling settings as CUDA tensors [max_seqs] (fp32, int32, fp32, fp32);
+        the tensors are kept alive here and may be rewritten in stream order between calls.
+        No arguments: greedy next tokens."""
+        torch = self.torch
+        if temperature is None:
+            qwen3_set_sampling(self.ctx, None)
+            self._sampling = None
+            return
+        for t, dt in ((temperature, torch.float32), (top_k, torch.int32), (top_p, torch.float32),
+                      (uniform, torch.float32)):
+            if t is None or t.dtype != dt or not t.is_cuda or not t.is_contiguous() or t.numel() < self.cfg.max_seqs:
+                raise Qwen3Error(QWEN3_E_INVALID, "set_sampling: contiguous CUDA tensors of max_seqs values")
+        qwen3_set_sampling(self.ctx, temperature.data_ptr(), top_k.data_ptr(), top_p.data_ptr(), uniform.data_ptr())
+        self._sampling = (temperature, top_k, top_p, uniform)
 
     def status(self) -> int:
         return qwen3_get_status(self.ctx)

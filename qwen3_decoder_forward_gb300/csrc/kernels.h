@@ -191,6 +191,13 @@ struct DecodePersistentArgs {
 bool decode_persistent_supported(int C, int Hq, int Hkv, int head_dim, int I, int B, int num_sms);
 cudaError_t launch_decode_persistent(const Launch &lc, const DecodePersistentArgs &p);
 
+// --- sample.cu ---------------------------------------------------------------------------
+// Temperature / top-k / top-p draw of next_tok[b] from logits fp32 [B, V] (the rule of
+// qwen3_sample); launched without programmatic dependent launch, after the lm_head.
+bool sample_supported(int V);
+cudaError_t launch_sample(const Launch &lc, const float *logits, int B, int V, const float *temperature,
+                          const int32_t *top_k, const float *top_p, const float *uniform, int32_t *next_tok);
+
 // --- lmhead.cu ---------------------------------------------------------------------------
 // next_tok[b] = argmax_v X[b] . E[v] (lowest index on ties); logits[B, V] if not null.
 // Also sets ctx_len[slot] = position + 1 of each sequence's last row.

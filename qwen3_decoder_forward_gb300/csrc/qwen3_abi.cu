@@ -126,6 +126,7 @@ struct GraphEntry {
     int B, n_split;
     const void *tokens, *slots;
     void *logits, *next;
+    qwen3_sampling sampling;
     cudaGraphExec_t exec;
     int64_t kernels;
 };
@@ -141,6 +142,7 @@ struct qwen3_ctx {
     cudaStream_t cap_stream = nullptr;
     std::vector<GraphEntry> graphs;
     int64_t launches = 0;
+    qwen3_sampling sampling = {};  // all NULL: greedy next tokens
     std::string err;
 
     template <typename T>
@@ -165,6 +167,18 @@ namespace {
         cudaError_t e_ = (x);                   \
         if (e_ != cudaSuccess) return e_;       \
     } while (0)
+
+bool sampling_on(const qwen3_ctx *c) { return c->sampling.temperature != nullptr; }
+
+// With sampling set, the next tokens are drawn from the logits the lm_head just wrote
+// (replacing its argmax); otherwise nothing to do.
+cudaError_t draw_next(qwen3_ctx *c, const Launch &lc, const float *logits, int B, int32_t *next) {
+    if (!sampling_on(c)) return cudaSuccess;
+    Launch ls = lc;
+    ls.pdl = false;
+    const qwen3_sampling &sp = c->sampling;
+    return launch_sample(ls, logits, B, c->cfg.vocab, sp.temperature, sp.top_k, sp.top_p, sp.uniform, next);
+}
 
 // Everything one call runs, in stream order.  `decode` selects the GEMV projections and the
 // split-KV attention; prefill uses the tiled GEMM and the flash prefill attention.
@@ -280,8 +294,9 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
     bf16 *last = c->at<bf16>(L.o_last);
     Q3_TRY(launch_final_norm(lc, mlp ? res[k.n_layers & 1] : resid, rows.cu_seqlens, rows.B,
                              c->at<float>(L.o_gfinal), last, C, k.rms_eps));
-    return launch_lmhead_argmax(lc, last, rows.B, C, embed, k.vocab, logits, c->at<float>(L.o_pval),
-                                c->at<int32_t>(L.o_pidx), c->n_parts, next, rows);
+    Q3_TRY(launch_lmhead_argmax(lc, last, rows.B, C, embed, k.vocab, logits, c->at<float>(L.o_pval),
+                                c->at<int32_t>(L.o_pidx), c->n_parts, next, rows));
+    return draw_next(c, lc, logits, rows.B, next);
 }
 
 Rows make_rows(qwen3_ctx *c, const int32_t *cu, const int32_t *slots, int B, int rows) {
@@ -439,6 +454,7 @@ int prefill_impl(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev,
         return c->fail(QWEN3_E_INVALID, "NULL argument");
     if (B < 1) return c->fail(QWEN3_E_INVALID, "B must be >= 1");
     if (B > c->cfg.max_seqs) return c->fail(QWEN3_E_CAPACITY, "B exceeds max_seqs");
+    if (sampling_on(c) && !logits_dev) return c->fail(QWEN3_E_INVALID, "sampling needs the logits buffer");
     if (cu_host[0] != 0) return c->fail(QWEN3_E_INVALID, "cu_seqlens[0] must be 0");
     if (int rc = check_slots(c, slots_host, B)) return rc;
     int max_len = 0;
@@ -494,6 +510,7 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
         return c->fail(QWEN3_E_INVALID, "NULL argument");
     if (B < 1) return c->fail(QWEN3_E_INVALID, "B must be >= 1");
     if (B > c->cfg.max_seqs) return c->fail(QWEN3_E_CAPACITY, "B exceeds max_seqs");
+    if (sampling_on(c) && !logits_dev) return c->fail(QWEN3_E_INVALID, "sampling needs the logits buffer");
     if (int rc = check_slots(c, slots_host, B)) return rc;
     int max_len = 0;
     for (int b = 0; b < B; ++b) {
@@ -556,6 +573,7 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
         lc.num_sms = c->num_sms;
         lc.counter = &c->launches;
         cudaError_t e = launch_decode_persistent(lc, p);
+        if (e == cudaSuccess) e = draw_next(c, lc, logits_dev, B, next_tok_dev);
         if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_decode_step (persistent)");
         for (int b = 0; b < B; ++b) c->len_host[slots_host[b]] += 1;
         return QWEN3_OK;
@@ -574,7 +592,8 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
         GraphEntry *g = nullptr;
         for (auto &x : c->graphs)
             if (x.B == B && x.n_split == n_split && x.tokens == tokens_dev &&
-                x.slots == slots_dev && x.logits == logits_dev && x.next == next_tok_dev)
+                x.slots == slots_dev && x.logits == logits_dev && x.next == next_tok_dev &&
+                !memcmp(&x.sampling, &c->sampling, sizeof(qwen3_sampling)))
                 g = &x;
         if (!g) {
             Launch lc;
@@ -608,7 +627,7 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
                 return c->cuda_fail(e, "decode graph instantiate");
             }
             c->graphs.push_back(GraphEntry{B, n_split, tokens_dev, slots_dev, logits_dev,
-                                           next_tok_dev, exec, kernels});
+                                           next_tok_dev, c->sampling, exec, kernels});
             g = &c->graphs.back();
         }
         cudaError_t e = cudaGraphLaunch(g->exec, st);
@@ -616,6 +635,20 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
         c->launches += g->kernels;
     }
     for (int b = 0; b < B; ++b) c->len_host[slots_host[b]] += 1;
+    return QWEN3_OK;
+}
+
+int qwen3_set_sampling(qwen3_ctx *c, const qwen3_sampling *sp) {
+    if (!c) return QWEN3_E_INVALID;
+    if (!sp || !sp->temperature) {
+        c->sampling = qwen3_sampling{};
+        return QWEN3_OK;
+    }
+    if (!sp->top_k || !sp->top_p || !sp->uniform)
+        return c->fail(QWEN3_E_INVALID, "qwen3_set_sampling: NULL array");
+    if (!sample_supported(c->cfg.vocab))
+        return c->fail(QWEN3_E_UNSUPPORTED, "qwen3_set_sampling: vocabulary too large for the sampler");
+    c->sampling = *sp;
     return QWEN3_OK;
 }
 

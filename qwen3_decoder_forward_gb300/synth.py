@@ -123,6 +123,36 @@ def make_lengths(n_seqs: int, lo: int, hi: int, seed: int) -> List[int]:
     return [int(x) for x in torch.randint(lo, hi + 1, (n_seqs,), generator=_gen(seed), dtype=torch.int64)]
 
 
+SAMPLE_SEED = 5
+
+# Per-row sampling settings, cycled over the rows of a batch: greedy rows, temperature alone,
+# Top-k alone, Top-p alone and both, with k on either side of the candidate count.
+SAMPLE_TEMPERATURES = (0.0, 0.7, 1.0, 1.3, 0.9, 0.5)
+SAMPLE_TOP_K = (0, 0, 50, 0, 20, 1000, 1, 5000)
+SAMPLE_TOP_P = (1.0, 1.0, 1.0, 0.9, 0.8, 0.95, 0.5)
+
+
+def make_sampling_batch(B: int, V: int, seed: int = SAMPLE_SEED, logit_std: float = 2.0,
+                        grid: float = 0.0, spikes: int = 4):
+    """Inputs of one sampling call: fp32 logits [B, V] ~ N(0, logit_std) with `spikes` tokens
+    per row raised by U(4, 12) (a confident next-token distribution; rounded to multiples of
+    `grid` when grid > 0, which makes many ties), the per-row settings above, and one uniform
+    draw in [0, 1) per row.  Returns (logits, temperature, top_k, top_p, uniform) on the CPU."""
+    g = _gen(seed)
+    logits = torch.randn((B, V), generator=g) * logit_std
+    if spikes:
+        idx = torch.randint(0, V, (B, spikes), generator=g)
+        logits.scatter_add_(1, idx, 4.0 + 8.0 * torch.rand((B, spikes), generator=g))
+    if grid > 0:
+        logits = torch.round(logits / grid) * grid
+    temperature = torch.tensor([SAMPLE_TEMPERATURES[b % len(SAMPLE_TEMPERATURES)] for b in range(B)],
+                               dtype=torch.float32)
+    top_k = torch.tensor([SAMPLE_TOP_K[b % len(SAMPLE_TOP_K)] for b in range(B)], dtype=torch.int32)
+    top_p = torch.tensor([SAMPLE_TOP_P[b % len(SAMPLE_TOP_P)] for b in range(B)], dtype=torch.float32)
+    uniform = torch.rand((B,), generator=g)
+    return logits.float(), temperature, top_k, top_p, uniform
+
+
 def cu_seqlens(lengths: List[int]) -> List[int]:
     out = [0]
     for n in lengths:

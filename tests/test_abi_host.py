@@ -74,6 +74,20 @@ def test_null_context_calls_are_rejected(lib):
     lib.qwen3_free(None)
 
 
+def test_sample_rejects_null_and_bad_sizes_before_any_launch(lib):
+    one = 16  # any non-NULL value: the checks return before a pointer is used
+    args = [one, 1, 8, one, one, one, one, one, None]
+    for i in (0, 3, 4, 5, 6, 7):
+        bad = list(args)
+        bad[i] = None
+        assert lib.qwen3_sample(*bad) == binding.QWEN3_E_INVALID
+        assert "NULL" in binding.qwen3_last_error(None)
+    for B, V in ((0, 8), (65536, 8), (1, 0)):
+        bad = list(args)
+        bad[1], bad[2] = B, V
+        assert lib.qwen3_sample(*bad) == binding.QWEN3_E_INVALID
+
+
 def test_package_import_loads_no_cuda():
     import importlib
     import sys
