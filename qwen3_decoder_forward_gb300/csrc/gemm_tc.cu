@@ -98,7 +98,7 @@ struct EpiArgs {
     // [rows, Hq, 128], k and v into the layer's cache at (row_slot, row_pos).
     const int32_t *row_slot, *row_pos;
     const float *q_gain, *k_gain;
-    const float2 *rope;
+    const float2 *rope_t;  // (cos, sin) by frequency: rope_t[i * max_ctx + pos], i < 64
     bf16 *q_out, *k_layer, *v_layer;
     int Hq, Hkv, max_ctx;
     float eps;
@@ -295,12 +295,14 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                                     xh[j] = __uint_as_float(hi[j]);
                                 }
                             } else {
-                                const float2 *cs = ea.rope + (size_t)pos * 64 + c * 32;
+                                // frequency-major table: the 32 lanes (rows at mostly
+                                // consecutive positions) read neighbouring entries
+                                const float2 *cs = ea.rope_t + (size_t)(c * 32) * ea.max_ctx + pos;
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) {
                                     const float a0 = __uint_as_float(lo[j]) * inv * gain[c * 32 + j];
                                     const float b0 = __uint_as_float(hi[j]) * inv * gain[64 + c * 32 + j];
-                                    const float2 r = cs[j];
+                                    const float2 r = cs[(size_t)j * ea.max_ctx];
                                     xl[j] = a0 * r.x - b0 * r.y;  // x_i cos - x_{i+64} sin
                                     xh[j] = b0 * r.x + a0 * r.y;  // x_{i+64} cos + x_i sin
                                 }
@@ -386,7 +388,7 @@ cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const 
 }
 
 cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, const Rows &r,
-                               const float *q_gain, const float *k_gain, const float2 *rope, bf16 *q_out,
+                               const float *q_gain, const float *k_gain, const float2 *rope_t, bf16 *q_out,
                                bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv, int max_ctx, float eps,
                                uint32_t *err) {
     if (!gemm_tc_supported(M, K, N) || N != (Hq + 2 * Hkv) * 128) return cudaErrorInvalidValue;
@@ -397,7 +399,7 @@ cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, co
     ea.row_pos = r.row_pos;
     ea.q_gain = q_gain;
     ea.k_gain = k_gain;
-    ea.rope = rope;
+    ea.rope_t = rope_t;
     ea.q_out = q_out;
     ea.k_layer = k_layer;
     ea.v_layer = v_layer;

@@ -28,7 +28,7 @@ struct Layout {
     // per-layer strides (bytes) and offsets within layer 0
     size_t layer_bytes = 0, o_wqkv = 0, o_wo = 0, o_wog = 0, o_wgu = 0, o_wdown = 0, o_wdownT = 0, o_gin = 0,
            o_gpost = 0, o_gq = 0, o_gk = 0;
-    size_t o_layers = 0, o_embed = 0, o_gfinal = 0, o_rope = 0, o_kcache = 0, o_vcache = 0,
+    size_t o_layers = 0, o_embed = 0, o_gfinal = 0, o_rope = 0, o_rope_t = 0, o_kcache = 0, o_vcache = 0,
            kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0;
     size_t o_resid = 0, o_xn = 0, o_qkv = 0, o_q = 0, o_attn = 0, o_act = 0, o_rowslot = 0,
            o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0, o_pflags = 0, o_pres = 0,
@@ -87,6 +87,7 @@ Layout make_layout(const qwen3_config &c) {
     L.o_embed = take((size_t)c.vocab * C * 2);
     L.o_gfinal = take(C * 4);
     L.o_rope = take((size_t)c.max_ctx * (D / 2) * 8);
+    L.o_rope_t = take((size_t)c.max_ctx * (D / 2) * 8);  // the same table, frequency-major
     L.kv_layer_bytes = (size_t)c.max_seqs * Hkv * c.max_ctx * D * 2;
     L.o_kcache = take(L.kv_layer_bytes * c.n_layers);
     L.o_vcache = take(L.kv_layer_bytes * c.n_layers);
@@ -196,6 +197,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
     uint32_t *err = c->at<uint32_t>(L.o_err);
     const bf16 *embed = c->at<bf16>(L.o_embed);
     const float2 *rope = c->at<float2>(L.o_rope);
+    const float2 *rope_t = c->at<float2>(L.o_rope_t);
     auto dump = [&](int l, const float *src) -> cudaError_t {
         if (!c->dump) return cudaSuccess;
         return cudaMemcpyAsync(c->dump + (size_t)l * R * C, src, (size_t)R * C * 4,
@@ -270,7 +272,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
             };
             if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
             if (gemm_tc_supported(R, C, qkv_n)) {  // QK-norm, RoPE and the KV write in the GEMM epilogue
-                Q3_TRY(launch_gemm_tc_qkv(lc, xn, R, C, w_qkv, qkv_n, rows, g_q, g_k, rope, q, c->kcache(l),
+                Q3_TRY(launch_gemm_tc_qkv(lc, xn, R, C, w_qkv, qkv_n, rows, g_q, g_k, rope_t, q, c->kcache(l),
                                           c->vcache(l), Hq, Hkv, k.max_ctx, k.rms_eps, err));
             } else {
                 Q3_TRY(gemm(xn, C, w_qkv, qkv_n, EPI_F32, qkv));
@@ -419,6 +421,11 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
                 tab[(size_t)p * (D / 2) + i] = make_float2((float)std::cos(a), (float)std::sin(a));
             }
         Q3_TRY(cudaMemcpyAsync(c->arena + lay.o_rope, tab.data(), tab.size() * sizeof(float2),
+                               cudaMemcpyHostToDevice, st));
+        std::vector<float2> tab_t(tab.size());  // [D/2][max_ctx]: rows at consecutive positions
+        for (int p = 0; p < cfg->max_ctx; ++p)  // read neighbouring entries
+            for (size_t i = 0; i < D / 2; ++i) tab_t[i * cfg->max_ctx + p] = tab[(size_t)p * (D / 2) + i];
+        Q3_TRY(cudaMemcpyAsync(c->arena + lay.o_rope_t, tab_t.data(), tab_t.size() * sizeof(float2),
                                cudaMemcpyHostToDevice, st));
         // The KV cache starts at zero: the tensor-core prefill attention multiplies whole
         // 128-key tiles, so rows past a sequence's end (weight 0) must hold finite values --
