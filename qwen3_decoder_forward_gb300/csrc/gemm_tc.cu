@@ -102,7 +102,65 @@ struct EpiArgs {
     bf16 *q_out, *k_layer, *v_layer;
     int Hq, Hkv, max_ctx;
     float eps;
+    // RMSNorm folded into the GEMMs around it (RowNorm in kernels.h): scale rows by
+    // rsqrt(sum(ss_in[row][*]) / norm_c + eps) (QKV, SwiGLU), or, with xn_out (residual add),
+    // also write bf16(h * gamma_out) and the sum of squares of each 128-column half of h.
+    const float *ss_in;
+    float *ss_out;
+    bf16 *xn_out;
+    const float *gamma_out;
+    int norm_c;
 };
+
+// rsqrt(mean of squares + eps) of a row from its per-128-column partial sums (fixed order).
+__device__ __forceinline__ float row_scale(const EpiArgs &ea, int row) {
+    const int np = ea.norm_c / 128;
+    const float *p = ea.ss_in + (size_t)row * np;
+    float s = 0.0f;
+    for (int i = 0; i < np; ++i) s += p[i];
+    return rsqrtf(s / (float)ea.norm_c + ea.eps);
+}
+
+// Residual add of 32 columns that also writes bf16(h * gamma) of the new values (the operand
+// of the next projection, before its row scale) and adds their squares to *ss.
+__device__ __forceinline__ void store_resid_norm(const uint32_t *v, int row, int col, int N, const EpiArgs &ea,
+                                                 float *ss) {
+    float4 *dst = reinterpret_cast<float4 *>((float *)ea.out + (size_t)row * N + col);
+    const float4 *g4 = reinterpret_cast<const float4 *>(ea.gamma_out + col);
+    uint32_t o[16];
+    float s = *ss;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float4 r = dst[j];
+        r.x += __uint_as_float(v[4 * j]);
+        r.y += __uint_as_float(v[4 * j + 1]);
+        r.z += __uint_as_float(v[4 * j + 2]);
+        r.w += __uint_as_float(v[4 * j + 3]);
+        dst[j] = r;
+        s += r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w;
+        const float4 g = g4[j];
+        o[2 * j] = pack_bf16x2(r.x * g.x, r.y * g.y);
+        o[2 * j + 1] = pack_bf16x2(r.z * g.z, r.w * g.w);
+    }
+    *ss = s;
+    uint4 *xd = reinterpret_cast<uint4 *>(ea.xn_out + (size_t)row * N + col);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) xd[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+}
+
+// SwiGLU of row-scaled gate/up pairs: silu(rs * g) * (rs * u), bf16.
+__device__ __forceinline__ void store_swiglu_scaled(const uint32_t *v, float rs, int row, int col, int N, void *out) {
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float a0 = silu(rs * __uint_as_float(v[4 * j])) * (rs * __uint_as_float(v[4 * j + 1]));
+        const float a1 = silu(rs * __uint_as_float(v[4 * j + 2])) * (rs * __uint_as_float(v[4 * j + 3]));
+        o[j] = pack_bf16x2(a0, a1);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>((bf16 *)out + (size_t)row * (N / 2) + col / 2);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
 
 __device__ __forceinline__ void store_chunk(int EPI_, const uint32_t *v, int row, int col, int N, void *out) {
     if (EPI_ == EPI_F32) {
@@ -244,7 +302,24 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
             const int m0 = (t / tiles_n) * TC_BM, n0 = (t % tiles_n) * TC_BN;
             const int row = m0 + q * 32 + lane;
             const uint32_t t_row = tmem + a * TC_BN + ((uint32_t)(q * 32) << 16);
-            if (EPI != EPI_QKV) {
+            if (EPI == EPI_RESID_ADD && ea.xn_out) {
+                float ss = 0.0f;
+#pragma unroll 1
+                for (int c = half * 4; c < half * 4 + 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(t_row + c * 32, v);
+                    if (row < M) store_resid_norm(v, row, n0 + c * 32, N, ea, &ss);
+                }
+                if (row < M) ea.ss_out[(size_t)row * (N / 128) + n0 / 128 + half] = ss;
+            } else if (EPI == EPI_SWIGLU && ea.ss_in) {
+                const float rs = row < M ? row_scale(ea, row) : 0.0f;
+#pragma unroll 1
+                for (int c = half * 4; c < half * 4 + 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(t_row + c * 32, v);
+                    if (row < M) store_swiglu_scaled(v, rs, row, n0 + c * 32, N, ea.out);
+                }
+            } else if (EPI != EPI_QKV) {
 #pragma unroll 1
                 for (int c = half * 4; c < half * 4 + 4; ++c) {
                     uint32_t v[32];
@@ -255,12 +330,14 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                 // two heads of 128 columns per tile: head index within [q | k | v]
                 const int slot = row < M ? ea.row_slot[row] : 0;
                 const int pos = row < M ? ea.row_pos[row] : 0;
+                // the input RMSNorm's row scale (1 when the operand came normalised)
+                const float rs = ea.ss_in && row < M ? row_scale(ea, row) : 1.0f;
                 {
                     const int hh = half;
                     const int head = n0 / 128 + hh;
                     const uint32_t th = t_row + hh * 128;
                     const bool is_v = head >= ea.Hq + ea.Hkv;
-                    float inv = 1.0f;
+                    float inv = rs;  // V: the row scale alone
                     if (!is_v) {  // pass 1: sum of squares over the head's 128 columns
                         float ss = 0.0f;
 #pragma unroll 1
@@ -270,7 +347,8 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
 #pragma unroll
                             for (int j = 0; j < 32; ++j) ss += __uint_as_float(v[j]) * __uint_as_float(v[j]);
                         }
-                        inv = rsqrtf(ss * (1.0f / 128.0f) + ea.eps);
+                        // head RMSNorm of the row-scaled values rs * v
+                        inv = rs * rsqrtf(ss * (rs * rs) * (1.0f / 128.0f) + ea.eps);
                     }
                     const float *gain = head < ea.Hq ? ea.q_gain : ea.k_gain;
                     bf16 *dst;
@@ -291,8 +369,8 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                             if (is_v) {
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) {
-                                    xl[j] = __uint_as_float(lo[j]);
-                                    xh[j] = __uint_as_float(hi[j]);
+                                    xl[j] = __uint_as_float(lo[j]) * inv;
+                                    xh[j] = __uint_as_float(hi[j]) * inv;
                                 }
                             } else {
                                 // frequency-major table: the 32 lanes (rows at mostly
@@ -372,13 +450,21 @@ bool gemm_tc_supported(int M, int K, int N) {
 }
 
 cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, int epi,
-                           void *out, uint32_t *err) {
+                           void *out, uint32_t *err, const RowNorm &rn) {
     if (!gemm_tc_supported(M, K, N) || epi == EPI_QKV) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(W)) & 15) return cudaErrorInvalidValue;
+    if (rn.xn_out && (epi != EPI_RESID_ADD || !rn.ss_out || !rn.gamma_out || N % 128)) return cudaErrorInvalidValue;
+    if (rn.ss_in && (epi != EPI_SWIGLU || rn.norm_c != K || K % 128)) return cudaErrorInvalidValue;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, M, K, TC_BM) || !make_map(&mb, W, N, K, TC_BN)) return cudaErrorInvalidValue;
     EpiArgs ea = {};
     ea.out = out;
+    ea.ss_in = rn.ss_in;
+    ea.ss_out = rn.ss_out;
+    ea.xn_out = rn.xn_out;
+    ea.gamma_out = rn.gamma_out;
+    ea.norm_c = rn.norm_c;
+    ea.eps = rn.eps;
     switch (epi) {
         case EPI_F32: return run_tcp<EPI_F32>(lc, ma, mb, M, N, K, ea, err);
         case EPI_RESID_ADD: return run_tcp<EPI_RESID_ADD>(lc, ma, mb, M, N, K, ea, err);
@@ -390,8 +476,8 @@ cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const 
 cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, const Rows &r,
                                const float *q_gain, const float *k_gain, const float2 *rope_t, bf16 *q_out,
                                bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv, int max_ctx, float eps,
-                               uint32_t *err) {
-    if (!gemm_tc_supported(M, K, N) || N != (Hq + 2 * Hkv) * 128) return cudaErrorInvalidValue;
+                               uint32_t *err, const float *ss_in) {
+    if (!gemm_tc_supported(M, K, N) || N != (Hq + 2 * Hkv) * 128 || (ss_in && K % 128)) return cudaErrorInvalidValue;
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, M, K, TC_BM) || !make_map(&mb, W, N, K, TC_BN)) return cudaErrorInvalidValue;
     EpiArgs ea = {};
@@ -407,6 +493,8 @@ cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, co
     ea.Hkv = Hkv;
     ea.max_ctx = max_ctx;
     ea.eps = eps;
+    ea.ss_in = ss_in;
+    ea.norm_c = K;
     return run_tcp<EPI_QKV>(lc, ma, mb, M, N, K, ea, err);
 }
 

@@ -88,15 +88,28 @@ cudaError_t launch_gemm(const Launch &lc, const bf16 *A, int M, int K, const bf1
 
 // --- gemm_tc.cu (prefill on tcgen05 tensor cores; K % 64 == 0, N % 256 == 0) -------------
 bool gemm_tc_supported(int M, int K, int N);
+// RMSNorm folded into the projections around it ("第 3 章", 3.2: the norm between the
+// residual add and the next projection).  The residual-add GEMM writes, besides h, the bf16
+// operand h * gamma_out (xn_out [M, N]) and the sums of squares of h over each 128 columns
+// (ss_out [M, N / 128]); the next GEMM reads that operand and multiplies row r of its product
+// by rsqrt(sum(ss_in[r][*]) / norm_c + eps), which equals projecting RMSNorm(h) * gamma.
+struct RowNorm {
+    const float *ss_in = nullptr;    // SwiGLU (and QKV): scale rows by the norm of their input
+    float *ss_out = nullptr;         // residual add: per-128-column sums of squares of h
+    bf16 *xn_out = nullptr;          // residual add: bf16 h * gamma_out
+    const float *gamma_out = nullptr;
+    int norm_c = 0;                  // the normalised width (K of the consuming GEMM)
+    float eps = 0.0f;
+};
 cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, int epi,
-                           void *out, uint32_t *err);
+                           void *out, uint32_t *err, const RowNorm &rn = RowNorm());
 // QKV projection with the epilogue of launch_qknorm_rope_kv fused in (no fp32 qkv buffer).
 // rope_t is the RoPE table by frequency: (cos, sin) of frequency i at position p at
 // rope_t[i * max_ctx + p].
 cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, const Rows &r,
                                const float *q_gain, const float *k_gain, const float2 *rope_t, bf16 *q_out,
                                bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv, int max_ctx, float eps,
-                               uint32_t *err);
+                               uint32_t *err, const float *ss_in = nullptr);
 
 // --- gemv.cu (decode; same contract as launch_gemm for small M) ---------------------------
 cudaError_t launch_gemv(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N,

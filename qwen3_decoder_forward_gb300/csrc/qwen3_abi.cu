@@ -32,7 +32,7 @@ struct Layout {
            kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0;
     size_t o_resid = 0, o_xn = 0, o_qkv = 0, o_q = 0, o_attn = 0, o_act = 0, o_rowslot = 0,
            o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0, o_pflags = 0, o_pres = 0,
-           o_resid2 = 0;
+           o_resid2 = 0, o_ssp = 0;
     size_t total = 0;
 };
 
@@ -111,6 +111,7 @@ Layout make_layout(const qwen3_config &c) {
     L.o_resid2 = take((size_t)c.max_seqs * C * 4);  // second residual buffer of the decode ping-pong
     L.o_pflags = take(PFLAG_WORDS * 4);  // persistent decode: arrival counters, argmax counter
     L.o_pres = take((size_t)3 * c.max_seqs * C * 4);  // persistent decode: three residual buffers
+    L.o_ssp = take(2 * R * (C / 128) * 4);  // prefill: per-128-column sums of squares of h, two norms
     L.total = off;
     return L;
 }
@@ -270,6 +271,49 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
                 return gemm_tc_supported(R, Kd, N) ? launch_gemm_tc(lc, X, R, Kd, W, N, epi, out, err)
                                                    : launch_gemm(lc, X, R, Kd, W, N, epi, out);
             };
+            // All four projections on the tensor cores: both RMSNorms ride in the GEMM epilogues.
+            // The residual-add GEMM before a norm leaves bf16(h * gamma) in xn and the sums of
+            // squares of h in ss_*; the GEMM after it scales its rows by rsqrt(mean + eps).
+            const bool tc_norm = gemm_tc_supported(R, C, qkv_n) && gemm_tc_supported(R, Hq * D, C) &&
+                                 gemm_tc_supported(R, C, 2 * I) && gemm_tc_supported(R, I, C) && C % 128 == 0;
+            float *ss_in = c->at<float>(L.o_ssp);
+            float *ss_post = ss_in + (size_t)std::max(k.max_prefill_tokens, k.max_seqs) * (C / 128);
+            if (tc_norm) {
+                // layer 0's operand comes normalised from the embedding kernel
+                Q3_TRY(launch_gemm_tc_qkv(lc, xn, R, C, w_qkv, qkv_n, rows, g_q, g_k, rope_t, q, c->kcache(l),
+                                          c->vcache(l), Hq, Hkv, k.max_ctx, k.rms_eps, err,
+                                          l > 0 ? ss_in : nullptr));
+                if (attn_prefill_tc_supported(Hq, Hkv))
+                    Q3_TRY(launch_attn_prefill_tc(lc, q, R, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots,
+                                                  rows.row_pos, rows.B, max_len, k.max_seqs, attn, Hq, Hkv,
+                                                  k.max_ctx, err));
+                else
+                    Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots,
+                                               rows.B, max_len, attn, Hq, Hkv, k.max_ctx));
+                RowNorm post;
+                post.ss_out = ss_post;
+                post.xn_out = xn;
+                post.gamma_out = g_post;
+                post.norm_c = C;
+                post.eps = k.rms_eps;
+                Q3_TRY(launch_gemm_tc(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, resid, err, post));
+                RowNorm mlp_in;
+                mlp_in.ss_in = ss_post;
+                mlp_in.norm_c = C;
+                mlp_in.eps = k.rms_eps;
+                Q3_TRY(launch_gemm_tc(lc, xn, R, C, w_gu, 2 * I, EPI_SWIGLU, act, err, mlp_in));
+                RowNorm next;  // the next layer's input norm (none after the last layer)
+                if (l + 1 < k.n_layers) {
+                    next.ss_out = ss_in;
+                    next.xn_out = xn;
+                    next.gamma_out = (const float *)(c->layer(l + 1) + L.o_gin);
+                    next.norm_c = C;
+                    next.eps = k.rms_eps;
+                }
+                Q3_TRY(launch_gemm_tc(lc, act, R, I, w_down, C, EPI_RESID_ADD, resid, err, next));
+                Q3_TRY(dump(l + 1, resid));
+                continue;
+            }
             if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
             if (gemm_tc_supported(R, C, qkv_n)) {  // QK-norm, RoPE and the KV write in the GEMM epilogue
                 Q3_TRY(launch_gemm_tc_qkv(lc, xn, R, C, w_qkv, qkv_n, rows, g_q, g_k, rope_t, q, c->kcache(l),
