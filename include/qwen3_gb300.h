@@ -202,6 +202,87 @@ int qwen3_kv_view(const qwen3_ctx *ctx, int32_t layer, int32_t slot, const void 
  * node of the graph). */
 int64_t qwen3_launch_count(const qwen3_ctx *ctx);
 
+/* Copies the context's configuration (as given to qwen3_create) to *cfg.  Errors: E_INVALID. */
+int qwen3_get_config(const qwen3_ctx *ctx, qwen3_config *cfg);
+
+/* Forgets the tokens KV slot `slot` holds: its length becomes 0 on the host and (in stream
+ * order on `stream`) on the device, so that the next qwen3_prefill_append or qwen3_prefill
+ * starts it at position 0 and decode steps reject it until then.  The cache rows keep their
+ * old values (finite, never attended to).  Errors: E_INVALID (bad slot), E_CUDA. */
+int qwen3_release_slot(qwen3_ctx *ctx, int32_t slot, void *stream);
+
+/* ---- Continuous batching ("第 3 章", the engine and its scheduler; "手写Qwen3-0.6B推理",
+ * generation that stops at the end-of-sequence token) -------------------------------------
+ * An engine runs requests (a prompt, a token limit, an end-of-sequence id) through one
+ * context.  Each qwen3_engine_step schedules at most token_budget tokens:
+ *   1. one token for every running request that has consumed its prompt (its last generated
+ *      token, appended at its slot's length);
+ *   2. the next chunk of every running request still in its prompt (chunked prefill);
+ *   3. waiting requests, first come first served, each into a free slot, while slots and
+ *      budget remain (a prompt longer than what is left is split over several steps).
+ * If every scheduled row is a single generated token the step is one qwen3_decode_step;
+ * otherwise it is one qwen3_prefill_append over all rows (prompt chunks and generated tokens
+ * packed together).  A request whose prompt is complete takes the greedy next token of its
+ * last row; it finishes on its eos_id (kept as its last token), after max_new_tokens
+ * tokens, or when its slot is full, and its slot is released for the waiting requests.
+ * The step synchronises `stream` once, to read the next tokens.
+ * The engine owns every slot of the context while it exists, and leaves the context's
+ * sampling setting off (a context with qwen3_set_sampling on makes the steps fail). */
+typedef struct qwen3_engine qwen3_engine;
+
+#define QWEN3_FINISH_NONE 0     /* waiting or running */
+#define QWEN3_FINISH_EOS 1      /* generated its eos_id */
+#define QWEN3_FINISH_LENGTH 2   /* generated max_new_tokens tokens */
+#define QWEN3_FINISH_CONTEXT 3  /* its slot holds max_ctx tokens: nothing more can be appended */
+
+typedef struct qwen3_engine_stats {
+    int64_t steps;             /* steps that ran the model */
+    int64_t mixed_steps;       /* of which prefill_append calls (prompt chunks, maybe generated tokens) */
+    int64_t decode_steps;      /* of which decode-only calls */
+    int64_t prompt_tokens;     /* prompt tokens run */
+    int64_t generated_tokens;  /* tokens generated */
+} qwen3_engine_stats;
+
+/* Device workspace of an engine (token, offset, slot and next-token arrays). */
+size_t qwen3_engine_workspace_bytes(const qwen3_ctx *ctx, int32_t token_budget);
+
+/* token_budget: tokens per step, max_seqs <= token_budget <= max_prefill_tokens.  workspace_dev:
+ * device memory of qwen3_engine_workspace_bytes bytes, 256-byte aligned, owned by the caller
+ * and kept while the engine lives.  Errors: E_INVALID. */
+int qwen3_engine_create(qwen3_ctx *ctx, int32_t token_budget, void *workspace_dev, size_t bytes,
+                        qwen3_engine **out);
+
+/* Queues a request.  prompt_host: host int32 [prompt_len] (copied), 1 <= prompt_len <= max_ctx;
+ * max_new_tokens >= 1; eos_id < 0 for none.  request_id must not be queued already.
+ * Errors: E_INVALID, E_CAPACITY (prompt longer than max_ctx). */
+int qwen3_engine_submit(qwen3_engine *e, int64_t request_id, const int32_t *prompt_host, int32_t prompt_len,
+                        int32_t max_new_tokens, int32_t eos_id);
+
+/* One scheduling step (see above); *n_finished (if not NULL) receives how many requests
+ * finished in it.  With nothing to run it returns QWEN3_OK at once.  Errors: those of the
+ * context's calls (the engine's state is then undefined: free it). */
+int qwen3_engine_step(qwen3_engine *e, void *stream, int32_t *n_finished);
+
+/* Requests submitted and not finished. */
+int32_t qwen3_engine_unfinished(const qwen3_engine *e);
+
+/* Tokens generated so far for request_id (up to capacity of them into tokens_host, which may
+ * be NULL when capacity is 0), their count and the finish reason (QWEN3_FINISH_*).
+ * Errors: E_INVALID (unknown id). */
+int qwen3_engine_result(const qwen3_engine *e, int64_t request_id, int32_t *tokens_host, int32_t capacity,
+                        int32_t *n_tokens, int32_t *finish_reason);
+
+/* Drops the record of a finished request.  Errors: E_INVALID (unknown or unfinished id). */
+int qwen3_engine_forget(qwen3_engine *e, int64_t request_id);
+
+int qwen3_engine_get_stats(const qwen3_engine *e, qwen3_engine_stats *out);
+
+/* Message of the engine's last failed call. */
+const char *qwen3_engine_last_error(const qwen3_engine *e);
+
+/* Frees the engine (not the workspace, not the context). */
+void qwen3_engine_free(qwen3_engine *e);
+
 /* ---- Single kernels, as the forward runs them (no context needed) ----------------------
  * These run one step of the forward on caller buffers, for per-kernel tests and timing.
  * All buffers are device memory; the calls are asynchronous on `stream`. */

@@ -35,6 +35,17 @@ class qwen3_sampling(ctypes.Structure):
     _fields_ = [("temperature", _P), ("top_k", _P), ("top_p", _P), ("uniform", _P)]
 
 
+class qwen3_engine_stats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int64), ("mixed_steps", ctypes.c_int64), ("decode_steps", ctypes.c_int64),
+                ("prompt_tokens", ctypes.c_int64), ("generated_tokens", ctypes.c_int64)]
+
+
+QWEN3_FINISH_NONE = 0
+QWEN3_FINISH_EOS = 1
+QWEN3_FINISH_LENGTH = 2
+QWEN3_FINISH_CONTEXT = 3
+
+
 class qwen3_config(ctypes.Structure):
     _fields_ = [
         ("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
@@ -85,6 +96,18 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_slot_length": (i32, [_P, i32]),
         "qwen3_kv_view": (ctypes.c_int, [_P, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
         "qwen3_launch_count": (i64, [_P]),
+        "qwen3_get_config": (ctypes.c_int, [_P, ctypes.POINTER(qwen3_config)]),
+        "qwen3_release_slot": (ctypes.c_int, [_P, i32, _P]),
+        "qwen3_engine_workspace_bytes": (sz, [_P, i32]),
+        "qwen3_engine_create": (ctypes.c_int, [_P, i32, _P, sz, ctypes.POINTER(_P)]),
+        "qwen3_engine_submit": (ctypes.c_int, [_P, i64, pi32, i32, i32, i32]),
+        "qwen3_engine_step": (ctypes.c_int, [_P, _P, pi32]),
+        "qwen3_engine_unfinished": (i32, [_P]),
+        "qwen3_engine_result": (ctypes.c_int, [_P, i64, pi32, i32, pi32, pi32]),
+        "qwen3_engine_forget": (ctypes.c_int, [_P, i64]),
+        "qwen3_engine_get_stats": (ctypes.c_int, [_P, ctypes.POINTER(qwen3_engine_stats)]),
+        "qwen3_engine_last_error": (ctypes.c_char_p, [_P]),
+        "qwen3_engine_free": (None, [_P]),
         "qwen3_free": (None, [_P]),
         "qwen3_op_gemv": (ctypes.c_int, [_P, i32, i32, _P, i32, i32, _P, _P]),
         "qwen3_op_gemm": (ctypes.c_int, [_P, i32, i32, _P, i32, i32, _P, _P]),
@@ -164,6 +187,72 @@ def qwen3_set_sampling(ctx, temperature_ptr: Optional[int], top_k_ptr: Optional[
         return
     sp = qwen3_sampling(temperature_ptr, top_k_ptr, top_p_ptr, uniform_ptr)
     _check(load_library().qwen3_set_sampling(ctx, ctypes.byref(sp)), ctx)
+
+
+def qwen3_get_config(ctx) -> qwen3_config:
+    cfg = qwen3_config()
+    _check(load_library().qwen3_get_config(ctx, ctypes.byref(cfg)), ctx)
+    return cfg
+
+
+def qwen3_release_slot(ctx, slot: int, stream: int = 0):
+    _check(load_library().qwen3_release_slot(ctx, slot, stream), ctx)
+
+
+def _engine_check(rc: int, eng) -> None:
+    if rc != QWEN3_OK:
+        msg = load_library().qwen3_engine_last_error(eng) if eng else b""
+        raise Qwen3Error(rc, msg.decode() if msg else "")
+
+
+def qwen3_engine_workspace_bytes(ctx, token_budget: int) -> int:
+    return int(load_library().qwen3_engine_workspace_bytes(ctx, token_budget))
+
+
+def qwen3_engine_create(ctx, token_budget: int, workspace_ptr: int, nbytes: int):
+    eng = _P()
+    _engine_check(load_library().qwen3_engine_create(ctx, token_budget, workspace_ptr, nbytes, ctypes.byref(eng)),
+                  None)
+    return eng
+
+
+def qwen3_engine_submit(eng, request_id: int, prompt: Sequence[int], max_new_tokens: int, eos_id: int = -1):
+    _engine_check(load_library().qwen3_engine_submit(eng, request_id, _i32_array(prompt), len(prompt),
+                                                     max_new_tokens, eos_id), eng)
+
+
+def qwen3_engine_step(eng, stream: int = 0) -> int:
+    n = ctypes.c_int32(0)
+    _engine_check(load_library().qwen3_engine_step(eng, stream, ctypes.byref(n)), eng)
+    return int(n.value)
+
+
+def qwen3_engine_unfinished(eng) -> int:
+    return int(load_library().qwen3_engine_unfinished(eng))
+
+
+def qwen3_engine_result(eng, request_id: int):
+    """(generated tokens, finish reason) of a request."""
+    lib = load_library()
+    n, why = ctypes.c_int32(0), ctypes.c_int32(0)
+    _engine_check(lib.qwen3_engine_result(eng, request_id, None, 0, ctypes.byref(n), ctypes.byref(why)), eng)
+    buf = (ctypes.c_int32 * max(1, n.value))()
+    _engine_check(lib.qwen3_engine_result(eng, request_id, buf, n.value, ctypes.byref(n), ctypes.byref(why)), eng)
+    return [int(buf[i]) for i in range(n.value)], int(why.value)
+
+
+def qwen3_engine_forget(eng, request_id: int):
+    _engine_check(load_library().qwen3_engine_forget(eng, request_id), eng)
+
+
+def qwen3_engine_get_stats(eng) -> Dict[str, int]:
+    st = qwen3_engine_stats()
+    _engine_check(load_library().qwen3_engine_get_stats(eng, ctypes.byref(st)), eng)
+    return {k: int(getattr(st, k)) for k, _ in qwen3_engine_stats._fields_}
+
+
+def qwen3_engine_free(eng):
+    load_library().qwen3_engine_free(eng)
 
 
 def qwen3_get_status(ctx) -> int:
@@ -361,3 +450,55 @@ class Model:
             t = whole[off: off + per].view(s.n_kv_heads, self.cfg.max_ctx, s.head_dim)
             out.append(t[:, :n].permute(1, 0, 2).contiguous())
         return out[0], out[1]
+
+
+class Engine:
+    """Continuous batching over a ``Model``'s context (qwen3_engine_*): the device workspace is
+    a PyTorch buffer kept here; the engine owns every KV slot of the model while it lives."""
+
+    def __init__(self, model: "Model", token_budget: int):
+        torch = model.torch
+        self.model = model
+        nbytes = qwen3_engine_workspace_bytes(model.ctx, token_budget)
+        if nbytes == 0:
+            raise Qwen3Error(QWEN3_E_INVALID, "engine: bad token budget")
+        self.ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=model.device)
+        ptr = (self.ws.data_ptr() + 255) // 256 * 256
+        self.eng = qwen3_engine_create(model.ctx, token_budget, ptr, nbytes)
+
+    def submit(self, request_id: int, prompt: Sequence[int], max_new_tokens: int, eos_id: int = -1):
+        qwen3_engine_submit(self.eng, request_id, [int(t) for t in prompt], max_new_tokens, eos_id)
+
+    def step(self) -> int:
+        return qwen3_engine_step(self.eng, self.model._stream())
+
+    def run(self, max_steps: int = 1 << 20) -> int:
+        """Steps until every submitted request has finished; returns the steps taken."""
+        n = 0
+        while self.unfinished() and n < max_steps:
+            self.step()
+            n += 1
+        return n
+
+    def unfinished(self) -> int:
+        return qwen3_engine_unfinished(self.eng)
+
+    def result(self, request_id: int):
+        return qwen3_engine_result(self.eng, request_id)
+
+    def forget(self, request_id: int):
+        qwen3_engine_forget(self.eng, request_id)
+
+    def stats(self) -> Dict[str, int]:
+        return qwen3_engine_get_stats(self.eng)
+
+    def close(self):
+        if getattr(self, "eng", None) is not None:
+            qwen3_engine_free(self.eng)
+            self.eng = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

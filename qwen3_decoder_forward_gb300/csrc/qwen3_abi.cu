@@ -749,6 +749,22 @@ int qwen3_kv_view(const qwen3_ctx *c, int32_t layer, int32_t slot, const void **
 
 int64_t qwen3_launch_count(const qwen3_ctx *c) { return c ? c->launches : 0; }
 
+int qwen3_get_config(const qwen3_ctx *c, qwen3_config *cfg) {
+    if (!c || !cfg) return QWEN3_E_INVALID;
+    *cfg = c->cfg;
+    return QWEN3_OK;
+}
+
+int qwen3_release_slot(qwen3_ctx *c, int32_t slot, void *stream) {
+    if (!c) return QWEN3_E_INVALID;
+    if (slot < 0 || slot >= c->cfg.max_seqs) return c->fail(QWEN3_E_INVALID, "qwen3_release_slot: slot out of range");
+    const cudaError_t e = cudaMemsetAsync(c->at<int32_t>(c->lay.o_ctxlen) + slot, 0, sizeof(int32_t),
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_release_slot");
+    c->len_host[slot] = 0;
+    return QWEN3_OK;
+}
+
 static bool gemv_k_ok(int K) {
     return K == 256 || K == 512 || K == 768 || K == 1024 || K == 1536 || K == 2048 || K == 2560 ||
            K == 3072 || K == 4096;

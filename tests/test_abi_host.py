@@ -94,3 +94,20 @@ def test_package_import_loads_no_cuda():
     mod = importlib.import_module("qwen3_decoder_forward_gb300")
     assert "libqwen3_gb300" not in str(sys.modules.get("qwen3_decoder_forward_gb300.binding", ""))
     assert mod is not None
+
+
+def test_engine_calls_reject_null_before_any_work(lib):
+    assert lib.qwen3_engine_workspace_bytes(None, 16) == 0
+    out = ctypes.c_void_p()
+    assert lib.qwen3_engine_create(None, 16, 256, 1 << 20, ctypes.byref(out)) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_engine_submit(None, 1, binding._i32_array([1, 2]), 2, 4, -1) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_engine_step(None, None, None) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_engine_unfinished(None) == 0
+    assert lib.qwen3_engine_result(None, 1, None, 0, None, None) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_engine_forget(None, 1) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_engine_get_stats(None, None) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_engine_last_error(None) == b""
+    lib.qwen3_engine_free(None)
+    cfg = binding.qwen3_config()
+    assert lib.qwen3_get_config(None, ctypes.byref(cfg)) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_release_slot(None, 0, None) == binding.QWEN3_E_INVALID
