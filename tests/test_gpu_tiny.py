@@ -90,15 +90,20 @@ def test_graph_replay_matches_direct_launches(setup):
 
 
 def test_persistent_matches_chain(setup):
-    """The persistent kernel and the kernel chain agree (same roundings; the fp32 sums are
-    taken in different orders, so logits within 1e-3 and tokens wherever the gap is clear)."""
+    """The persistent kernel and the kernel chain agree.  They round at the same points, but
+    their attention and MLP take the fp32 sums in different orders, so now and then a value
+    that is stored in bf16 (attention output, normed MLP input, SwiGLU activation) rounds to
+    the neighbouring bf16 number on one path.  Most steps then agree to ~1e-7; a step with
+    such a flip in a heavily weighted element differs by up to ~2.5e-3 (measured), while each
+    path stays 5-6e-3 from the oracle.  Hence logits within 5e-3 (half the parity gate) and
+    the same token wherever the gap is clear."""
     w, prompt, ref = setup
     a, la = run_gpu(w, prompt, ref["fed"], flags=binding.QWEN3_FLAG_PERSISTENT, dump=False)
     b, lb = run_gpu(w, prompt, ref["fed"], flags=0, dump=False)
     # one launch per persistent decode step, several per chained step
     assert la < lb
     for x, y in zip(a, b):
-        assert gc.rel_l2(x["logits"], y["logits"]) <= 1e-3
+        assert gc.rel_l2(x["logits"], y["logits"]) <= 5e-3
         top2 = np.sort(y["logits"])[-2:]
         if top2[1] - top2[0] > 1e-3:
             assert x["token"] == y["token"]
