@@ -33,14 +33,16 @@ METRIC = "decode tokens/s & prefill tokens/s on 1 GB300; % of HBM / bf16 tensor 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2 ** 20
 
-# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel, from the
-# capture summarised in profiles/ (None until taken for the current kernel).
-# DRAM bytes (read + write) per launch of the roofline kernels, medians of ncu captures of the
-# kernels as they stand (dram__bytes_read.sum + dram__bytes_write.sum): the decode gate_up GEMV
-# at one row reads exactly its 12.6 MB of weights; the prefill gate_up GEMM at 23,460 rows reads
-# A (48 MB) and W (12.6 MB) once and writes 86 MB of its 144 MB output before the kernel ends
-# (the rest leaves L2 later).
-TRAFFIC_BYTES = {"gemv_gate_up": 12609536, "gemm_gate_up": 146652416}
+# DRAM bytes (read + write) per launch of the roofline kernels: medians of ncu captures
+# (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel as it stands, None where no
+# capture of the current kernel exists.  The fused decode MLP at one row reads exactly its
+# 18.9 MB of weights (launches as timed here, without the next-layer L2 prefetch of the decode
+# chain); the decode gate_up GEMV at one row (k_gemv_bulk) reads exactly its 12.6 MB; the
+# prefill gate_up GEMM at 23,460 rows (launches of the prefill call, the same kernel) reads A
+# (48 MB) and W (12.6 MB) once and writes 86 MB of its 144 MB output before it ends (the rest
+# leaves L2 later).
+TRAFFIC_BYTES = {"gemv_bulk_gate_up": 12609536, "gemv_mma_gate_up": None, "gemm_gate_up": 147362304,
+                 "mlp_fused": 18910976}
 
 
 def parse_args():
@@ -251,10 +253,54 @@ def units_per_step(wl):
     return wl.n_prompt_tokens, "tokens/s"
 
 
+def measure_mlp_roofline(torch, binding, wl, peaks, peak_kind):
+    """Average duration of the fused decode MLP kernel (RMSNorm + gate_up + SwiGLU + down +
+    residual; 60% of a layer's weight bytes), the kernel decode steps of up to 4 sequences run
+    for the MLP, over launches cycling through 28 layers' weights (528 MB, larger than L2),
+    timed with CUDA events on the launching stream."""
+    s = wl.shape
+    dev = torch.device("cuda")
+    M, C, I = wl.n_seqs, s.hidden, s.intermediate
+    g = torch.Generator(device="cpu").manual_seed(5)
+    layers = [((torch.randn(2 * I, C, generator=g) * 0.02).to(torch.bfloat16).to(dev),
+               (torch.randn(I, C, generator=g) * 0.02).to(torch.bfloat16).to(dev)) for _ in range(s.n_layers)]
+    h = torch.randn(M, C, generator=g).to(dev)
+    gain = torch.ones(C, device=dev)
+    out = torch.zeros(M, C, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def launch(wgu, wdt):
+        binding.qwen3_op_mlp_decode(h.data_ptr(), M, C, gain.data_ptr(), s.rms_eps, wgu.data_ptr(), wdt.data_ptr(),
+                                    I, out.data_ptr(), stream)
+    for wgu, wdt in layers:
+        launch(wgu, wdt)
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(reps):
+        for wgu, wdt in layers:
+            launch(wgu, wdt)
+    e1.record()
+    torch.cuda.synchronize()
+    launches = reps * len(layers)
+    avg_s = e0.elapsed_time(e1) / 1e3 / launches
+    algo_bytes = 3 * I * C * 2 + M * C * 4 * 3  # weights; h read, out read and written
+    achieved = algo_bytes / avg_s / 1e9
+    peak = float(peaks["hbm_gbs"])
+    return {"kernel": "k_mlp_fused (decode MLP: RMSNorm + gate_up + SwiGLU + down + residual, bf16 weights "
+                      f"[{2 * I},{C}] + [{I},{C}], {M} row(s))",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": TRAFFIC_BYTES.get("mlp_fused"),
+            "algorithmic_bytes_per_launch": algo_bytes, "avg_launch_us": round(avg_s * 1e6, 3),
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+
+
 def measure_gemv_roofline(torch, binding, wl, peaks, peak_kind):
     """Average duration of the decode gate_up projection kernel, the largest decode kernel by
-    weight bytes (40% of the layer), over launches cycling through 28 weight matrices (352 MB,
-    larger than L2), timed with CUDA events on the launching stream."""
+    weight bytes (40% of the layer) at 9-32 rows, over launches cycling through 28 weight
+    matrices (352 MB, larger than L2), timed with CUDA events on the launching stream."""
     s = wl.shape
     dev = torch.device("cuda")
     M, K, N = wl.n_seqs, s.hidden, 2 * s.intermediate
@@ -280,9 +326,11 @@ def measure_gemv_roofline(torch, binding, wl, peaks, peak_kind):
     algo_bytes = N * K * 2 + M * K * 2 + M * (N // 2) * 2
     achieved = algo_bytes / avg_s / 1e9
     peak = float(peaks["hbm_gbs"])
-    return {"kernel": "k_gemv (decode gate_up projection + SwiGLU, bf16 weights [6144,1024])",
+    kname = "k_gemv_bulk" if M <= 8 else "k_gemv_mma"
+    return {"kernel": f"{kname} (decode gate_up projection + SwiGLU, bf16 weights [{N},{K}], {M} rows)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": TRAFFIC_BYTES["gemv_gate_up"],
+            "frac": round(achieved / peak, 4),
+            "traffic": TRAFFIC_BYTES["gemv_bulk_gate_up" if M <= 8 else "gemv_mma_gate_up"],
             "algorithmic_bytes_per_launch": algo_bytes, "avg_launch_us": round(avg_s * 1e6, 3),
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
             else "fallback 6.8 TB/s"}
@@ -508,8 +556,12 @@ def gpu_arm(args, wl):
     e2e_s_max, e2e_units = reduce_over_ranks(torch, world, e2e_s * 1e3, units * args.steps)
     e2e_value = e2e_units / (e2e_s_max / 1e3)
 
-    roofline = (measure_gemv_roofline(torch, binding, wl, peaks, peak_kind) if wl.decode_steps
-                else measure_gemm_roofline(torch, binding, wl, peaks, peak_kind))
+    if not wl.decode_steps:
+        roofline = measure_gemm_roofline(torch, binding, wl, peaks, peak_kind)
+    elif wl.n_seqs <= 4 and wl.shape.hidden == 1024:
+        roofline = measure_mlp_roofline(torch, binding, wl, peaks, peak_kind)
+    else:
+        roofline = measure_gemv_roofline(torch, binding, wl, peaks, peak_kind)
     assert runner.model.status() == 0, binding.qwen3_last_error(runner.model.ctx)
     runner.model.close()
     del runner

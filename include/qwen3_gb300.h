@@ -299,6 +299,19 @@ void qwen3_engine_free(qwen3_engine *e);
 int qwen3_op_gemv(const void *x_dev, int32_t M, int32_t K, const void *w_dev, int32_t N,
                   int32_t epilogue, void *out_dev, void *stream);
 
+/* The decode MLP of up to 4 rows in one kernel, as decode steps of up to 4 sequences run it
+ * ("手写Qwen3-0.6B推理", MLP and Qwen3DecoderLayer's residual add; "第 3 章", 3.2/3.4):
+ *   out[b] += h[b] + Wdown (silu(Wgate m[b]) * (Wup m[b])),  m[b] = RMSNorm(h[b]; gain),
+ * with m and the activation rounded to bf16.  h_dev fp32 [M, C]; gain_dev fp32 [C];
+ * w_gate_up_dev bf16 [2I, C] with the gate and up rows interleaved (gate_0, up_0, gate_1, ...);
+ * w_down_t_dev bf16 [I, C], the down weight transposed; out_dev fp32 [M, C], accumulated into
+ * (zero it for out = h + MLP(h)) with fp32 atomics in an unspecified order.  Supported:
+ * 1 <= M <= 4, C == 1024, I a multiple of 256 whose per-SM share fits shared memory.
+ * Errors: E_INVALID (NULL, bad size), E_UNSUPPORTED, E_CUDA. */
+int qwen3_op_mlp_decode(const float *h_dev, int32_t M, int32_t C, const float *gain_dev, float eps,
+                        const void *w_gate_up_dev, const void *w_down_t_dev, int32_t I, float *out_dev,
+                        void *stream);
+
 /* Prefill projection (tiled tensor-core GEMM), same operands and epilogues as qwen3_op_gemv;
  * N a multiple of 128, K a multiple of 32, any M >= 1.  Errors: E_INVALID, E_CUDA. */
 int qwen3_op_gemm(const void *x_dev, int32_t M, int32_t K, const void *w_dev, int32_t N,

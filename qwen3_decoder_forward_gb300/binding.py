@@ -111,6 +111,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_free": (None, [_P]),
         "qwen3_op_gemv": (ctypes.c_int, [_P, i32, i32, _P, i32, i32, _P, _P]),
         "qwen3_op_gemm": (ctypes.c_int, [_P, i32, i32, _P, i32, i32, _P, _P]),
+        "qwen3_op_mlp_decode": (ctypes.c_int, [_P, i32, i32, _P, ctypes.c_float, _P, _P, i32, _P, _P]),
         "qwen3_op_lmhead_workspace_bytes": (sz, [i32]),
         "qwen3_op_lmhead_argmax": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P, sz, _P]),
         "qwen3_op_lmhead_argmax_noalloc": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P]),
@@ -305,6 +306,14 @@ def qwen3_op_lmhead_argmax_noalloc(x_ptr: int, B: int, C: int, embed_ptr: int, V
     """lm_head + argmax with the library's fixed scratch instead of a caller workspace (B <= 32)."""
     _check(load_library().qwen3_op_lmhead_argmax_noalloc(x_ptr, B, C, embed_ptr, V, logits_ptr, next_ptr,
                                                          stream), None)
+
+
+def qwen3_op_mlp_decode(h_ptr: int, M: int, C: int, gain_ptr: int, eps: float, w_gate_up_ptr: int,
+                        w_down_t_ptr: int, I: int, out_ptr: int, stream: int = 0):
+    """out[M, C] += h + down(silu(gate m) * up m), m = RMSNorm(h) * gain: the fused decode MLP
+    (gate/up rows interleaved in w_gate_up [2I, C], down transposed in w_down_t [I, C])."""
+    _check(load_library().qwen3_op_mlp_decode(h_ptr, M, C, gain_ptr, eps, w_gate_up_ptr, w_down_t_ptr, I,
+                                              out_ptr, stream), None)
 
 
 QWEN3_SAMPLE_CANDIDATES = 1024

@@ -802,6 +802,27 @@ int qwen3_op_gemv(const void *x, int32_t M, int32_t K, const void *w, int32_t N,
     return QWEN3_OK;
 }
 
+int qwen3_op_mlp_decode(const float *h, int32_t M, int32_t C, const float *gain, float eps, const void *w_gu,
+                        const void *w_dt, int32_t I, float *out, void *stream) {
+    g_create_error.clear();
+    if (!h || !gain || !w_gu || !w_dt || !out || M < 1 || C < 1 || I < 1 || I % 256 || !(eps >= 0.0f)) {
+        g_create_error = "qwen3_op_mlp_decode: bad argument";
+        return QWEN3_E_INVALID;
+    }
+    const Launch lc = op_launch(stream);
+    if (!mlp_fused_supported(M, C, I, lc.num_sms)) {
+        g_create_error = "qwen3_op_mlp_decode: unsupported size (M <= 4, C == 1024)";
+        return QWEN3_E_UNSUPPORTED;
+    }
+    const cudaError_t e = launch_mlp_fused(lc, h, M, C, gain, eps, (const bf16 *)w_gu, (const bf16 *)w_dt, I, out,
+                                           nullptr, nullptr, nullptr);
+    if (e != cudaSuccess) {
+        g_create_error = std::string("qwen3_op_mlp_decode: ") + cudaGetErrorString(e);
+        return QWEN3_E_CUDA;
+    }
+    return QWEN3_OK;
+}
+
 int qwen3_op_gemm(const void *x, int32_t M, int32_t K, const void *w, int32_t N, int32_t epi,
                   void *out, void *stream) {
     g_create_error.clear();

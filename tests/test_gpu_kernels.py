@@ -87,3 +87,32 @@ def test_lmhead_argmax_vs_torch(B, V):
     top2 = torch.topk(ref, 2, dim=1).values
     clear = (top2[:, 0] - top2[:, 1]) > 1e-3
     assert torch.equal(tok.long()[clear], torch.argmax(ref, dim=1)[clear])
+
+
+@pytest.mark.parametrize("M", [1, 2, 4])
+def test_decode_mlp_vs_torch(M):
+    """The fused decode MLP against fp32: out = base + h + Wd(silu(Wg m) * Wu m), m = RMSNorm(h)
+    * gain, rounding m and the activation to bf16 where the kernel stores them."""
+    gc.ensure_library()
+    C, I, eps = 1024, 3072, 1e-6
+    g = torch.Generator(device="cpu").manual_seed(40 + M)
+    h = torch.randn((M, C), generator=g).cuda()
+    gain = (1 + 0.05 * torch.randn(C, generator=g)).cuda()
+    wg = _rand((I, C), 41 + M, 0.02)
+    wu = _rand((I, C), 42 + M, 0.02)
+    wd = _rand((C, I), 43 + M, 0.02)
+    w_gu = torch.stack([wg, wu], dim=1).reshape(2 * I, C).contiguous()  # gate_0, up_0, gate_1, ...
+    w_dt = wd.T.contiguous()
+    base = torch.randn((M, C), generator=g).cuda()
+    out = base.clone()
+    binding.qwen3_op_mlp_decode(h.data_ptr(), M, C, gain.data_ptr(), eps, w_gu.data_ptr(), w_dt.data_ptr(), I,
+                                out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    m = (h * torch.rsqrt((h * h).mean(dim=1, keepdim=True) + eps) * gain).to(torch.bfloat16).float()
+    act = (F.silu(m @ wg.float().T) * (m @ wu.float().T)).to(torch.bfloat16).float()
+    ref = base + h + act @ wd.float().T
+    assert gc.rel_l2((out - base - h).cpu().numpy(), (ref - base - h).cpu().numpy()) <= 4e-3
+    assert gc.rel_l2(out.cpu().numpy(), ref.cpu().numpy()) <= 1e-4
+    with pytest.raises(binding.Qwen3Error):
+        binding.qwen3_op_mlp_decode(h.data_ptr(), 5, C, gain.data_ptr(), eps, w_gu.data_ptr(), w_dt.data_ptr(), I,
+                                    out.data_ptr(), 0)
