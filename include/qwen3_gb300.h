@@ -75,6 +75,15 @@ typedef struct qwen3_config {
     int32_t max_ctx;             /* tokens per slot (prompt + generated) */
     int32_t max_prefill_tokens;  /* largest N of one qwen3_prefill call */
     uint32_t flags;              /* QWEN3_FLAG_* */
+    /* KV cache layout.  kv_block_tokens == 0: every slot owns max_ctx positions (max_seqs *
+     * max_ctx rows per layer).  kv_block_tokens > 0 (a multiple of 128): a paged cache ("第 3 章",
+     * the engine's KV-cache blocks) -- a pool of kv_pool_blocks blocks of kv_block_tokens
+     * positions shared by all slots; a slot takes blocks as its length grows (any block of the
+     * pool, in any order) and gives them back when it restarts or is released.  A call that
+     * needs more blocks than are free fails with E_CAPACITY before it launches anything.
+     * Paged needs n_q_heads == 2 * n_kv_heads and is not combined with QWEN3_FLAG_PERSISTENT. */
+    int32_t kv_block_tokens;
+    int32_t kv_pool_blocks;
 } qwen3_config;
 
 /* Weights: device pointers to bf16 tensors in the checkpoint's layout ([out, in] row-major
@@ -194,9 +203,19 @@ int32_t qwen3_slot_length(const qwen3_ctx *ctx, int32_t slot);
 
 /* Device pointers to layer `layer`, slot `slot` of the KV cache: K and V are each
  * bf16 [Hkv][max_ctx][D] (rows 0..length-1 valid; K after q/k-norm and RoPE, V raw).
- * Read-only for the caller.  Errors: E_INVALID. */
+ * Read-only for the caller.  Errors: E_INVALID, E_UNSUPPORTED (a paged cache: the slot's
+ * rows are not contiguous; use qwen3_kv_copy_rows). */
 int qwen3_kv_view(const qwen3_ctx *ctx, int32_t layer, int32_t slot, const void **k_dev,
                   const void **v_dev);
+
+/* Copies cached rows pos0 .. pos0+n-1 of (layer, slot) to k_out_dev and v_out_dev, each bf16
+ * [Hkv][n][D] (K after q/k-norm and RoPE, V raw), in stream order; works for both cache
+ * layouts.  Errors: E_INVALID (bad layer/slot, rows beyond the slot's length), E_CUDA. */
+int qwen3_kv_copy_rows(const qwen3_ctx *ctx, int32_t layer, int32_t slot, int32_t pos0, int32_t n,
+                       void *k_out_dev, void *v_out_dev, void *stream);
+
+/* Free blocks of a paged cache (-1 for a contiguous one). */
+int32_t qwen3_kv_free_blocks(const qwen3_ctx *ctx);
 
 /* Number of kernels this context has launched so far (graph replays count every kernel
  * node of the graph). */

@@ -53,6 +53,7 @@ class qwen3_config(ctypes.Structure):
         ("intermediate", ctypes.c_int32), ("vocab", ctypes.c_int32), ("rms_eps", ctypes.c_float),
         ("rope_theta", ctypes.c_double), ("max_seqs", ctypes.c_int32), ("max_ctx", ctypes.c_int32),
         ("max_prefill_tokens", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("kv_block_tokens", ctypes.c_int32), ("kv_pool_blocks", ctypes.c_int32),
     ]
 
 
@@ -97,6 +98,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_kv_view": (ctypes.c_int, [_P, i32, i32, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
         "qwen3_launch_count": (i64, [_P]),
         "qwen3_get_config": (ctypes.c_int, [_P, ctypes.POINTER(qwen3_config)]),
+        "qwen3_kv_copy_rows": (ctypes.c_int, [_P, i32, i32, i32, i32, _P, _P, _P]),
+        "qwen3_kv_free_blocks": (i32, [_P]),
         "qwen3_release_slot": (ctypes.c_int, [_P, i32, _P]),
         "qwen3_engine_workspace_bytes": (sz, [_P, i32]),
         "qwen3_engine_create": (ctypes.c_int, [_P, i32, _P, sz, ctypes.POINTER(_P)]),
@@ -135,10 +138,11 @@ def _i32_array(values: Sequence[int]):
     return (ctypes.c_int32 * len(values))(*[int(v) for v in values])
 
 
-def make_config(shape, max_seqs: int, max_ctx: int, max_prefill_tokens: int, flags: int = 0) -> qwen3_config:
+def make_config(shape, max_seqs: int, max_ctx: int, max_prefill_tokens: int, flags: int = 0,
+                kv_block_tokens: int = 0, kv_pool_blocks: int = 0) -> qwen3_config:
     return qwen3_config(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
                         shape.intermediate, shape.vocab, shape.rms_eps, shape.rope_theta, max_seqs, max_ctx,
-                        max_prefill_tokens, flags)
+                        max_prefill_tokens, flags, kv_block_tokens, kv_pool_blocks)
 
 
 # --- the C ABI, one wrapper per call ------------------------------------------------------
@@ -357,13 +361,13 @@ class Model:
     """
 
     def __init__(self, shape, weights: Dict, max_seqs: int, max_ctx: int, max_prefill_tokens: int,
-                 flags: int = 0, device: str = "cuda"):
+                 flags: int = 0, device: str = "cuda", kv_block_tokens: int = 0, kv_pool_blocks: int = 0):
         import torch
 
         self.torch = torch
         self.shape = shape
         self.device = torch.device(device)
-        self.cfg = make_config(shape, max_seqs, max_ctx, max_prefill_tokens, flags)
+        self.cfg = make_config(shape, max_seqs, max_ctx, max_prefill_tokens, flags, kv_block_tokens, kv_pool_blocks)
         nbytes = qwen3_arena_bytes(self.cfg)
         if nbytes == 0:
             raise Qwen3Error(QWEN3_E_UNSUPPORTED, "configuration not supported")
@@ -446,6 +450,22 @@ class Model:
 
     def status(self) -> int:
         return qwen3_get_status(self.ctx)
+
+    def kv_copy(self, layer: int, slot: int, pos0: int, n: int):
+        """K and V rows pos0 .. pos0+n-1 of (layer, slot) as new bf16 tensors [n, Hkv, D], for
+        either cache layout (qwen3_kv_copy_rows)."""
+        torch = self.torch
+        s = self.shape
+        k = torch.empty(s.n_kv_heads, n, s.head_dim, dtype=torch.bfloat16, device=self.device)
+        v = torch.empty_like(k)
+        rc = load_library().qwen3_kv_copy_rows(self.ctx, layer, slot, pos0, n, k.data_ptr(), v.data_ptr(),
+                                               self._stream())
+        if rc != QWEN3_OK:
+            raise Qwen3Error(rc, "qwen3_kv_copy_rows")
+        return k.permute(1, 0, 2).contiguous(), v.permute(1, 0, 2).contiguous()
+
+    def kv_free_blocks(self) -> int:
+        return int(load_library().qwen3_kv_free_blocks(self.ctx))
 
     def kv_rows(self, layer: int, slot: int, n: int):
         """Copies K and V rows 0..n-1 of (layer, slot) to new tensors [n, Hkv, D] (bf16, device)."""

@@ -86,16 +86,23 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
     const int k_end = pos_ok ? min(pos + 1, k_begin + per) : k_begin;
     const int cache_end = max(k_begin, min(k_end, pos));  // cached keys [k_begin, cache_end)
     const int n_chunks = (cache_end - k_begin + CHUNK - 1) / CHUNK;
-    const size_t head_base = ((size_t)slot * Hkv + g) * max_ctx * D;
-
     auto issue = [&](int c) {  // chunk c of this split into stage c % STAGES
         const int st = c % STAGES;
         const int j0 = k_begin + c * CHUNK;
         const int n = min(CHUNK, cache_end - j0);
-        const uint32_t bytes = (uint32_t)n * D * 2;
-        mbar_expect_tx(&full[st], 2 * bytes);
-        bulk_g2s(ring + st * STAGE_BYTES, k_layer + head_base + (size_t)j0 * D, bytes, &full[st]);
-        bulk_g2s(ring + st * STAGE_BYTES + CHUNK * D * 2, v_layer + head_base + (size_t)j0 * D, bytes, &full[st]);
+        mbar_expect_tx(&full[st], 2 * (uint32_t)n * D * 2);
+        // keys j0 .. j0+n-1 as runs of consecutive cache rows: one run, or two where a paged
+        // cache's block ends inside the chunk (blocks hold at least CHUNK keys)
+        for (int done = 0; done < n;) {
+            const int p = j0 + done;
+            const int run = r.kv.table ? min(n - done, r.kv.bs - p % r.kv.bs) : n - done;
+            const size_t row = kv_row(r.kv, slot, Hkv, g, max_ctx, p);
+            const uint32_t bytes = (uint32_t)run * D * 2;
+            bulk_g2s(ring + st * STAGE_BYTES + (size_t)done * D * 2, k_layer + row * D, bytes, &full[st]);
+            bulk_g2s(ring + st * STAGE_BYTES + CHUNK * D * 2 + (size_t)done * D * 2, v_layer + row * D, bytes,
+                     &full[st]);
+            done += run;
+        }
     };
     if (threadIdx.x == 0) {
         for (int st = 0; st < STAGES; ++st) mbar_init(&full[st], 1);
@@ -169,8 +176,9 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
                 a[e] = pack_bf16x2(x[G][2 * e], x[G][2 * e + 1]);
                 c[e] = pack_bf16x2(x[G + 1][2 * e], x[G + 1][2 * e + 1]);
             }
-            uint4 *kd = reinterpret_cast<uint4 *>(k_layer + head_base + (size_t)pos * D + sub * 16);
-            uint4 *vd = reinterpret_cast<uint4 *>(v_layer + head_base + (size_t)pos * D + sub * 16);
+            const size_t row = kv_row(r.kv, slot, Hkv, g, max_ctx, pos);
+            uint4 *kd = reinterpret_cast<uint4 *>(k_layer + row * D + sub * 16);
+            uint4 *vd = reinterpret_cast<uint4 *>(v_layer + row * D + sub * 16);
             kd[0] = pk[0]; kd[1] = pk[1];
             vd[0] = pv[0]; vd[1] = pv[1];
         }

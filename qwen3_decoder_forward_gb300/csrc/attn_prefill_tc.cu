@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
     const __grid_constant__ CUtensorMap tmV, const int32_t *__restrict__ cu, const int32_t *__restrict__ slots,
     const int32_t *__restrict__ row_pos, bf16 *__restrict__ out, int Hq, int Hkv, int max_ctx, float scale_log2,
-    uint32_t *err) {
+    uint32_t *err, KvMap kv) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_s = smem;                    // [2] tiles
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
     const int q0 = qt * BQ;
     if (q0 >= len) return;  // uniform: no barrier or TMEM touched yet
     const int h0 = g * 2;    // the pair of query heads of KV head g (Hq == 2 Hkv)
-    const int kv_row0 = (slots[b] * Hkv + g) * max_ctx;  // first cache row of this (slot, head)
+    const int slot = slots[b];  // cache rows of key tile j: kv_row(kv, slot, Hkv, g, max_ctx, j * BK) + 0..127
     // The sequence's rows are positions off .. off+len-1 of its slot (off > 0 when the call
     // continues a slot that already holds off tokens): query off+i sees keys 0 .. off+i, the
     // bottom-right alignment of the causal mask.
@@ -204,13 +204,15 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int st = j & 1;  // K tile j into ring stage j % 2, once tile j - 2 has been used
                 if (j >= 2 && !mbar_wait_bounded(&bars->kempty[st], ((j - 2) >> 1) & 1, err)) { ok = false; break; }
+                // a paged cache keeps whole 128-key tiles inside one block (block size % 128 == 0)
+                const int row_j = (int)kv_row(kv, slot, Hkv, g, max_ctx, j * BK);
                 mbar_expect_tx(&bars->kfull[st], TILE_BYTES);
-                tma2d(k_s + st * TILE_BYTES, &tmK, 0, kv_row0 + j * BK, &bars->kfull[st]);
-                tma2d(k_s + st * TILE_BYTES + HALF_BYTES, &tmK, 64, kv_row0 + j * BK, &bars->kfull[st]);
+                tma2d(k_s + st * TILE_BYTES, &tmK, 0, row_j, &bars->kfull[st]);
+                tma2d(k_s + st * TILE_BYTES + HALF_BYTES, &tmK, 64, row_j, &bars->kfull[st]);
                 if (j > 0 && !mbar_wait_bounded(&bars->vempty, (j - 1) & 1, err)) { ok = false; break; }
                 mbar_expect_tx(&bars->vfull, TILE_BYTES);
-                tma2d(v_s, &tmV, 0, kv_row0 + j * BK, &bars->vfull);
-                tma2d(v_s + HALF_BYTES, &tmV, 64, kv_row0 + j * BK, &bars->vfull);
+                tma2d(v_s, &tmV, 0, row_j, &bars->vfull);
+                tma2d(v_s + HALF_BYTES, &tmV, 64, row_j, &bars->vfull);
             }
         }
     } else if (warp == MMA_WARP) {
@@ -449,9 +451,10 @@ bool attn_prefill_tc_supported(int Hq, int Hkv) { return Hq == 2 * Hkv && encode
 cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const bf16 *k_layer,
                                    const bf16 *v_layer, const int32_t *cu_seqlens, const int32_t *slots,
                                    const int32_t *row_pos, int B, int max_len, int max_seqs, bf16 *out, int Hq,
-                                   int Hkv, int max_ctx, uint32_t *err) {
+                                   int Hkv, int max_ctx, uint32_t *err, const KvMap &kv, size_t kv_rows_paged) {
     CUtensorMap mq, mk, mv;
-    const uint64_t kv_rows = (uint64_t)max_seqs * Hkv * max_ctx;
+    if (kv.table && (kv.bs % BK || kv_rows_paged == 0)) return cudaErrorInvalidValue;
+    const uint64_t kv_rows = kv.table ? (uint64_t)kv_rows_paged : (uint64_t)max_seqs * Hkv * max_ctx;
     if (!map2d(&mq, q, (uint64_t)N, (uint64_t)Hq * D) || !map2d(&mk, k_layer, kv_rows, D) ||
         !map2d(&mv, v_layer, kv_rows, D))
         return cudaErrorInvalidValue;
@@ -459,7 +462,7 @@ cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const
     if (e != cudaSuccess) return e;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
     return launch(lc, k_attn_prefill_tc, dim3((max_len + BQ - 1) / BQ, Hkv, B), dim3(THREADS), SMEM_BYTES, mq, mk, mv,
-                  cu_seqlens, slots, row_pos, out, Hq, Hkv, max_ctx, scale_log2, err);
+                  cu_seqlens, slots, row_pos, out, Hq, Hkv, max_ctx, scale_log2, err, kv);
 }
 
 }  // namespace q3

@@ -101,6 +101,7 @@ struct EpiArgs {
     const float2 *rope_t;  // (cos, sin) by frequency: rope_t[i * max_ctx + pos], i < 64
     bf16 *q_out, *k_layer, *v_layer;
     int Hq, Hkv, max_ctx;
+    KvMap kv;  // where the cache row of (slot, head, pos) lives
     float eps;
     // RMSNorm folded into the GEMMs around it (RowNorm in kernels.h): scale rows by
     // rsqrt(sum(ss_in[row][*]) / norm_c + eps) (QKV, SwiGLU), or, with xn_out (residual add),
@@ -356,7 +357,9 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                         dst = ea.q_out + ((size_t)row * ea.Hq + head) * 128;
                     else {
                         const int g = is_v ? head - ea.Hq - ea.Hkv : head - ea.Hq;
-                        dst = (is_v ? ea.v_layer : ea.k_layer) + (((size_t)slot * ea.Hkv + g) * ea.max_ctx + pos) * 128;
+                        // (pos is checked against max_ctx before the store; keep the table index in range)
+                        dst = (is_v ? ea.v_layer : ea.k_layer) +
+                              kv_row(ea.kv, slot, ea.Hkv, g, ea.max_ctx, pos < ea.max_ctx ? pos : 0) * 128;
                     }
                     // pass 2: elements i (chunk c) and i+64 (chunk c+2) rotate together
 #pragma unroll 1
@@ -492,6 +495,7 @@ cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, co
     ea.Hq = Hq;
     ea.Hkv = Hkv;
     ea.max_ctx = max_ctx;
+    ea.kv = r.kv;
     ea.eps = eps;
     ea.ss_in = ss_in;
     ea.norm_c = K;

@@ -52,6 +52,25 @@ cudaError_t launch(const Launch &lc, void (*kern)(KArgs...), dim3 grid, dim3 blo
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// Where the cached K (or V) row of (slot, KV head g, position p) lives, in rows of D elements
+// from the layer's base.  Contiguous (table == nullptr): [slot][Hkv][max_ctx][D].  Paged:
+// blocks of bs positions, [block][Hkv][bs][D], the block of position p of a slot being
+// table[slot * max_blocks + p / bs]; the host fills the table for every position a call can
+// touch before launching it.
+struct KvMap {
+    const int32_t *table = nullptr;
+    int32_t max_blocks = 0;
+    int32_t bs = 0;
+};
+
+// The table is read through L2 (ld.global.cg): kernels may read it before their dependency
+// wait, when this SM's L1 could still hold an older copy of the line.
+__device__ __forceinline__ size_t kv_row(const KvMap &m, int slot, int Hkv, int g, int max_ctx, int p) {
+    if (!m.table) return ((size_t)slot * Hkv + g) * max_ctx + p;
+    const int blk = __ldcg(m.table + (size_t)slot * m.max_blocks + p / m.bs);
+    return ((size_t)blk * Hkv + g) * m.bs + p % m.bs;
+}
+
 // Row bookkeeping of one call: row r of the packed batch belongs to KV slot row_slot[r]
 // at absolute position row_pos[r].
 struct Rows {
@@ -63,6 +82,7 @@ struct Rows {
     bool append = false;                  // prefill rows continue their slot: positions start at ctx_len
     int32_t B = 0;
     int32_t rows = 0;
+    KvMap kv;                             // where the cache rows of the slots live
 };
 
 // --- norm.cu ---------------------------------------------------------------------------
@@ -159,10 +179,12 @@ cudaError_t launch_attn_prefill(const Launch &lc, const bf16 *q, const bf16 *k_l
 bool attn_prefill_tc_supported(int Hq, int Hkv);
 // Rows of sequence b are positions row_pos[cu[b]] .. of its slot (non-zero when a call
 // continues a slot); keys come from the cache, causal mask aligned bottom-right.
+// kv_rows: rows of the layer's K (and V) array (tensor-map extent); a paged kv needs bs % 128 == 0.
 cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const bf16 *k_layer,
                                    const bf16 *v_layer, const int32_t *cu_seqlens, const int32_t *slots,
                                    const int32_t *row_pos, int B, int max_len, int max_seqs, bf16 *out, int Hq,
-                                   int Hkv, int max_ctx, uint32_t *err);
+                                   int Hkv, int max_ctx, uint32_t *err, const KvMap &kv = KvMap(),
+                                   size_t kv_rows = 0);
 
 // --- attn_decode.cu ----------------------------------------------------------------------
 // Most key ranges per (sequence, KV head) of the decode attention.

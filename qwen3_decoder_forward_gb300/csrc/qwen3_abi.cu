@@ -29,7 +29,8 @@ struct Layout {
     size_t layer_bytes = 0, o_wqkv = 0, o_wo = 0, o_wog = 0, o_wgu = 0, o_wdown = 0, o_wdownT = 0, o_gin = 0,
            o_gpost = 0, o_gq = 0, o_gk = 0;
     size_t o_layers = 0, o_embed = 0, o_gfinal = 0, o_rope = 0, o_rope_t = 0, o_kcache = 0, o_vcache = 0,
-           kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0;
+           kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0, o_kvtable = 0;
+    int32_t kv_max_blocks = 0;  // paged cache: table entries per slot
     size_t o_resid = 0, o_xn = 0, o_qkv = 0, o_q = 0, o_attn = 0, o_act = 0, o_rowslot = 0,
            o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0, o_pflags = 0, o_pres = 0,
            o_resid2 = 0, o_ssp = 0;
@@ -57,6 +58,16 @@ bool config_supported(const qwen3_config &c, std::string *why) {
         (2 * c.intermediate) % 128)
         return fail("config: projection widths must be multiples of 128");
     if (c.max_seqs > 1024) return fail("config: max_seqs must be at most 1024");
+    if (c.kv_block_tokens < 0 || (c.kv_block_tokens > 0 && (c.kv_block_tokens % 128 || c.kv_pool_blocks < 1)))
+        return fail("config: kv_block_tokens must be 0 or a multiple of 128, with kv_pool_blocks >= 1");
+    if (c.kv_block_tokens > 0) {
+        if (c.n_q_heads != 2 * c.n_kv_heads) return fail("config: a paged KV cache needs n_q_heads == 2 * n_kv_heads");
+        if (((c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim) % 256 || c.hidden % 64)
+            return fail("config: a paged KV cache needs the tensor-core QKV projection shape");
+        if (c.flags & QWEN3_FLAG_PERSISTENT) return fail("config: a paged KV cache does not run the persistent decode kernel");
+        if ((size_t)c.kv_pool_blocks * c.n_kv_heads * c.kv_block_tokens > (size_t)INT32_MAX)
+            return fail("config: kv_pool_blocks too large");
+    }
     return true;
 }
 
@@ -88,7 +99,13 @@ Layout make_layout(const qwen3_config &c) {
     L.o_gfinal = take(C * 4);
     L.o_rope = take((size_t)c.max_ctx * (D / 2) * 8);
     L.o_rope_t = take((size_t)c.max_ctx * (D / 2) * 8);  // the same table, frequency-major
-    L.kv_layer_bytes = (size_t)c.max_seqs * Hkv * c.max_ctx * D * 2;
+    if (c.kv_block_tokens > 0) {  // paged: a pool of blocks [block][Hkv][bs][D] and a block table
+        L.kv_layer_bytes = (size_t)c.kv_pool_blocks * Hkv * c.kv_block_tokens * D * 2;
+        L.kv_max_blocks = (c.max_ctx + c.kv_block_tokens - 1) / c.kv_block_tokens;
+        L.o_kvtable = take((size_t)c.max_seqs * L.kv_max_blocks * 4);
+    } else {
+        L.kv_layer_bytes = (size_t)c.max_seqs * Hkv * c.max_ctx * D * 2;
+    }
     L.o_kcache = take(L.kv_layer_bytes * c.n_layers);
     L.o_vcache = take(L.kv_layer_bytes * c.n_layers);
     L.o_ctxlen = take((size_t)c.max_seqs * 4);
@@ -146,6 +163,9 @@ struct qwen3_ctx {
     int64_t launches = 0;
     qwen3_sampling sampling = {};  // all NULL: greedy next tokens
     std::string err;
+    // paged KV cache: host copy of the block table [max_seqs][max_blocks], blocks held per
+    // slot, and the free blocks (a stack)
+    std::vector<int32_t> kv_table, kv_nblk, kv_free;
 
     template <typename T>
     T *at(size_t off) const { return reinterpret_cast<T *>(arena + off); }
@@ -286,9 +306,10 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
                 if (attn_prefill_tc_supported(Hq, Hkv))
                     Q3_TRY(launch_attn_prefill_tc(lc, q, R, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots,
                                                   rows.row_pos, rows.B, max_len, k.max_seqs, attn, Hq, Hkv,
-                                                  k.max_ctx, err));
+                                                  k.max_ctx, err, rows.kv, L.kv_layer_bytes / (D * 2)));
                 else
-                    Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots,
+                    Q3_TRY(rows.kv.table ? cudaErrorNotSupported :  // the mma.sync kernel reads a contiguous cache
+                           launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots,
                                                rows.B, max_len, attn, Hq, Hkv, k.max_ctx));
                 RowNorm post;
                 post.ss_out = ss_post;
@@ -320,15 +341,17 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
                                           c->vcache(l), Hq, Hkv, k.max_ctx, k.rms_eps, err));
             } else {
                 Q3_TRY(gemm(xn, C, w_qkv, qkv_n, EPI_F32, qkv));
-                Q3_TRY(launch_qknorm_rope_kv(lc, qkv, rows, g_q, g_k, rope, q, c->kcache(l), c->vcache(l), Hq,
+                Q3_TRY(rows.kv.table ? cudaErrorNotSupported :  // writes a contiguous cache
+                       launch_qknorm_rope_kv(lc, qkv, rows, g_q, g_k, rope, q, c->kcache(l), c->vcache(l), Hq,
                                              Hkv, k.max_ctx, k.rms_eps, err));
             }
             if (attn_prefill_tc_supported(Hq, Hkv))
                 Q3_TRY(launch_attn_prefill_tc(lc, q, R, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots,
                                               rows.row_pos, rows.B, max_len, k.max_seqs, attn, Hq, Hkv, k.max_ctx,
-                                              err));
+                                              err, rows.kv, L.kv_layer_bytes / (D * 2)));
             else
-                Q3_TRY(launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots, rows.B,
+                Q3_TRY(rows.kv.table ? cudaErrorNotSupported :
+                       launch_attn_prefill(lc, q, c->kcache(l), c->vcache(l), rows.cu_seqlens, rows.slots, rows.B,
                                            max_len, attn, Hq, Hkv, k.max_ctx));
             Q3_TRY(gemm(attn, Hq * D, w_o, C, EPI_RESID_ADD, resid));
             Q3_TRY(launch_rmsnorm(lc, resid, R, g_post, xn, C, k.rms_eps));
@@ -354,7 +377,59 @@ Rows make_rows(qwen3_ctx *c, const int32_t *cu, const int32_t *slots, int B, int
     r.ctx_len = c->at<int32_t>(c->lay.o_ctxlen);
     r.B = B;
     r.rows = rows;
+    if (c->cfg.kv_block_tokens > 0) {
+        r.kv.table = c->at<int32_t>(c->lay.o_kvtable);
+        r.kv.max_blocks = c->lay.kv_max_blocks;
+        r.kv.bs = c->cfg.kv_block_tokens;
+    }
     return r;
+}
+
+bool kv_paged(const qwen3_ctx *c) { return c->cfg.kv_block_tokens > 0; }
+
+// Gives back every block of `slot` (paged cache; host bookkeeping only).
+void kv_release(qwen3_ctx *c, int slot) {
+    const int mb = c->lay.kv_max_blocks;
+    for (int i = c->kv_nblk[slot] - 1; i >= 0; --i) c->kv_free.push_back(c->kv_table[(size_t)slot * mb + i]);
+    c->kv_nblk[slot] = 0;
+}
+
+// Makes each slots[b] hold blocks for positions 0 .. new_len[b]-1 (restart: its old blocks
+// are given back first), then copies the changed table rows to the device in stream order.
+// Nothing changes when the free blocks do not suffice.
+int kv_reserve(qwen3_ctx *c, const int32_t *slots, const int *new_len, int B, bool restart, cudaStream_t st) {
+    if (!kv_paged(c)) return QWEN3_OK;
+    const int bs = c->cfg.kv_block_tokens, mb = c->lay.kv_max_blocks;
+    long need = 0, avail = (long)c->kv_free.size();
+    for (int b = 0; b < B; ++b) {
+        const int have = c->kv_nblk[slots[b]];
+        const int want = (new_len[b] + bs - 1) / bs;
+        if (restart) {
+            avail += have;
+            need += want;
+        } else {
+            need += std::max(0, want - have);
+        }
+    }
+    if (need > avail) return c->fail(QWEN3_E_CAPACITY, "paged KV cache: not enough free blocks");
+    for (int b = 0; b < B; ++b) {
+        const int slot = slots[b];
+        if (restart) kv_release(c, slot);
+        const int have = c->kv_nblk[slot];
+        const int want = (new_len[b] + bs - 1) / bs;
+        if (want <= have) continue;
+        for (int i = have; i < want; ++i) {
+            c->kv_table[(size_t)slot * mb + i] = c->kv_free.back();
+            c->kv_free.pop_back();
+        }
+        c->kv_nblk[slot] = want;
+        // pageable source: the copy is staged before the call returns
+        const cudaError_t e = cudaMemcpyAsync(c->at<int32_t>(c->lay.o_kvtable) + (size_t)slot * mb + have,
+                                              c->kv_table.data() + (size_t)slot * mb + have,
+                                              (size_t)(want - have) * 4, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return c->cuda_fail(e, "paged KV cache: block table upload");
+    }
+    return QWEN3_OK;
 }
 
 int check_slots(qwen3_ctx *c, const int32_t *slots_host, int B) {
@@ -413,6 +488,11 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
     c->lay = lay;
     c->arena = static_cast<uint8_t *>(arena_dev);
     c->len_host.assign(cfg->max_seqs, 0);
+    if (cfg->kv_block_tokens > 0) {
+        c->kv_table.assign((size_t)cfg->max_seqs * lay.kv_max_blocks, 0);
+        c->kv_nblk.assign(cfg->max_seqs, 0);
+        for (int i = 0; i < cfg->kv_pool_blocks; ++i) c->kv_free.push_back(i);  // the highest block goes first
+    }
     c->num_sms = prop.multiProcessorCount;
     c->n_parts = std::min(lmhead_parts(c->num_sms), MAX_PARTS);
     c->attn_ctas_per_sm = attn_decode_ctas_per_sm(cfg->n_q_heads, cfg->n_kv_heads);
@@ -477,6 +557,8 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_kcache, 0, lay.kv_layer_bytes * cfg->n_layers, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_vcache, 0, lay.kv_layer_bytes * cfg->n_layers, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_ctxlen, 0, (size_t)cfg->max_seqs * 4, st));
+        if (cfg->kv_block_tokens > 0)  // unused entries name block 0: never read for a position a slot lacks
+            Q3_TRY(cudaMemsetAsync(c->arena + lay.o_kvtable, 0, (size_t)cfg->max_seqs * lay.kv_max_blocks * 4, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_err, 0, 16, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_counters, 0, (size_t)cfg->max_seqs * cfg->n_kv_heads * 4, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_pflags, 0, PFLAG_WORDS * 4, st));
@@ -528,6 +610,12 @@ int prefill_impl(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *cu_dev,
     lc.pdl = !(c->cfg.flags & QWEN3_FLAG_NO_PDL);
     lc.num_sms = c->num_sms;
     lc.counter = &c->launches;
+    if (kv_paged(c)) {
+        std::vector<int> new_len(B);
+        for (int b = 0; b < B; ++b)
+            new_len[b] = (append ? c->len_host[slots_host[b]] : 0) + cu_host[b + 1] - cu_host[b];
+        if (int rc = kv_reserve(c, slots_host, new_len.data(), B, !append, lc.stream)) return rc;
+    }
     Rows rows = make_rows(c, cu_dev, slots_dev, B, N);
     rows.append = append;
     cudaError_t e = run_forward(c, lc, tokens_dev, rows, false, max_len, 0, logits_dev, next_tok_dev);
@@ -586,6 +674,11 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
     const int n_split = std::max(1, std::min({slots / pairs, MAX_SPLIT, (bucket + 63) / 64}));
 
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);
+    if (kv_paged(c)) {  // a block for the appended position where a slot's last block is full
+        std::vector<int> new_len(B);
+        for (int b = 0; b < B; ++b) new_len[b] = c->len_host[slots_host[b]] + 1;
+        if (int rc = kv_reserve(c, slots_host, new_len.data(), B, false, st)) return rc;
+    }
     const qwen3_config &k = c->cfg;
     if ((k.flags & QWEN3_FLAG_PERSISTENT) && c->num_sms <= MAX_PARTS && k.n_kv_heads <= PFLAG_WORDS - 8 &&
         decode_persistent_supported(k.hidden, k.n_q_heads, k.n_kv_heads, k.head_dim, k.intermediate, B, c->num_sms)) {
@@ -741,6 +834,7 @@ int qwen3_kv_view(const qwen3_ctx *c, int32_t layer, int32_t slot, const void **
     if (!c || !k_dev || !v_dev) return QWEN3_E_INVALID;
     if (layer < 0 || layer >= c->cfg.n_layers || slot < 0 || slot >= c->cfg.max_seqs)
         return QWEN3_E_INVALID;
+    if (kv_paged(c)) return QWEN3_E_UNSUPPORTED;
     const size_t per_slot = (size_t)c->cfg.n_kv_heads * c->cfg.max_ctx * c->cfg.head_dim;
     *k_dev = c->kcache(layer) + (size_t)slot * per_slot;
     *v_dev = c->vcache(layer) + (size_t)slot * per_slot;
@@ -762,7 +856,40 @@ int qwen3_release_slot(qwen3_ctx *c, int32_t slot, void *stream) {
                                           static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_release_slot");
     c->len_host[slot] = 0;
+    if (kv_paged(c)) kv_release(c, slot);
     return QWEN3_OK;
+}
+
+int qwen3_kv_copy_rows(const qwen3_ctx *c, int32_t layer, int32_t slot, int32_t pos0, int32_t n, void *k_out,
+                       void *v_out, void *stream) {
+    if (!c || !k_out || !v_out) return QWEN3_E_INVALID;
+    if (layer < 0 || layer >= c->cfg.n_layers || slot < 0 || slot >= c->cfg.max_seqs || pos0 < 0 || n < 1 ||
+        pos0 + n > c->len_host[slot])
+        return QWEN3_E_INVALID;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int Hkv = c->cfg.n_kv_heads, D = c->cfg.head_dim, mb = c->lay.kv_max_blocks;
+    const int bs = kv_paged(c) ? c->cfg.kv_block_tokens : c->cfg.max_ctx;
+    for (int g = 0; g < Hkv; ++g)
+        for (int p = pos0; p < pos0 + n;) {  // runs of rows inside one block (one run when contiguous)
+            const int run = std::min(pos0 + n - p, bs - p % bs);
+            const size_t row = kv_paged(c)
+                                   ? ((size_t)c->kv_table[(size_t)slot * mb + p / bs] * Hkv + g) * bs + p % bs
+                                   : ((size_t)slot * Hkv + g) * c->cfg.max_ctx + p;
+            const size_t dst = ((size_t)g * n + (p - pos0)) * D;
+            for (int kv = 0; kv < 2; ++kv) {
+                const bf16 *src = (kv ? c->vcache(layer) : c->kcache(layer)) + row * D;
+                bf16 *out = static_cast<bf16 *>(kv ? v_out : k_out) + dst;
+                const cudaError_t e = cudaMemcpyAsync(out, src, (size_t)run * D * 2, cudaMemcpyDeviceToDevice, st);
+                if (e != cudaSuccess) return QWEN3_E_CUDA;
+            }
+            p += run;
+        }
+    return QWEN3_OK;
+}
+
+int32_t qwen3_kv_free_blocks(const qwen3_ctx *c) {
+    if (!c || !kv_paged(c)) return -1;
+    return (int32_t)c->kv_free.size();
 }
 
 static bool gemv_k_ok(int K) {

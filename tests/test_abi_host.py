@@ -111,3 +111,24 @@ def test_engine_calls_reject_null_before_any_work(lib):
     cfg = binding.qwen3_config()
     assert lib.qwen3_get_config(None, ctypes.byref(cfg)) == binding.QWEN3_E_INVALID
     assert lib.qwen3_release_slot(None, 0, None) == binding.QWEN3_E_INVALID
+
+
+def test_paged_kv_config_sizes_and_rejections(lib):
+    s = synth.QWEN3_0P6B
+    flat = binding.qwen3_arena_bytes(binding.make_config(s, 16, 16384, 4096))
+    paged = binding.qwen3_arena_bytes(binding.make_config(s, 16, 16384, 4096, kv_block_tokens=256,
+                                                          kv_pool_blocks=64))
+    kv_flat = 28 * 2 * 16 * 8 * 16384 * 128 * 2
+    kv_paged = 28 * 2 * 64 * 8 * 256 * 128 * 2
+    assert 0 < paged < flat
+    assert abs((flat - paged) - (kv_flat - kv_paged)) < 2 ** 20  # the pool replaces the per-slot rows
+    for bt, pool, flags, heads in ((100, 8, 0, 8), (64, 8, 0, 8), (128, 0, 0, 8), (-128, 8, 0, 8),
+                                   (128, 8, binding.QWEN3_FLAG_PERSISTENT, 8), (128, 8, 0, 4)):
+        cfg = binding.make_config(s, 4, 512, 512, flags, bt, pool)
+        cfg.n_kv_heads = heads
+        assert binding.qwen3_arena_bytes(cfg) == 0, (bt, pool, flags, heads)
+
+
+def test_paged_kv_calls_reject_null(lib):
+    assert lib.qwen3_kv_copy_rows(None, 0, 0, 0, 1, 16, 16, None) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_kv_free_blocks(None) == -1
