@@ -52,7 +52,7 @@ constexpr int STAGE_BYTES = CHUNK * D * 2 * 2;  // K and V rows of one chunk
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16(x)); }
 
-template <int G>
+template <int G, bool PAGED>
 __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
     const float *__restrict__ qkv, Rows r, const float *__restrict__ q_gain,
     const float *__restrict__ k_gain, const float2 *__restrict__ rope, bf16 *__restrict__ k_layer,
@@ -86,6 +86,8 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
     const int k_end = pos_ok ? min(pos + 1, k_begin + per) : k_begin;
     const int cache_end = max(k_begin, min(k_end, pos));  // cached keys [k_begin, cache_end)
     const int n_chunks = (cache_end - k_begin + CHUNK - 1) / CHUNK;
+    KvMap kv = r.kv;
+    if (!PAGED) kv.table = nullptr;  // the contiguous form compiles to plain slot-major offsets
     auto issue = [&](int c) {  // chunk c of this split into stage c % STAGES
         const int st = c % STAGES;
         const int j0 = k_begin + c * CHUNK;
@@ -95,8 +97,8 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
         // cache's block ends inside the chunk (blocks hold at least CHUNK keys)
         for (int done = 0; done < n;) {
             const int p = j0 + done;
-            const int run = r.kv.table ? min(n - done, r.kv.bs - p % r.kv.bs) : n - done;
-            const size_t row = kv_row(r.kv, slot, Hkv, g, max_ctx, p);
+            const int run = PAGED ? min(n - done, kv.bs - p % kv.bs) : n - done;
+            const size_t row = kv_row(kv, slot, Hkv, g, max_ctx, p);
             const uint32_t bytes = (uint32_t)run * D * 2;
             bulk_g2s(ring + st * STAGE_BYTES + (size_t)done * D * 2, k_layer + row * D, bytes, &full[st]);
             bulk_g2s(ring + st * STAGE_BYTES + CHUNK * D * 2 + (size_t)done * D * 2, v_layer + row * D, bytes,
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
                 a[e] = pack_bf16x2(x[G][2 * e], x[G][2 * e + 1]);
                 c[e] = pack_bf16x2(x[G + 1][2 * e], x[G + 1][2 * e + 1]);
             }
-            const size_t row = kv_row(r.kv, slot, Hkv, g, max_ctx, pos);
+            const size_t row = kv_row(kv, slot, Hkv, g, max_ctx, pos);
             uint4 *kd = reinterpret_cast<uint4 *>(k_layer + row * D + sub * 16);
             uint4 *vd = reinterpret_cast<uint4 *>(v_layer + row * D + sub * 16);
             kd[0] = pk[0]; kd[1] = pk[1];
@@ -386,20 +388,19 @@ cudaError_t run_fused(const Launch &lc, const float *qkv, const Rows &r, const f
                   "merge scratch fits in the ring");
     if (n_split < 1 || n_split > ATTN_DECODE_MAX_SPLIT) return cudaErrorInvalidValue;
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-    cudaError_t e = cudaFuncSetAttribute(k_attn_decode_fused<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    auto kern = r.kv.table ? k_attn_decode_fused<G, true> : k_attn_decode_fused<G, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    return launch(lc, k_attn_decode_fused<G>, dim3(n_split, Hkv, r.B), dim3(NW * 32), SMEM_BYTES, qkv, r, q_gain,
-                  k_gain, rope, k_layer, v_layer, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps,
-                  scale_log2, err);
+    return launch(lc, kern, dim3(n_split, Hkv, r.B), dim3(NW * 32), SMEM_BYTES, qkv, r, q_gain, k_gain, rope,
+                  k_layer, v_layer, ws_ml, ws_o, counters, out, Hq, Hkv, max_ctx, eps, scale_log2, err);
 }
 
 template <int G>
 int ctas_per_sm() {
     int n = 0;
-    if (cudaFuncSetAttribute(k_attn_decode_fused<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_attn_decode_fused<G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn_decode_fused<G>, NW * 32, SMEM_BYTES) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_attn_decode_fused<G, false>, NW * 32, SMEM_BYTES) !=
             cudaSuccess)
         return 1;
     return n < 1 ? 1 : n;
