@@ -128,7 +128,8 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
  * NULL, the fp32 logits of those rows to logits_dev[B, V].  cu_seqlens and slots are given
  * twice, on the device and on the host (same values).  Errors: E_INVALID (NULL, B < 1,
  * cu_seqlens not starting at 0 or not increasing, repeated or out-of-range slot),
- * E_CAPACITY (B > max_seqs, N > max_prefill_tokens, len_b > max_ctx), E_CUDA. */
+ * E_CAPACITY (B > max_seqs, N > max_prefill_tokens, len_b > max_ctx, a paged cache without
+ * the free blocks the call needs), E_CUDA. */
 int qwen3_prefill(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *cu_seqlens_dev,
                   const int32_t *cu_seqlens_host, const int32_t *slots_dev,
                   const int32_t *slots_host, int32_t B, float *logits_dev,
@@ -157,7 +158,8 @@ int qwen3_prefill_append(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_
  * unless QWEN3_FLAG_NO_GRAPH is set, the step's kernel chain is recorded once per (B,
  * pointers, split plan) as a CUDA graph and replayed.  Errors: E_INVALID (NULL, B < 1,
  * repeated slot, slot never prefilled), E_CAPACITY (B > max_seqs, a slot already holding
- * max_ctx tokens), E_CUDA. */
+ * max_ctx tokens, a paged cache without a free block for a slot whose last block is full),
+ * E_CUDA. */
 int qwen3_decode_step(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_t *slots_dev,
                       const int32_t *slots_host, int32_t B, float *logits_dev,
                       int32_t *next_tok_dev, void *stream);
