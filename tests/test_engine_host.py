@@ -35,8 +35,10 @@ def lib(tmp_path_factory):
     if not gxx or not os.path.isdir(CUDA_INCLUDE):
         pytest.skip("needs g++ and the CUDA headers")
     out = str(tmp_path_factory.mktemp("engine_mock") / "libengine_mock.so")
-    cmd = [gxx, "-std=c++17", "-O1", "-shared", "-fPIC", "-I", os.path.join(ROOT, "include"), "-I", CUDA_INCLUDE,
-           "-x", "c++", ENGINE_SRC, "-x", "c++", MOCK_SRC, "-o", out]
+    # -Bsymbolic: the engine's calls resolve to the stand-ins in this library even when the
+    # process has loaded the real CUDA runtime or the real library (other tests do)
+    cmd = [gxx, "-std=c++17", "-O1", "-shared", "-fPIC", "-Wl,-Bsymbolic", "-I", os.path.join(ROOT, "include"),
+           "-I", CUDA_INCLUDE, "-x", "c++", ENGINE_SRC, "-x", "c++", MOCK_SRC, "-o", out]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
     lib = ctypes.CDLL(out)
