@@ -132,3 +132,33 @@ def test_paged_kv_config_sizes_and_rejections(lib):
 def test_paged_kv_calls_reject_null(lib):
     assert lib.qwen3_kv_copy_rows(None, 0, 0, 0, 1, 16, 16, None) == binding.QWEN3_E_INVALID
     assert lib.qwen3_kv_free_blocks(None) == -1
+
+
+def test_header_is_c99_and_matches_the_binding_structs(tmp_path):
+    """The header compiles as plain C99 (-pedantic, no warnings), and every field of the
+    structures the binding mirrors sits at the same offset, with the same size, in both."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if not gcc:
+        pytest.skip("needs gcc")
+    structs = {"qwen3_config": binding.qwen3_config, "qwen3_sampling": binding.qwen3_sampling,
+               "qwen3_engine_stats": binding.qwen3_engine_stats}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "qwen3_gb300.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'    printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'    printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    want = []
+    for name, cls in structs.items():
+        want.append(f"{name} size {ctypes.sizeof(cls)}")
+        want += [f"{name} {field} {getattr(cls, field).offset}" for field, _ in cls._fields_]
+    assert [l for l in got if l] == want
