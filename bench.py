@@ -136,10 +136,13 @@ class ClockSampler:
 
 
 def clocks_rejected(c) -> bool:
+    """A measurement is taken again when the GPU throttled for heat or a hardware slowdown, or
+    when its SM clock sat well below the maximum under load with no reason given (a clock lock
+    left by someone else); a power-cap limit alone is kept (and reported)."""
     bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
     if bad & set(c["reasons"]):
         return True
-    if c["sm_mhz"] and c["sm_max_mhz"] and c["sm_mhz"] < 0.5 * c["sm_max_mhz"] and not c["reasons"]:
+    if c["sm_mhz"] and c["sm_max_mhz"] and c["sm_mhz"] < 0.85 * c["sm_max_mhz"] and not c["reasons"]:
         return True
     return False
 
