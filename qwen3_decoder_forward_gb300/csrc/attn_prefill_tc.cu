@@ -38,7 +38,7 @@ namespace q3 {
 namespace {
 
 constexpr int D = 128, BQ = 128, BK = 128, THREADS = 576;
-constexpr int SM_WARPS = 16, TMA_WARP = 16, MMA_WARP = 17;
+constexpr int TMA_WARP = 16, MMA_WARP = 17;  // warps 0-15 run the softmax
 constexpr int TILE_BYTES = 128 * D * 2;  // a [128][128] bf16 tile as two 64-column halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int SMEM_BYTES = TILE_BYTES * 5 + 6144 + 1024;  // Q0, Q1, K ring (2), V, barriers

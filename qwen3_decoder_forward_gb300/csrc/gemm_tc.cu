@@ -24,12 +24,11 @@ namespace q3 {
 
 namespace {
 
-constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4, TC_THREADS = 128;
+constexpr int TC_BM = 128, TC_BN = 256, TC_BK = 64, TC_STAGES = 4;
 constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;                  // 16 KB
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;                  // 32 KB
 constexpr int TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;        // 48 KB
 constexpr int TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 256 + 1024;  // ring + barriers + alignment
-constexpr uint32_t TC_TMEM_COLS = 256;
 
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with the 128-byte
 // swizzle: rows of 128 bytes (64 elements), 8-row groups 1024 bytes apart.
