@@ -1,17 +1,23 @@
 #!/usr/bin/env python3
 """Throughput benchmark of the Qwen3-0.6B-shaped decoder forward on GB300.
 
-One step = one pass of the whole forward over a synthetic request batch: the packed prefill
-of every prompt (embedding, 28 decoder layers, last-row lm_head + argmax) followed by the
-workload's greedy decode steps, each step's token fed back on the device.  Default workload
-"decode_b1": one sequence, a 128-token prompt and 128 greedy decode steps.
+Default workload "decode_long": 16 sequences whose 16,384-token prompts fill the KV cache
+(about 30 GB), then 32 greedy decode steps of all 16 at once.  One timed step is those 32
+decode steps, each step's tokens fed back on the device; before each step the slots are
+rewound to their prompts (qwen3_truncate_slot), so every step decodes at the same contexts
+16,384..16,415 and rewrites the same cache rows.  The prompts' prefill (the KV fill) is timed
+once and reported beside it.  The same line carries the ragged prefill workload
+("prefill_ragged": 8 prompts of 512..4096 tokens packed into one call), timed on its own, as
+its "prefill" object.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-Under torchrun (N > 1) every rank runs an independent replica of the workload on its own GPU
-(no collective on the data path); rank 0 prints one JSON line with the sum of tokens over the
-ranks divided by the slowest rank's time.  ``--impl reference`` times the CPU oracle instead
-(rank 0 only), on a bounded sample of the same workload.
+A prefill-only workload (prefill_ragged, or --workload tiny / decode_* with --decode-steps 0)
+times one packed prefill call per step.  Under torchrun (N > 1) every rank runs an
+independent replica of the workload on its own GPU (no collective on the data path); rank 0
+prints one JSON line with the units of all ranks over the slowest rank's time.
+``--impl reference`` times the CPU oracle instead (rank 0 only), on a bounded sample of the
+same workload.
 """
 
 from __future__ import annotations
@@ -33,16 +39,15 @@ METRIC = "decode tokens/s & prefill tokens/s on 1 GB300; % of HBM / bf16 tensor 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 2 ** 20
 
-# DRAM bytes (read + write) per launch of the roofline kernels: medians of ncu captures
-# (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel as it stands, None where no
+# DRAM bytes (read + write) per launch of the roofline kernels, from ncu captures
+# (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel as it stands; None where no
 # capture of the current kernel exists.  The fused decode MLP at one row reads exactly its
-# 18.9 MB of weights (launches as timed here, without the next-layer L2 prefetch of the decode
-# chain); the decode gate_up GEMV at one row (k_gemv_bulk) reads exactly its 12.6 MB; the
-# prefill gate_up GEMM at 23,460 rows (launches of the prefill call, the same kernel) reads A
-# (48 MB) and W (12.6 MB) once and writes 86 MB of its 144 MB output before it ends (the rest
-# leaves L2 later).
-TRAFFIC_BYTES = {"gemv_bulk_gate_up": 12609536, "gemv_mma_gate_up": None, "gemm_gate_up": 147362304,
-                 "mlp_fused": 18910976}
+# 18.9 MB of weights; the prefill gate_up GEMM at 23,460 rows reads A (48 MB) and W (12.6 MB)
+# once and writes 86 MB of its 144 MB output before it ends (the rest leaves L2 later).
+# "attn_decode_per_key_row": bytes per (sequence, position) row of one layer's K and V that a
+# decode attention launch reads, measured on a smaller case and scaled by the rows a launch
+# reads (the traffic grows in proportion).
+TRAFFIC_BYTES = {"gemm_gate_up": 147362304, "mlp_fused": 18910976, "attn_decode_per_key_row": None}
 
 
 def parse_args():
@@ -50,7 +55,9 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
-    p.add_argument("--workload", default="decode_b1")
+    p.add_argument("--workload", default="decode_long")
+    p.add_argument("--prefill-workload", default="prefill_ragged",
+                   help="workload of the line's 'prefill' object when the main workload decodes ('none': skip)")
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--launch", default="graph", choices=["graph", "graph-nopdl", "direct", "persistent"],
@@ -59,6 +66,10 @@ def parse_args():
                         "persistent kernel")
     p.add_argument("--decode-steps", type=int, default=None,
                    help="override the workload's decode steps (shorter runs for profilers)")
+    p.add_argument("--roofline-only", action="store_true",
+                   help="run only the roofline kernel's timing of the workload (for ncu captures)")
+    p.add_argument("--roofline-ctx", type=int, default=None,
+                   help="context of the decode attention roofline launch (default: the workload's)")
     return p.parse_args()
 
 
@@ -148,7 +159,7 @@ def clocks_rejected(c) -> bool:
 
 
 # --------------------------------------------------------------------------------------
-# the workload
+# the workload and its algorithmic work
 # --------------------------------------------------------------------------------------
 
 def workload_desc(wl):
@@ -172,206 +183,15 @@ def chunk_prefills(lengths, max_tokens):
     return groups
 
 
-class GpuRunner:
-    """Holds the model and the device buffers of one replica and runs steps of the workload."""
-
-    def __init__(self, wl, device, flags=0):
-        import torch
-        from qwen3_decoder_forward_gb300 import binding, synth
-
-        self.torch, self.binding, self.wl, self.device = torch, binding, wl, device
-        s = wl.shape
-        self.max_prefill = min(max(wl.lengths) if wl.n_seqs == 1 else 32768, wl.n_prompt_tokens)
-        self.max_prefill = max(self.max_prefill, max(wl.lengths))
-        w = synth.make_weights(s)
-        self.model = binding.Model(s, w, max_seqs=wl.n_seqs, max_ctx=wl.max_ctx,
-                                   max_prefill_tokens=self.max_prefill, flags=flags, device=str(device))
-        del w
-        prompts = wl.prompts()
-        self.groups = chunk_prefills(wl.lengths, self.max_prefill)
-        self.group_tokens = [torch.cat([prompts[i] for i in g]).to(device) for g in self.groups]
-        self.group_tokens_host = [torch.cat([prompts[i] for i in g]).pin_memory() for g in self.groups]
-        self.B = wl.n_seqs
-        self.slots = list(range(self.B))
-        self.slots_d = torch.tensor(self.slots, dtype=torch.int32, device=device)
-        self.first = torch.zeros(self.B, dtype=torch.int32, device=device)
-        self.bufs = [torch.zeros(self.B, dtype=torch.int32, device=device) for _ in range(2)]
-        self.gen = torch.zeros(max(wl.decode_steps, 1), self.B, dtype=torch.int32, device=device)
-        self.gen_host = torch.zeros(max(wl.decode_steps, 1), self.B, dtype=torch.int32).pin_memory()
-        self.stream = torch.cuda.current_stream(device)
-
-    def prefill_all(self, host_inputs=False):
-        torch = self.torch
-        h2d = 0
-        for g, toks, toks_h in zip(self.groups, self.group_tokens, self.group_tokens_host):
-            if host_inputs:
-                toks = torch.empty_like(toks_h, device=self.device)
-                toks.copy_(toks_h, non_blocking=True)
-                h2d += toks_h.numel() * 4
-            lengths = [self.wl.lengths[i] for i in g]
-            nxt, _ = self.model.prefill(toks, lengths, [self.slots[i] for i in g])
-            h2d += (len(g) + 1) * 4 + len(g) * 4  # cu_seqlens and slots
-            self.first[g[0]: g[-1] + 1].copy_(nxt)
-        return h2d
-
-    def decode_all(self, record=False):
-        if self.wl.decode_steps == 0:
-            return
-        self.bufs[0].copy_(self.first)
-        for i in range(self.wl.decode_steps):
-            src, dst = self.bufs[i % 2], self.bufs[(i + 1) % 2]
-            self.model.decode_step(src, self.slots_d, self.slots, dst)
-            if record:
-                self.gen[i].copy_(dst)
-
-    def step(self, ev=None):
-        if ev is not None:
-            ev[0].record(self.stream)
-        self.prefill_all()
-        if ev is not None:
-            ev[1].record(self.stream)
-        self.decode_all()
-        if ev is not None:
-            ev[2].record(self.stream)
-
-    def step_e2e(self):
-        """The same step from host memory: prompts copied in, generated tokens read back."""
-        h2d = self.prefill_all(host_inputs=True)
-        self.decode_all(record=True)
-        d2h = 0
-        if self.wl.decode_steps:
-            self.gen_host.copy_(self.gen, non_blocking=True)
-            d2h = self.gen.numel() * 4
-        else:
-            self.gen_host[0].copy_(self.first, non_blocking=True)
-            d2h = self.B * 4
-        self.stream.synchronize()
-        return h2d, d2h
-
-
-def units_per_step(wl):
-    """(units, unit name): generated tokens for decode workloads, prompt tokens for prefill-only."""
-    if wl.decode_steps:
-        return wl.n_seqs * wl.decode_steps, "tokens/s"
-    return wl.n_prompt_tokens, "tokens/s"
-
-
-def measure_mlp_roofline(torch, binding, wl, peaks, peak_kind):
-    """Average duration of the fused decode MLP kernel (RMSNorm + gate_up + SwiGLU + down +
-    residual; 60% of a layer's weight bytes), the kernel decode steps of up to 4 sequences run
-    for the MLP, over launches cycling through 28 layers' weights (528 MB, larger than L2),
-    timed with CUDA events on the launching stream."""
+def decode_step_bytes(wl):
+    """Algorithmic HBM bytes of one decode step of the workload: all linear weights, the tied
+    head, every sequence's cached K/V rows (read) and the new rows (written)."""
     s = wl.shape
-    dev = torch.device("cuda")
-    M, C, I = wl.n_seqs, s.hidden, s.intermediate
-    g = torch.Generator(device="cpu").manual_seed(5)
-    layers = [((torch.randn(2 * I, C, generator=g) * 0.02).to(torch.bfloat16).to(dev),
-               (torch.randn(I, C, generator=g) * 0.02).to(torch.bfloat16).to(dev)) for _ in range(s.n_layers)]
-    h = torch.randn(M, C, generator=g).to(dev)
-    gain = torch.ones(C, device=dev)
-    out = torch.zeros(M, C, device=dev)
-    stream = torch.cuda.current_stream().cuda_stream
-
-    def launch(wgu, wdt):
-        binding.qwen3_op_mlp_decode(h.data_ptr(), M, C, gain.data_ptr(), s.rms_eps, wgu.data_ptr(), wdt.data_ptr(),
-                                    I, out.data_ptr(), stream)
-    for wgu, wdt in layers:
-        launch(wgu, wdt)
-    reps = 20
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(reps):
-        for wgu, wdt in layers:
-            launch(wgu, wdt)
-    e1.record()
-    torch.cuda.synchronize()
-    launches = reps * len(layers)
-    avg_s = e0.elapsed_time(e1) / 1e3 / launches
-    algo_bytes = 3 * I * C * 2 + M * C * 4 * 3  # weights; h read, out read and written
-    achieved = algo_bytes / avg_s / 1e9
-    peak = float(peaks["hbm_gbs"])
-    return {"kernel": "k_mlp_fused (decode MLP: RMSNorm + gate_up + SwiGLU + down + residual, bf16 weights "
-                      f"[{2 * I},{C}] + [{I},{C}], {M} row(s))",
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": TRAFFIC_BYTES.get("mlp_fused"),
-            "algorithmic_bytes_per_launch": algo_bytes, "avg_launch_us": round(avg_s * 1e6, 3),
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6.8 TB/s"}
-
-
-def measure_gemv_roofline(torch, binding, wl, peaks, peak_kind):
-    """Average duration of the decode gate_up projection kernel, the largest decode kernel by
-    weight bytes (40% of the layer) at 9-32 rows, over launches cycling through 28 weight
-    matrices (352 MB, larger than L2), timed with CUDA events on the launching stream."""
-    s = wl.shape
-    dev = torch.device("cuda")
-    M, K, N = wl.n_seqs, s.hidden, 2 * s.intermediate
-    g = torch.Generator(device="cpu").manual_seed(5)
-    ws = [(torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).to(dev) for _ in range(s.n_layers)]
-    x = (torch.randn(M, K, generator=g)).to(torch.bfloat16).to(dev)
-    out = torch.empty(M, N // 2, dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream().cuda_stream
-    for wt in ws:
-        binding.qwen3_op_gemv(x.data_ptr(), M, K, wt.data_ptr(), N, binding.QWEN3_EPI_SWIGLU, out.data_ptr(), stream)
-    reps = 20
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(reps):
-        for wt in ws:
-            binding.qwen3_op_gemv(x.data_ptr(), M, K, wt.data_ptr(), N, binding.QWEN3_EPI_SWIGLU, out.data_ptr(),
-                                  stream)
-    e1.record()
-    torch.cuda.synchronize()
-    launches = reps * len(ws)
-    avg_s = e0.elapsed_time(e1) / 1e3 / launches
-    algo_bytes = N * K * 2 + M * K * 2 + M * (N // 2) * 2
-    achieved = algo_bytes / avg_s / 1e9
-    peak = float(peaks["hbm_gbs"])
-    kname = "k_gemv_bulk" if M <= 8 else "k_gemv_mma"
-    return {"kernel": f"{kname} (decode gate_up projection + SwiGLU, bf16 weights [{N},{K}], {M} rows)",
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "traffic": TRAFFIC_BYTES["gemv_bulk_gate_up" if M <= 8 else "gemv_mma_gate_up"],
-            "algorithmic_bytes_per_launch": algo_bytes, "avg_launch_us": round(avg_s * 1e6, 3),
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6.8 TB/s"}
-
-
-def measure_gemm_roofline(torch, binding, wl, peaks, peak_kind):
-    """Average duration of the prefill gate_up projection GEMM (tcgen05, SwiGLU epilogue), the
-    largest prefill GEMM, at the workload's packed token count N, timed with CUDA events on the
-    launching stream.  At N = 23,460 the activations and the output (48 MB + 144 MB) exceed L2;
-    the 12.6 MB of weights may stay in it."""
-    s = wl.shape
-    dev = torch.device("cuda")
-    M, K, N = wl.n_prompt_tokens, s.hidden, 2 * s.intermediate
-    g = torch.Generator(device="cpu").manual_seed(6)
-    x = (torch.randn(M, K, generator=g)).to(torch.bfloat16).to(dev)
-    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).to(dev)
-    out = torch.empty(M, N // 2, dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream().cuda_stream
-    for _ in range(3):
-        binding.qwen3_op_gemm(x.data_ptr(), M, K, w.data_ptr(), N, binding.QWEN3_EPI_SWIGLU, out.data_ptr(), stream)
-    reps = 10
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record()
-    for _ in range(reps):
-        binding.qwen3_op_gemm(x.data_ptr(), M, K, w.data_ptr(), N, binding.QWEN3_EPI_SWIGLU, out.data_ptr(), stream)
-    e1.record()
-    torch.cuda.synchronize()
-    avg_s = e0.elapsed_time(e1) / 1e3 / reps
-    flops = 2 * M * N * K
-    achieved = flops / avg_s / 1e12
-    peak = float(peaks["bf16_tflops"])
-    return {"kernel": f"k_gemm_tcp (prefill gate_up GEMM + SwiGLU, tcgen05, [{M},{K}] x [{N},{K}]^T)",
-            "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "traffic": TRAFFIC_BYTES["gemm_gate_up"],
-            "algorithmic_flops_per_launch": flops, "avg_launch_us": round(avg_s * 1e6, 3),
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, burst: kernel timed alone)"
-            if peak_kind == "measured" else "fallback 1.9 PFLOP/s"}
+    lin = s.n_layers * ((s.q_dim + 2 * s.kv_dim) * s.hidden + s.hidden * s.q_dim + 3 * s.intermediate * s.hidden) * 2
+    head = s.vocab * s.hidden * 2
+    kv_tok = s.n_layers * 2 * s.kv_dim * 2
+    mean_ctx = sum(n + 1 + (wl.decode_steps - 1) / 2 for n in wl.lengths) / wl.n_seqs
+    return lin + head + wl.n_seqs * (mean_ctx + 1) * kv_tok
 
 
 def prefill_flops(wl):
@@ -386,14 +206,307 @@ def prefill_flops(wl):
     return lin + attn + head
 
 
+def decode_positions(wl):
+    """Position of each sequence's query in the middle decode step of the workload."""
+    return [n + wl.decode_steps // 2 for n in wl.lengths]
+
+
 # --------------------------------------------------------------------------------------
-# CPU oracle timing (reference arm and the cpu_baseline object)
+# GPU runner
 # --------------------------------------------------------------------------------------
 
-def oracle_sample(wl, n_samples=1, decode_sample=8, warmup=0):
-    """Times the CPU oracle on the first sequence: its prefill and `decode_sample` greedy steps,
-    extrapolated to the workload's request (prefill + decode_steps) per sequence."""
-    import numpy as np  # noqa: F401
+class GpuRunner:
+    """Holds the model and the device buffers of one replica and runs steps of the workload."""
+
+    def __init__(self, wl, device, flags=0, weights=None):
+        import torch
+        from qwen3_decoder_forward_gb300 import binding, synth
+
+        self.torch, self.binding, self.wl, self.device = torch, binding, wl, device
+        s = wl.shape
+        self.max_prefill = min(max(wl.lengths) if wl.n_seqs == 1 else 32768, wl.n_prompt_tokens)
+        self.max_prefill = max(self.max_prefill, max(wl.lengths))
+        w = weights if weights is not None else synth.make_weights(s)
+        self.model = binding.Model(s, w, max_seqs=wl.n_seqs, max_ctx=wl.max_ctx,
+                                   max_prefill_tokens=self.max_prefill, flags=flags, device=str(device))
+        del w
+        prompts = wl.prompts()
+        self.groups = chunk_prefills(wl.lengths, self.max_prefill)
+        self.group_tokens = [torch.cat([prompts[i] for i in g]).to(device) for g in self.groups]
+        self.group_tokens_host = [torch.cat([prompts[i] for i in g]).pin_memory() for g in self.groups]
+        self.B = wl.n_seqs
+        self.slots = list(range(self.B))
+        self.slots_d = torch.tensor(self.slots, dtype=torch.int32, device=device)
+        self.first = torch.zeros(self.B, dtype=torch.int32, device=device)
+        self.first_host = torch.zeros(self.B, dtype=torch.int32).pin_memory()
+        self.bufs = [torch.zeros(self.B, dtype=torch.int32, device=device) for _ in range(2)]
+        self.gen = torch.zeros(max(wl.decode_steps, 1), self.B, dtype=torch.int32, device=device)
+        self.gen_host = torch.zeros(max(wl.decode_steps, 1), self.B, dtype=torch.int32).pin_memory()
+        self.stream = torch.cuda.current_stream(device)
+
+    def prefill_all(self, host_inputs=False):
+        """Every prompt, in packed groups; returns the host->device bytes it copied."""
+        torch = self.torch
+        h2d = 0
+        for g, toks, toks_h in zip(self.groups, self.group_tokens, self.group_tokens_host):
+            if host_inputs:
+                toks = torch.empty_like(toks_h, device=self.device)
+                toks.copy_(toks_h, non_blocking=True)
+                h2d += toks_h.numel() * 4
+            lengths = [self.wl.lengths[i] for i in g]
+            nxt, _ = self.model.prefill(toks, lengths, [self.slots[i] for i in g])
+            h2d += (len(g) + 1) * 4 + len(g) * 4  # cu_seqlens and slots
+            self.first[g[0]: g[-1] + 1].copy_(nxt)
+        return h2d
+
+    def decode_all(self, record=False):
+        """Rewinds every slot to its prompt, then runs the workload's decode steps from the
+        prefill's next tokens, each step's output fed to the next on the device."""
+        for i, n in enumerate(self.wl.lengths):
+            self.model.truncate(self.slots[i], n)
+        self.bufs[0].copy_(self.first)
+        for i in range(self.wl.decode_steps):
+            src, dst = self.bufs[i % 2], self.bufs[(i + 1) % 2]
+            self.model.decode_step(src, self.slots_d, self.slots, dst)
+            if record:
+                self.gen[i].copy_(dst)
+
+    def step(self):
+        if self.wl.decode_steps:
+            self.decode_all()
+        else:
+            self.prefill_all()
+
+    def step_e2e(self):
+        """The same step through host memory: its inputs copied in from pinned host buffers
+        (the prompts, or the first tokens of the decode steps), its tokens read back."""
+        if self.wl.decode_steps:
+            self.first.copy_(self.first_host, non_blocking=True)
+            h2d = self.B * 4
+            self.decode_all(record=True)
+            self.gen_host.copy_(self.gen, non_blocking=True)
+            d2h = self.gen.numel() * 4
+        else:
+            h2d = self.prefill_all(host_inputs=True)
+            self.first_host.copy_(self.first, non_blocking=True)
+            d2h = self.B * 4
+        self.stream.synchronize()
+        return h2d, d2h
+
+
+def units_per_step(wl):
+    """(units, unit name): generated tokens for decode workloads, prompt tokens for prefill-only."""
+    if wl.decode_steps:
+        return wl.n_seqs * wl.decode_steps, "tokens/s"
+    return wl.n_prompt_tokens, "tokens/s"
+
+
+def timed_steps(torch, binding, runner, steps, local_rank, world):
+    """`steps` steps between CUDA events on the launching stream (barrier + synchronize on both
+    sides), clocks sampled meanwhile; retaken once if the clocks were throttled or locked."""
+    def once():
+        sampler = ClockSampler(local_rank)
+        sampler.start()
+        time.sleep(0.3)
+        n0 = binding.qwen3_launch_count(runner.model.ctx)
+        barrier(world)
+        torch.cuda.synchronize()
+        sampler.mark(True)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(runner.stream)
+        for _ in range(steps):
+            runner.step()
+        end.record(runner.stream)
+        torch.cuda.synchronize()
+        sampler.mark(False)
+        barrier(world)
+        n1 = binding.qwen3_launch_count(runner.model.ctx)
+        time.sleep(0.2)
+        sampler.stop()
+        return start.elapsed_time(end), n1 - n0, sampler.summary()
+
+    ms, launches, clocks = once()
+    retried = False
+    if clocks_rejected(clocks):
+        ms, launches, clocks = once()
+        retried = True
+    clocks = dict(clocks, retried=retried)
+    return ms, launches, clocks
+
+
+def e2e_steps(torch, runner, steps, world):
+    for _ in range(2):
+        runner.step_e2e()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    h2d = d2h = 0
+    for _ in range(steps):
+        h2d, d2h = runner.step_e2e()
+    return (time.perf_counter() - t0) * 1e3, h2d, d2h
+
+
+# --------------------------------------------------------------------------------------
+# roofline kernels, each timed alone with CUDA events on its launching stream
+# --------------------------------------------------------------------------------------
+
+def _peak_source(peak_kind, key, note=""):
+    if peak_kind == "measured":
+        return f"measured (MEASURED_PEAKS.json {key}{note})"
+    return "fallback " + ("6.8 TB/s" if key == "hbm_gbs" else "1.9 PFLOP/s")
+
+
+def _time_launches(torch, launch, reps):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def measure_mlp_roofline(torch, binding, wl, peaks, peak_kind):
+    """Average duration of the fused decode MLP kernel (RMSNorm + gate_up + SwiGLU + down +
+    residual; 60% of a layer's weight bytes), the kernel decode steps of up to 4 sequences run
+    for the MLP, over launches cycling through 28 layers' weights (528 MB, larger than L2)."""
+    s = wl.shape
+    dev = torch.device("cuda")
+    M, C, I = wl.n_seqs, s.hidden, s.intermediate
+    g = torch.Generator(device="cpu").manual_seed(5)
+    layers = [((torch.randn(2 * I, C, generator=g) * 0.02).to(torch.bfloat16).to(dev),
+               (torch.randn(I, C, generator=g) * 0.02).to(torch.bfloat16).to(dev)) for _ in range(s.n_layers)]
+    h = torch.randn(M, C, generator=g).to(dev)
+    gain = torch.ones(C, device=dev)
+    out = torch.zeros(M, C, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    it = [0]
+
+    def launch():
+        wgu, wdt = layers[it[0] % len(layers)]
+        it[0] += 1
+        binding.qwen3_op_mlp_decode(h.data_ptr(), M, C, gain.data_ptr(), s.rms_eps, wgu.data_ptr(), wdt.data_ptr(),
+                                    I, out.data_ptr(), stream)
+    for _ in range(len(layers)):
+        launch()
+    avg_s = _time_launches(torch, launch, 20 * len(layers))
+    algo_bytes = 3 * I * C * 2 + M * C * 4 * 3  # weights; h read, out read and written
+    achieved = algo_bytes / avg_s / 1e9
+    peak = float(peaks["hbm_gbs"])
+    return {"kernel": "k_mlp_fused (decode MLP: RMSNorm + gate_up + SwiGLU + down + residual, bf16 weights "
+                      f"[{2 * I},{C}] + [{I},{C}], {M} row(s))",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": TRAFFIC_BYTES.get("mlp_fused"),
+            "algorithmic_bytes_per_launch": algo_bytes, "avg_launch_us": round(avg_s * 1e6, 3),
+            "peak_source": _peak_source(peak_kind, "hbm_gbs")}
+
+
+def measure_attn_roofline(torch, binding, wl, peaks, peak_kind, ctx=None, reps=20):
+    """Average duration of the split-KV decode attention kernel (QK-norm + RoPE + KV write +
+    attention over keys 0..p), the kernel that streams the KV cache, at the workload's batch
+    and the positions of its middle decode step (or every row at position ctx - 1), over one
+    layer's K/V rows of the workload's size in their own buffer (larger than L2 for the long
+    contexts), through qwen3_op_attn_decode."""
+    import math
+    s = wl.shape
+    dev = torch.device("cuda")
+    B, Hq, Hkv, D = wl.n_seqs, s.n_q_heads, s.n_kv_heads, s.head_dim
+    positions = decode_positions(wl) if ctx is None else [ctx - 1] * B
+    max_ctx = max(positions) + 1
+    g = torch.Generator(device=dev).manual_seed(7)
+    kc = torch.randn((B, Hkv, max_ctx, D), generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn((B, Hkv, max_ctx, D), generator=g, device=dev).to(torch.bfloat16)
+    qkv = torch.randn((B, (Hq + 2 * Hkv) * D), generator=g, device=dev)
+    gain = torch.ones(D, device=dev)
+    inv = [s.rope_theta ** (-2.0 * i / D) for i in range(D // 2)]
+    rope = torch.tensor([[[math.cos(p * f), math.sin(p * f)] for f in inv] for p in sorted(set(positions))],
+                        dtype=torch.float32)
+    rope_full = torch.zeros((max_ctx, D // 2, 2), dtype=torch.float32)
+    for i, p in enumerate(sorted(set(positions))):
+        rope_full[p] = rope[i]  # only the rows of the positions used are read
+    rope_d = rope_full.to(dev)
+    slots = list(range(B))
+    slots_d = torch.tensor(slots, dtype=torch.int32, device=dev)
+    pos_d = torch.tensor(positions, dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    ws_bytes = binding.qwen3_op_attn_decode_workspace_bytes(B, Hq, Hkv)
+    ws = torch.zeros(ws_bytes + 256, dtype=torch.uint8, device=dev)
+    ws_ptr = (ws.data_ptr() + 255) // 256 * 256
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def launch():
+        binding.qwen3_op_attn_decode(qkv.data_ptr(), B, slots_d.data_ptr(), slots, pos_d.data_ptr(), positions,
+                                     gain.data_ptr(), gain.data_ptr(), rope_d.data_ptr(), kc.data_ptr(),
+                                     vc.data_ptr(), B, max_ctx, Hq, Hkv, s.rms_eps, 0, out.data_ptr(), ws_ptr,
+                                     ws_bytes, stream)
+    for _ in range(3):
+        launch()
+    avg_s = _time_launches(torch, launch, reps)
+    rows = sum(p + 1 for p in positions)
+    algo_bytes = rows * Hkv * D * 2 * 2  # K and V rows 0..p of every (sequence, KV head), the new one written
+    achieved = algo_bytes / avg_s / 1e9
+    peak = float(peaks["hbm_gbs"])
+    per_row = TRAFFIC_BYTES.get("attn_decode_per_key_row")
+    del kc, vc
+    return {"kernel": f"k_attn_decode_fused (split-KV decode attention + QK-norm + RoPE + KV write, {B} rows at "
+                      f"positions {min(positions)}..{max(positions)}, {Hq}/{Hkv} heads, one layer)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": round(per_row * rows) if per_row else None,
+            "algorithmic_bytes_per_launch": algo_bytes, "avg_launch_us": round(avg_s * 1e6, 3),
+            "peak_source": _peak_source(peak_kind, "hbm_gbs")}
+
+
+def measure_gemm_roofline(torch, binding, wl, peaks, peak_kind):
+    """Average duration of the prefill gate_up projection GEMM (tcgen05, SwiGLU epilogue), the
+    largest prefill GEMM, at the workload's packed token count N.  At N = 23,460 the activations
+    and the output (48 MB + 144 MB) exceed L2; the 12.6 MB of weights may stay in it."""
+    s = wl.shape
+    dev = torch.device("cuda")
+    M, K, N = wl.n_prompt_tokens, s.hidden, 2 * s.intermediate
+    g = torch.Generator(device="cpu").manual_seed(6)
+    x = (torch.randn(M, K, generator=g)).to(torch.bfloat16).to(dev)
+    w = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).to(dev)
+    out = torch.empty(M, N // 2, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def launch():
+        binding.qwen3_op_gemm(x.data_ptr(), M, K, w.data_ptr(), N, binding.QWEN3_EPI_SWIGLU, out.data_ptr(), stream)
+    for _ in range(3):
+        launch()
+    avg_s = _time_launches(torch, launch, 10)
+    flops = 2 * M * N * K
+    achieved = flops / avg_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    return {"kernel": f"k_gemm_tcp (prefill gate_up GEMM + SwiGLU, tcgen05, [{M},{K}] x [{N},{K}]^T)",
+            "bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": TRAFFIC_BYTES["gemm_gate_up"],
+            "algorithmic_flops_per_launch": flops, "avg_launch_us": round(avg_s * 1e6, 3),
+            "peak_source": _peak_source(peak_kind, "bf16_tflops", ", burst: kernel timed alone")}
+
+
+def roofline_for(torch, binding, wl, peaks, peak_kind, ctx=None):
+    """The roofline object of the workload's dominant kernel: the gate_up GEMM for prefill, the
+    fused MLP (the most weight bytes) for decode of up to 4 rows, the KV-streaming attention
+    for larger decode batches."""
+    if not wl.decode_steps:
+        return measure_gemm_roofline(torch, binding, wl, peaks, peak_kind)
+    if wl.n_seqs <= 4 and wl.shape.hidden == 1024 and ctx is None:
+        return measure_mlp_roofline(torch, binding, wl, peaks, peak_kind)
+    return measure_attn_roofline(torch, binding, wl, peaks, peak_kind, ctx=ctx)
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle timing (reference arm and the cpu_baseline objects)
+# --------------------------------------------------------------------------------------
+
+ORACLE_PREFILL_SAMPLE = 256   # prompt tokens of one oracle prefill sample
+ORACLE_DECODE_STEPS_SHORT = 8  # decode steps of the cpu_baseline sample below 8K of context
+ORACLE_DECODE_STEPS_LONG = 3   # ... at 8K of context and more
+
+
+def _oracle_model(wl):
     from oracle import qwen3_oracle as oracle
     from qwen3_decoder_forward_gb300 import synth
 
@@ -403,30 +516,56 @@ def oracle_sample(wl, n_samples=1, decode_sample=8, warmup=0):
                         s.rms_eps, s.rope_theta)
     ow = oracle.Weights(w["embed"].float().numpy(), w["final_norm"].float().numpy(),
                         [{k: v.float().numpy() for k, v in d.items()} for d in w["layers"]])
-    del w
-    prompt = wl.prompts()[0].tolist()
-    steps = decode_sample if wl.decode_steps else 0
-    times = []
-    for it in range(warmup + n_samples):
-        cache = oracle.KVCache(cfg.n_layers)
+    return oracle, cfg, ow
+
+
+class OracleSample:
+    """Bounded samples of the workload on the CPU oracle, as it stands.
+
+    Decode workloads: greedy decode steps of sequence 0 continuing one cache that starts at
+    its prompt's length (rows drawn at random: the oracle's step does the same work whatever
+    the cached values), `capacity` steps in all.  The oracle runs sequences one after
+    another, so its tokens/s for B sequences equals one sequence's.  Prefill workloads: the
+    oracle's prefill of the first ORACLE_PREFILL_SAMPLE tokens of sequence 0."""
+
+    def __init__(self, wl, capacity=0):
+        import numpy as np
+        self.wl = wl
+        self.oracle, self.cfg, self.ow = _oracle_model(wl)
+        s = wl.shape
+        self.prompt = wl.prompts()[0].tolist()
+        self.done = 0
+        if wl.decode_steps:
+            rng = np.random.default_rng(11)
+            n = wl.lengths[0]
+            k = rng.standard_normal((n, s.n_kv_heads, s.head_dim))
+            v = rng.standard_normal((n, s.n_kv_heads, s.head_dim))
+            self.cache = self.oracle.KVCache.from_arrays([k] * s.n_layers, [v] * s.n_layers, spare=capacity)
+            self.tok = self.prompt[-1]
+
+    def run(self, steps=1):
+        """Seconds per unit (one generated token, or one prompt token) over one sample."""
+        o = self.oracle
+        if self.wl.decode_steps:
+            t0 = time.perf_counter()
+            for _ in range(steps):
+                self.tok = o.forward(self.cfg, self.ow, [self.tok], self.cache)["token"]
+            self.done += steps
+            return (time.perf_counter() - t0) / steps
+        ids = self.prompt[:ORACLE_PREFILL_SAMPLE]
         t0 = time.perf_counter()
-        out = oracle.forward(cfg, ow, prompt, cache)
-        t1 = time.perf_counter()
-        tok = out["token"]
-        for _ in range(steps):
-            tok = oracle.forward(cfg, ow, [tok], cache)["token"]
-        t2 = time.perf_counter()
-        if it >= warmup:
-            times.append((t1 - t0, (t2 - t1) / max(steps, 1)))
-    return times
+        o.forward(self.cfg, self.ow, ids, o.KVCache(self.cfg.n_layers))
+        return (time.perf_counter() - t0) / len(ids)
 
-
-def oracle_value(wl, t_prefill, t_step):
-    """Extrapolated oracle throughput in the metric's unit for the whole workload."""
-    if wl.decode_steps:
-        per_seq = t_prefill + wl.decode_steps * t_step  # sequences run one after another
-        return wl.decode_steps / per_seq
-    return len(wl.prompts()[0]) / t_prefill
+    def describe(self, steps):
+        if self.wl.decode_steps:
+            n = self.wl.lengths[0]
+            return (f"oracle (numpy float64) on the host: greedy decode steps of one sequence at contexts from "
+                    f"{n + 1} ({steps} per sample), continuing a {n}-row cache of seeded random rows; the "
+                    f"oracle runs sequences one after another, so its tokens/s for {self.wl.n_seqs} sequences "
+                    f"is one sequence's")
+        n = min(ORACLE_PREFILL_SAMPLE, self.wl.lengths[0])
+        return f"oracle (numpy float64) on the host: prefill of the first {n} tokens of sequence 0"
 
 
 def cores_used():
@@ -436,32 +575,38 @@ def cores_used():
         return os.cpu_count()
 
 
-def sample_text(wl, decode_sample):
-    if wl.decode_steps:
-        return (f"oracle (numpy float64) on the host: prefill of sequence 0's {wl.lengths[0]}-token prompt + "
-                f"{decode_sample} greedy steps, extrapolated to its {wl.decode_steps}-step request "
-                f"(generated tokens / (prefill time + {wl.decode_steps} x step time))")
-    return f"oracle (numpy float64) on the host: prefill of sequence 0 ({wl.lengths[0]} tokens)"
+def cpu_baseline(wl, unit):
+    steps = (ORACLE_DECODE_STEPS_LONG if max(wl.lengths) >= 8192 else ORACLE_DECODE_STEPS_SHORT) \
+        if wl.decode_steps else 1
+    smp = OracleSample(wl, capacity=steps)
+    t = smp.run(steps)
+    return {"value": round(1.0 / t, 4), "unit": unit, "cores": cores_used(), "kind": "oracle",
+            "sample": smp.describe(steps)}
 
 
 def reference_arm(args, wl):
+    """The oracle timed as the reference: each of the warm-up and timed steps is one sample
+    (one decode step of one sequence, or one ORACLE_PREFILL_SAMPLE-token prefill)."""
     rank, _, world = dist_env()
     if rank != 0:
         return 0
-    decode_sample = 8
-    times = oracle_sample(wl, n_samples=args.steps, decode_sample=decode_sample, warmup=args.warmup)
-    tp = sum(t[0] for t in times) / len(times)
-    ts = sum(t[1] for t in times) / len(times)
-    value = oracle_value(wl, tp, ts)
     unit = units_per_step(wl)[1]
-    ms = statistics.mean((t[0] + t[1] * (decode_sample if wl.decode_steps else 0)) * 1e3 for t in times)
+    steps = max(args.steps, 1)
+    smp = OracleSample(wl, capacity=args.warmup + steps)
+    for _ in range(args.warmup):
+        smp.run()
+    per_unit = [smp.run() for _ in range(steps)]
+    t = sum(per_unit) / len(per_unit)
+    value = 1.0 / t
+    units = 1 if wl.decode_steps else min(ORACLE_PREFILL_SAMPLE, wl.lengths[0])
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": unit,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t * units * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded random-init weights and token ids)",
             "config": {"workload": workload_desc(wl)},
             "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": cores_used(), "kind": "oracle",
-                             "sample": sample_text(wl, decode_sample)},
+                             "sample": smp.describe(1) + "; each step is one sample"},
             "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -489,9 +634,71 @@ def barrier(world):
         dist.barrier()
 
 
+def prefill_once_timed(torch, runner):
+    """One pass of every prompt's prefill between CUDA events (the KV fill of a decode
+    workload); milliseconds."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(runner.stream)
+    runner.prefill_all()
+    e1.record(runner.stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, weights=None, cpu=True):
+    """Runs one workload: warm-up, the timed steps, the end-to-end steps, the roofline kernel
+    and (rank 0, one GPU) the CPU oracle sample.  Returns the fields of its JSON object."""
+    import torch
+    from qwen3_decoder_forward_gb300 import binding
+
+    runner = GpuRunner(wl, device, flags, weights)
+    units, unit = units_per_step(wl)
+    out = {}
+    if wl.decode_steps:
+        runner.prefill_all()  # first pass: graphs and lazily loaded kernels
+        fill_ms = prefill_once_timed(torch, runner)
+        runner.first_host.copy_(runner.first)  # the decode steps' first tokens, for the e2e steps
+        fill_flops = prefill_flops(wl)
+        out["kv_fill"] = {"what": f"prefill of the {wl.n_seqs} prompts ({wl.n_prompt_tokens} tokens) that fill "
+                                  "the KV cache, timed once", "ms": round(fill_ms, 3),
+                          "tokens_s": round(wl.n_prompt_tokens / (fill_ms / 1e3), 1),
+                          "tflops": round(fill_flops / (fill_ms / 1e3) / 1e12, 1),
+                          "tensor_frac": round(fill_flops / (fill_ms / 1e3) / 1e12 / float(peaks["bf16_tflops"]), 4)}
+    for _ in range(max(args.warmup, 3)):
+        runner.step()
+    torch.cuda.synchronize()
+    ms, launches, clocks = timed_steps(torch, binding, runner, args.steps, local_rank, world)
+    ms_max, units_all = reduce_over_ranks(torch, world, ms, units * args.steps)
+    e2e_ms, h2d, d2h = e2e_steps(torch, runner, args.steps, world)
+    e2e_ms_max, e2e_units = reduce_over_ranks(torch, world, e2e_ms, units * args.steps)
+    assert runner.model.status() == 0, binding.qwen3_last_error(runner.model.ctx)
+    runner.model.close()
+    del runner
+    torch.cuda.empty_cache()
+    roofline = roofline_for(torch, binding, wl, peaks, peak_kind)
+    torch.cuda.empty_cache()
+    out.update({"value": units_all / (ms_max / 1e3), "unit": unit, "ms_per_step": ms_max / args.steps,
+                "units_per_step": units, "launches": launches, "clocks": clocks,
+                "e2e": {"value": round(e2e_units / (e2e_ms_max / 1e3), 2), "unit": unit,
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "roofline": roofline})
+    step_s = ms_max / 1e3 / args.steps
+    if wl.decode_steps:
+        out["decode_step_hbm_frac"] = round(decode_step_bytes(wl) / (step_s / wl.decode_steps) / 1e9 /
+                                            float(peaks["hbm_gbs"]), 4)
+        out["decode_step_bytes"] = int(decode_step_bytes(wl))
+    else:
+        out["tflops"] = round(prefill_flops(wl) / step_s / 1e12, 1)
+        out["tensor_frac"] = round(prefill_flops(wl) / step_s / 1e12 / float(peaks["bf16_tflops"]), 4)
+    rank = dist_env()[0]
+    out["cpu_baseline"] = cpu_baseline(wl, unit) if (cpu and rank == 0 and world == 1) else None
+    return out
+
+
 def gpu_arm(args, wl):
     import torch
-    from qwen3_decoder_forward_gb300 import binding, build
+    from qwen3_decoder_forward_gb300 import binding, build, synth
 
     rank, local_rank, world = dist_env()
     build.build()
@@ -505,127 +712,64 @@ def gpu_arm(args, wl):
     flags = {"graph": 0, "graph-nopdl": binding.QWEN3_FLAG_NO_PDL,
              "direct": binding.QWEN3_FLAG_NO_GRAPH | binding.QWEN3_FLAG_NO_PDL,
              "persistent": binding.QWEN3_FLAG_PERSISTENT}[args.launch]
-    runner = GpuRunner(wl, device, flags)
-    units, unit = units_per_step(wl)
-
     args.warmup = max(args.warmup, 3)  # at least three untimed steps
-    for _ in range(args.warmup):
-        runner.step()
-    torch.cuda.synchronize()
 
-    def timed():
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-        sampler = ClockSampler(local_rank)
-        sampler.start()
-        time.sleep(0.3)
-        n0 = binding.qwen3_launch_count(runner.model.ctx)
-        barrier(world)
-        torch.cuda.synchronize()
-        sampler.mark(True)
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record()
-        for k in range(args.steps):
-            runner.step(evs[k])
-        end.record()
-        torch.cuda.synchronize()
-        sampler.mark(False)
-        barrier(world)
-        n1 = binding.qwen3_launch_count(runner.model.ctx)
-        time.sleep(0.2)
-        sampler.stop()
-        ms = start.elapsed_time(end)
-        pre = sum(e[0].elapsed_time(e[1]) for e in evs)
-        dec = sum(e[1].elapsed_time(e[2]) for e in evs)
-        return ms, pre, dec, n1 - n0, sampler.summary()
+    if args.roofline_only:
+        r = roofline_for(torch, binding, wl, peaks, peak_kind, ctx=args.roofline_ctx)
+        if rank == 0:
+            print(json.dumps({"roofline_only": True, "workload": wl.name, "roofline": r}), flush=True)
+        return 0
 
-    ms, pre_ms, dec_ms, launches, clocks = timed()
-    retried = False
-    if clocks_rejected(clocks):
-        ms, pre_ms, dec_ms, launches, clocks = timed()
-        retried = True
-    ms_max, units_all = reduce_over_ranks(torch, world, ms, units * args.steps)
-    value = units_all / (ms_max / 1e3)
-
-    # end to end: host buffers in, generated tokens out, every step
-    for _ in range(2):
-        runner.step_e2e()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    h2d = d2h = 0
-    for _ in range(args.steps):
-        h2d, d2h = runner.step_e2e()
-    e2e_s = time.perf_counter() - t0
-    e2e_s_max, e2e_units = reduce_over_ranks(torch, world, e2e_s * 1e3, units * args.steps)
-    e2e_value = e2e_units / (e2e_s_max / 1e3)
-
-    if not wl.decode_steps:
-        roofline = measure_gemm_roofline(torch, binding, wl, peaks, peak_kind)
-    elif wl.n_seqs <= 4 and wl.shape.hidden == 1024:
-        roofline = measure_mlp_roofline(torch, binding, wl, peaks, peak_kind)
-    else:
-        roofline = measure_gemv_roofline(torch, binding, wl, peaks, peak_kind)
-    assert runner.model.status() == 0, binding.qwen3_last_error(runner.model.ctx)
-    runner.model.close()
-    del runner
-    torch.cuda.empty_cache()
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        decode_sample = 8
-        t = oracle_sample(wl, n_samples=1, decode_sample=decode_sample)
-        cv = oracle_value(wl, t[0][0], t[0][1])
-        cpu = {"value": round(cv, 4), "unit": unit, "cores": cores_used(), "kind": "oracle",
-               "sample": sample_text(wl, decode_sample)}
+    weights = synth.make_weights(wl.shape)
+    main = run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, weights,
+                        cpu=not args.no_cpu_baseline)
+    pre = None
+    if wl.decode_steps and args.prefill_workload != "none":
+        pwl = synth.WORKLOADS[args.prefill_workload]
+        if pwl.shape != wl.shape:
+            weights = synth.make_weights(pwl.shape)
+        pre = run_workload(args, pwl, device, flags, peaks, peak_kind, world, local_rank, weights,
+                           cpu=not args.no_cpu_baseline)
+    del weights
 
     if rank == 0:
         s = wl.shape
-        prompt_tokens = wl.n_prompt_tokens * args.steps
-        gen_tokens = wl.n_seqs * wl.decode_steps * args.steps
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "metric": METRIC, "value": round(main["value"], 2), "unit": main["unit"], "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(main["ms_per_step"], 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random-init bf16 weights N(0,0.02), gains 1+N(0,0.05), uniform token ids)",
             "config": {"workload": workload_desc(wl),
-                       "value_is": ("generated tokens per second of the whole step (prompt prefill included in "
-                                    "the time)") if wl.decode_steps else "prompt tokens per second",
-                       "l2": "inputs larger than L2: every decode step streams 1.19 GB of weights (L2 is 129 MB)",
+                       "value_is": ("generated tokens per second: one step is the workload's decode steps of all "
+                                    "its sequences from their prompts' KV cache (slots rewound before each step; "
+                                    "the KV fill timed once, in kv_fill)") if wl.decode_steps
+                       else "prompt tokens per second: one step is one packed prefill of every prompt",
+                       "l2": "inputs larger than L2: every decode step streams 1.19 GB of weights and the KV "
+                             "rows; a prefill streams the weights per layer (L2 is 129 MB)",
                        "replicas": world, "launch": args.launch},
-            "breakdown": {"prefill_ms_per_step": round(pre_ms / args.steps, 4),
-                          "decode_ms_per_step": round(dec_ms / args.steps, 4),
-                          "prefill_tok_s": round(prompt_tokens / (pre_ms / 1e3), 1),
-                          "decode_tok_s": round(gen_tokens / (dec_ms / 1e3), 1) if gen_tokens else None},
-            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
-                       "samples": clocks["samples"], "retried": retried},
-            "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": int(launches),
-            "roofline": roofline,
-            "cpu_baseline": cpu,
+            "clocks": main["clocks"],
+            "e2e": main["e2e"],
+            "gpu_launches": int(main["launches"] + (pre["launches"] if pre else 0)),
+            "roofline": main["roofline"],
+            "cpu_baseline": main["cpu_baseline"],
         }
-        if wl.decode_steps:
-            step_bytes = decode_step_bytes(wl)
-            dec_s = dec_ms / 1e3 / args.steps / wl.decode_steps
-            line["breakdown"]["decode_step_hbm_frac"] = round(step_bytes / dec_s / 1e9 / float(peaks["hbm_gbs"]), 4)
-        pre_s = pre_ms / 1e3 / args.steps
-        line["breakdown"]["prefill_tflops"] = round(prefill_flops(wl) / pre_s / 1e12, 1)
-        line["breakdown"]["prefill_tensor_frac"] = round(prefill_flops(wl) / pre_s / 1e12 / float(peaks["bf16_tflops"]), 4)
+        bd = {}
+        for k in ("kv_fill", "decode_step_hbm_frac", "decode_step_bytes", "tflops", "tensor_frac"):
+            if k in main:
+                bd[k] = main[k]
+        line["breakdown"] = bd
+        if pre is not None:
+            line["prefill"] = {"workload": workload_desc(synth.WORKLOADS[args.prefill_workload]),
+                               "value": round(pre["value"], 1), "unit": pre["unit"],
+                               "ms_per_step": round(pre["ms_per_step"], 4), "tflops": pre["tflops"],
+                               "tensor_frac": pre["tensor_frac"], "e2e": pre["e2e"], "clocks": pre["clocks"],
+                               "gpu_launches": int(pre["launches"]), "roofline": pre["roofline"],
+                               "cpu_baseline": pre["cpu_baseline"]}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
-
-
-def decode_step_bytes(wl):
-    """Algorithmic HBM bytes of one decode step of the workload: all linear weights, the tied
-    head, every sequence's cached K/V rows (read) and the new rows (written)."""
-    s = wl.shape
-    lin = s.n_layers * ((s.q_dim + 2 * s.kv_dim) * s.hidden + s.hidden * s.q_dim + 3 * s.intermediate * s.hidden) * 2
-    head = s.vocab * s.hidden * 2
-    kv_tok = s.n_layers * 2 * s.kv_dim * 2
-    mean_ctx = sum(n + 1 + (wl.decode_steps - 1) / 2 for n in wl.lengths) / wl.n_seqs
-    return lin + head + wl.n_seqs * (mean_ctx + 1) * kv_tok
 
 
 def main():

@@ -194,8 +194,20 @@ typedef struct qwen3_sampling {
 int qwen3_set_sampling(qwen3_ctx *ctx, const qwen3_sampling *sampling);
 
 /* Synchronises the device, then returns QWEN3_OK, E_CUDA (a pending CUDA error) or E_DEVICE
- * (the device error word was set; the word is cleared). */
+ * (the device error word was set; the word is cleared).  The word records token ids out of
+ * range (clamped), positions beyond max_ctx (KV write skipped) and bounded waits that gave up
+ * (the outputs of the call they belong to are not valid; see qwen3_set_wait_limit). */
 int qwen3_get_status(qwen3_ctx *ctx);
+
+/* Failure detection.  Every wait of a kernel on an asynchronous copy or on another CTA is
+ * bounded: past its limit the kernel records "a bounded wait gave up" in the device error word,
+ * lets its own copies in flight land, and returns (no trap, no hang; qwen3_get_status then
+ * reports E_DEVICE).  This sets the limit, in SM clock cycles, of the waits of the decode
+ * kernels (the weight and KV-cache streams of qwen3_decode_step; graphs recorded earlier read
+ * the new value when replayed); 0 restores the default of 2^31 cycles (about a second).  A
+ * small limit makes those waits give up on purpose, to test the error path.  Synchronises the
+ * device.  Errors: E_INVALID, E_CUDA. */
+int qwen3_set_wait_limit(qwen3_ctx *ctx, uint32_t cycles);
 
 /* Message of the last failed call on ctx (or of the last failed qwen3_create when ctx is NULL). */
 const char *qwen3_last_error(const qwen3_ctx *ctx);
@@ -231,6 +243,15 @@ int qwen3_get_config(const qwen3_ctx *ctx, qwen3_config *cfg);
  * starts it at position 0 and decode steps reject it until then.  The cache rows keep their
  * old values (finite, never attended to).  Errors: E_INVALID (bad slot), E_CUDA. */
 int qwen3_release_slot(qwen3_ctx *ctx, int32_t slot, void *stream);
+
+/* Shortens KV slot `slot` to its first `length` tokens (0 <= length <= its current length), on
+ * the host and, in stream order on `stream`, on the device: the next decode step or
+ * qwen3_prefill_append continues at position `length` and overwrites the rows after it
+ * ("古法手撕简易LLM推理器", prefill与predict: the position offset is the cached length).  Used
+ * to rewind generated tokens (rejected drafts, a re-run of the same steps from one prompt).  A
+ * paged cache gives back the blocks past the kept positions.  length 0 is qwen3_release_slot.
+ * Errors: E_INVALID (bad slot or length), E_CUDA. */
+int qwen3_truncate_slot(qwen3_ctx *ctx, int32_t slot, int32_t length, void *stream);
 
 /* ---- Continuous batching ("第 3 章", the engine and its scheduler; "手写Qwen3-0.6B推理",
  * generation that stops at the end-of-sequence token) -------------------------------------
@@ -345,7 +366,9 @@ size_t qwen3_op_lmhead_workspace_bytes(int32_t B);
  * next_tok[b] = argmax_v E[v] . x[b] (fp32 logits, lowest index on ties) for x bf16 [B, C]
  * (the final-normed last rows) and E bf16 [V, C]; logits_dev fp32 [B, V] is written when not
  * NULL.  `workspace_dev` (>= qwen3_op_lmhead_workspace_bytes(B) bytes, 16-byte aligned) holds
- * per-CTA partial maxima.  C one of the GEMV K values; 1 <= B <= 1024.
+ * per-CTA partial maxima.  C one of 256, 512, 768, 1024, 1536, 2048, 2560, 3072; 1 <= B <= 1024.
+ * A next_tok of -1 means a bounded wait of the tensor-core pass (C == 1024, 9 to 32 rows
+ * per pass) gave up: that row's logits and token are not valid.
  * Errors: E_INVALID (NULL, bad size, small workspace), E_CUDA. */
 int qwen3_op_lmhead_argmax(const void *x_dev, int32_t B, int32_t C, const void *embed_dev,
                            int32_t V, float *logits_dev, int32_t *next_tok_dev,
@@ -365,18 +388,47 @@ int qwen3_op_lmhead_argmax(const void *x_dev, int32_t B, int32_t C, const void *
  * limit. The call itself allocates nothing.
  *
  * Set-up: the first call on each device looks up the array's address with that device
- * current, so make that first call before any stream capture.
+ * current, so make that first call before any stream capture.  The address is kept for the
+ * life of the process: do not call this again on a device after a cudaDeviceReset of it.
  *
  * Sharing: all calls on a device share the array, and it keeps the last call's contents.
  * Every partial a call reads is written by that same call, so nothing needs clearing.
  * Calls that overlap on the GPU (e.g. on two streams without ordering) race on the array
- * and must not be issued.
+ * and must not be issued.  A next_tok of -1 reports a bounded wait that gave up, as for
+ * qwen3_op_lmhead_argmax.
  *
  * Arguments, outputs and the other errors are those of qwen3_op_lmhead_argmax; the message
  * of a failure is returned by qwen3_last_error(NULL). */
 int qwen3_op_lmhead_argmax_noalloc(const void *x_dev, int32_t B, int32_t C,
                                    const void *embed_dev, int32_t V, float *logits_dev,
                                    int32_t *next_tok_dev, void *stream);
+
+/* Bytes of workspace qwen3_op_attn_decode needs for B rows. */
+size_t qwen3_op_attn_decode_workspace_bytes(int32_t B, int32_t n_q_heads, int32_t n_kv_heads);
+
+/* Split-KV decode attention of B new rows, as decode steps run it ("古法手撕简易LLM推理器",
+ * 核心计算函数与Transformer层: the new key appended, then attention over the whole cache;
+ * "从零开始写Qwen3", Attn: a one-row query sees every cached key; "手写Qwen3-0.6B推理",
+ * Attention: per-head q/k RMSNorm, rotate-half RoPE, K/V shared by Hq/Hkv query heads):
+ *   for row b at position p = positions[b] of cache slot s = slots[b]:
+ *     q_h, k = RMSNorm per head (q_gain, k_gain; eps), rotated at p (rope table);
+ *     cache K[s][g][p] = bf16(k), V[s][g][p] = bf16(v);
+ *     out[b][h] = softmax(q_h K[s][g][0..p]^T / sqrt(128)) V[s][g][0..p],  g = h / (Hq/Hkv).
+ * qkv_dev fp32 [B, (Hq + 2 Hkv) * 128] (q heads, then k, then v); q_gain_dev, k_gain_dev fp32
+ * [128]; rope_dev fp32 [max_ctx][64][2] = (cos, sin) of p * theta^(-2i/128); k_cache_dev,
+ * v_cache_dev bf16 [n_slots][Hkv][max_ctx][128] (rows 0..p-1 of each used slot hold the
+ * cached keys and values; row p is written); out_dev bf16 [B, Hq, 128].  slots and positions
+ * are given on the device and on the host (same values; slots distinct, 0 <= slot < n_slots,
+ * 0 <= position < max_ctx).  n_split key ranges per (row, KV head), 1..64, or 0 for one wave
+ * of CTAs as a decode step plans it.  workspace_dev: qwen3_op_attn_decode_workspace_bytes
+ * bytes, 256-byte aligned, zero-filled before its first use (calls leave it reusable).
+ * head_dim 128; Hq/Hkv in {1, 2, 4, 8}.  Errors: E_INVALID (NULL, bad size or index), E_CUDA. */
+int qwen3_op_attn_decode(const float *qkv_dev, int32_t B, const int32_t *slots_dev,
+                         const int32_t *slots_host, const int32_t *positions_dev,
+                         const int32_t *positions_host, const float *q_gain_dev, const float *k_gain_dev,
+                         const float *rope_dev, void *k_cache_dev, void *v_cache_dev, int32_t n_slots,
+                         int32_t max_ctx, int32_t n_q_heads, int32_t n_kv_heads, float eps, int32_t n_split,
+                         void *out_dev, void *workspace_dev, size_t workspace_bytes, void *stream);
 
 /* Candidates qwen3_sample draws from: the most likely tokens of a row, at most this many. */
 #define QWEN3_SAMPLE_CANDIDATES 1024

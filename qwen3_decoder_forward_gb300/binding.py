@@ -101,6 +101,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_kv_copy_rows": (ctypes.c_int, [_P, i32, i32, i32, i32, _P, _P, _P]),
         "qwen3_kv_free_blocks": (i32, [_P]),
         "qwen3_release_slot": (ctypes.c_int, [_P, i32, _P]),
+        "qwen3_truncate_slot": (ctypes.c_int, [_P, i32, i32, _P]),
+        "qwen3_set_wait_limit": (ctypes.c_int, [_P, ctypes.c_uint32]),
         "qwen3_engine_workspace_bytes": (sz, [_P, i32]),
         "qwen3_engine_create": (ctypes.c_int, [_P, i32, _P, sz, ctypes.POINTER(_P)]),
         "qwen3_engine_submit": (ctypes.c_int, [_P, i64, pi32, i32, i32, i32]),
@@ -119,6 +121,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_op_lmhead_argmax": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P, sz, _P]),
         "qwen3_op_lmhead_argmax_noalloc": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P]),
         "qwen3_sample": (ctypes.c_int, [_P, i32, i32, _P, _P, _P, _P, _P, _P]),
+        "qwen3_op_attn_decode_workspace_bytes": (sz, [i32, i32, i32]),
+        "qwen3_op_attn_decode": (ctypes.c_int, [_P, i32, _P, pi32, _P, pi32, _P, _P, _P, _P, _P, i32, i32, i32, i32,
+                                                ctypes.c_float, i32, _P, _P, sz, _P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -202,6 +207,14 @@ def qwen3_get_config(ctx) -> qwen3_config:
 
 def qwen3_release_slot(ctx, slot: int, stream: int = 0):
     _check(load_library().qwen3_release_slot(ctx, slot, stream), ctx)
+
+
+def qwen3_truncate_slot(ctx, slot: int, length: int, stream: int = 0):
+    _check(load_library().qwen3_truncate_slot(ctx, slot, length, stream), ctx)
+
+
+def qwen3_set_wait_limit(ctx, cycles: int):
+    _check(load_library().qwen3_set_wait_limit(ctx, int(cycles)), ctx)
 
 
 def _engine_check(rc: int, eng) -> None:
@@ -318,6 +331,21 @@ def qwen3_op_mlp_decode(h_ptr: int, M: int, C: int, gain_ptr: int, eps: float, w
     (gate/up rows interleaved in w_gate_up [2I, C], down transposed in w_down_t [I, C])."""
     _check(load_library().qwen3_op_mlp_decode(h_ptr, M, C, gain_ptr, eps, w_gate_up_ptr, w_down_t_ptr, I,
                                               out_ptr, stream), None)
+
+
+def qwen3_op_attn_decode_workspace_bytes(B: int, n_q_heads: int, n_kv_heads: int) -> int:
+    return int(load_library().qwen3_op_attn_decode_workspace_bytes(B, n_q_heads, n_kv_heads))
+
+
+def qwen3_op_attn_decode(qkv_ptr: int, B: int, slots_ptr: int, slots_host: Sequence[int], positions_ptr: int,
+                         positions_host: Sequence[int], q_gain_ptr: int, k_gain_ptr: int, rope_ptr: int,
+                         k_cache_ptr: int, v_cache_ptr: int, n_slots: int, max_ctx: int, n_q_heads: int,
+                         n_kv_heads: int, eps: float, n_split: int, out_ptr: int, ws_ptr: int, ws_bytes: int,
+                         stream: int = 0):
+    _check(load_library().qwen3_op_attn_decode(qkv_ptr, B, slots_ptr, _i32_array(slots_host), positions_ptr,
+                                               _i32_array(positions_host), q_gain_ptr, k_gain_ptr, rope_ptr,
+                                               k_cache_ptr, v_cache_ptr, n_slots, max_ctx, n_q_heads, n_kv_heads,
+                                               eps, n_split, out_ptr, ws_ptr, ws_bytes, stream), None)
 
 
 QWEN3_SAMPLE_CANDIDATES = 1024
@@ -450,6 +478,13 @@ class Model:
 
     def status(self) -> int:
         return qwen3_get_status(self.ctx)
+
+    def truncate(self, slot: int, length: int):
+        """Shortens a slot to its first `length` tokens (qwen3_truncate_slot)."""
+        qwen3_truncate_slot(self.ctx, slot, length, self._stream())
+
+    def set_wait_limit(self, cycles: int):
+        qwen3_set_wait_limit(self.ctx, cycles)
 
     def kv_copy(self, layer: int, slot: int, pos0: int, n: int):
         """K and V rows pos0 .. pos0+n-1 of (layer, slot) as new bf16 tensors [n, Hkv, D], for

@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
         for (int st = 0; st < STAGES; ++st) mbar_init(&full[st], 1);
         for (int c = 0; c < min(STAGES, n_chunks); ++c) issue(c);
     }
+    const long long lim = wait_limit(err);
     float gq[16], gk[16];
     float2 cs[16];
 #pragma unroll
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
     pdl_wait();
     pdl_trigger();
     if (!pos_ok) {
-        if (threadIdx.x == 0 && split == 0) atomicOr(err, ERR_POSITION);
+        if (threadIdx.x == 0 && split == 0 && err) atomicOr(err, ERR_POSITION);
         return;  // no copy was issued
     }
     const int heads = Hq + 2 * Hkv;
@@ -239,10 +240,12 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
     };
 
     bool ok = true;
+    int stop = 0;  // first chunk not consumed: chunks stop .. stop + STAGES - 1 may be in flight
     const int j0 = (warp * 4 + kg) * KPG;  // this group's first key in each chunk
     for (int c = 0; c < n_chunks; ++c) {
         const int st = c % STAGES;
-        const bool late = !mbar_wait_bounded(&full[st], (c / STAGES) & 1, err);
+        stop = c;
+        const bool late = !mbar_wait_ctx(&full[st], (c / STAGES) & 1, err, lim);
         if (__syncthreads_or(late)) {  // the whole CTA gives up together
             ok = false;
             break;
@@ -268,8 +271,14 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
         if (threadIdx.x == 0 && c + STAGES < n_chunks) issue(c + STAGES);
     }
     if (!ok) {
-        // give the copies already issued a bounded chance to land, then leave
-        for (int c = 0; c < min(STAGES, n_chunks); ++c) mbar_wait_bounded(&full[c % STAGES], 0, nullptr);
+        // Let the copies in flight land (the latest issued phase of each stage), then take part
+        // in the split count as usual, so the counter is left zero; the output stays unwritten
+        // and the error word says why.
+        if (threadIdx.x == 0)
+            for (int c = stop; c < min(stop + STAGES, n_chunks); ++c)
+                mbar_wait_bounded(&full[c % STAGES], (c / STAGES) & 1, nullptr);
+        if (n_split > 1 && threadIdx.x == 0 && atomicAdd(&counters[b * Hkv + g], 1) == n_split - 1)
+            counters[b * Hkv + g] = 0;
         return;
     }
     __syncthreads();  // s_new is visible

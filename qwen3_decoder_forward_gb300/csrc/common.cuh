@@ -116,12 +116,51 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
     return ok != 0;
 }
 
-// Waits for phase `phase` of `bar` for at most ~2^31 SM cycles (about a second); on timeout
+// Default limit of a bounded wait: 2^31 SM cycles, about a second at 2 GHz.
+constexpr long long WAIT_LIMIT_DEFAULT = 1ll << 31;
+
+// Waits for phase `phase` of `bar` for at most WAIT_LIMIT_DEFAULT SM cycles; on timeout
 // sets ERR_TIMEOUT in *err and returns false instead of spinning forever.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase, uint32_t *err) {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, phase)) {
-        if (clock64() - t0 > (1ll << 31)) {
+        if (clock64() - t0 > WAIT_LIMIT_DEFAULT) {
+            if (err) atomicOr(err, ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// The device status block of a context is err[0] = error bits, err[1] = the wait limit of
+// the decode kernels in SM cycles (0: WAIT_LIMIT_DEFAULT), set by the host between calls.
+// Kernels read it once, at their start, with their other constant inputs.
+__device__ __forceinline__ long long wait_limit(const uint32_t *err) {
+    if (!err) return WAIT_LIMIT_DEFAULT;
+    const uint32_t l = __ldcg(err + 1);
+    return l ? (long long)l : WAIT_LIMIT_DEFAULT;
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait_bounded with the limit `lim` from wait_limit (the decode kernels: weight and KV
+// streams).  The default limit waits as mbar_wait_bounded does; a limit set by the host polls
+// without suspending, so that a wait on a copy issued just before gives up deterministically
+// when the limit is a few cycles.  A caller that gives up must still let its issued copies land
+// (mbar_wait_bounded with a null err, the default limit) before the CTA exits.
+__device__ __forceinline__ bool mbar_wait_ctx(uint64_t *bar, uint32_t phase, uint32_t *err, long long lim) {
+    if (lim == WAIT_LIMIT_DEFAULT) return mbar_wait_bounded(bar, phase, err);
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, phase)) {
+        if (clock64() - t0 > lim) {
             if (err) atomicOr(err, ERR_TIMEOUT);
             return false;
         }

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(V2_WARPS * 32) k_gemv_bulk(const void *__restr
         // now, so HBM keeps streaming while the dependency chain runs from L2.
         prefetch_l2(W_ahead + (size_t)row0 * K, (uint32_t)nrows * K * 2);
     }
+    const long long lim = wait_limit(err);
     float4 gv[NORM ? 2 * KV : 1];  // static gains: loaded before the dependency wait
     if (NORM) {
 #pragma unroll
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(V2_WARPS * 32) k_gemv_bulk(const void *__restr
         for (int i = threadIdx.x; i < M * (K / 8); i += V2_WARPS * 32) xs[i] = xg[i];
     }
     __syncthreads();
-    if (!mbar_wait_bounded(bar, 0, err)) {
+    if (!mbar_wait_ctx(bar, 0, err, lim)) {
         mbar_wait_bounded(bar, 0, nullptr);  // let the copy land before the CTA exits
         return;
     }
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(MLP_WARPS * 32) k_mlp_fused(const float *__res
         prefetch_l2(Wgu_ahead + (size_t)2 * a0 * C, (uint32_t)na * 2 * C * 2);
         prefetch_l2(WdT_ahead + (size_t)a0 * C, (uint32_t)na * C * 2);
     }
+    const long long lim = wait_limit(err);
     float4 gv[2 * KV];
 #pragma unroll
     for (int i = 0; i < 2 * KV; ++i) gv[i] = reinterpret_cast<const float4 *>(gain)[i * 32 + lane];
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(MLP_WARPS * 32) k_mlp_fused(const float *__res
         }
     }
     __syncthreads();
-    const bool ok = __syncthreads_and(mbar_wait_bounded(bar, 0, err));
+    const bool ok = __syncthreads_and(mbar_wait_ctx(bar, 0, err, lim));
     if (!ok) {
         mbar_wait_bounded(bar, 0, nullptr);
         return;
@@ -489,6 +491,7 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restr
         __syncwarp();
         if (lane < MMA_ROWS) bulk_g2s(ws + lane * stride, W + (size_t)(row0 + lane) * K + k0, Kc * 2, bar);
     }
+    const long long lim = wait_limit(err);
     // rows of X beyond M are zero
     for (int i = threadIdx.x; i < (MMA_MPAD - M) * (Kc / 8); i += MMA_WARPS * 32)
         *reinterpret_cast<uint4 *>(xs + (M + i / (Kc / 8)) * stride + (i % (Kc / 8)) * 16) = make_uint4(0, 0, 0, 0);
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restr
         __syncwarp();
         if (lane < M) bulk_g2s(xs + lane * stride, X + (size_t)lane * K + k0, Kc * 2, xbar);
     }
-    const bool ok = __syncthreads_and(mbar_wait_bounded(bar, 0, err) && mbar_wait_bounded(xbar, 0, err));
+    const bool ok = __syncthreads_and(mbar_wait_ctx(bar, 0, err, lim) && mbar_wait_ctx(xbar, 0, err, lim));
     if (!ok) {
         mbar_wait_bounded(bar, 0, nullptr);
         mbar_wait_bounded(xbar, 0, nullptr);
@@ -597,6 +600,7 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_lmhead_mma(const bf16 *__res
         for (int st = 0; st < LM_STAGES; ++st) mbar_init(&full[st], 1);
         mbar_init(xbar, 1);
     }
+    const long long lim = wait_limit(err);
     if (threadIdx.x < MMA_MPAD) {
         best_v[threadIdx.x] = -INFINITY;
         best_i[threadIdx.x] = 0x7fffffff;
@@ -616,12 +620,14 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_lmhead_mma(const bf16 *__res
         __syncwarp();
         if (lane < M) bulk_g2s(xs + lane * stride, X + (size_t)lane * C, C * 2, xbar);
     }
-    bool ok = __syncthreads_and(mbar_wait_bounded(xbar, 0, err));
+    bool ok = __syncthreads_and(mbar_wait_ctx(xbar, 0, err, lim));
     const uint32_t xsa = smem_addr(xs);
     const int g = lane >> 2, t = lane & 3;
+    int stop = 0;  // first tile not consumed: tiles stop .. stop + LM_STAGES - 1 may be in flight
     for (int i = 0; ok && i < my_tiles; ++i) {
         const int st = i % LM_STAGES;
-        ok = __syncthreads_and(mbar_wait_bounded(&full[st], (i / LM_STAGES) & 1, err));
+        stop = i;
+        ok = __syncthreads_and(mbar_wait_ctx(&full[st], (i / LM_STAGES) & 1, err, lim));
         if (!ok) break;
         const uint32_t wsa = smem_addr(ring + st * MMA_ROWS * stride);
         float acc[4][4];
@@ -677,9 +683,19 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_lmhead_mma(const bf16 *__res
         }
         __syncthreads();  // red is rewritten by the next tile
     }
-    if (!ok) {  // let issued copies land
-        for (int i = 0; i < min(LM_STAGES, my_tiles); ++i) mbar_wait_bounded(&full[i], 0, nullptr);
-        mbar_wait_bounded(xbar, 0, nullptr);
+    if (!ok) {
+        // Let the copies in flight land: the latest issued phase of each stage.  Then report the
+        // failure through the partials: (+inf, -1) wins the reduction, so the row's token is -1.
+        if (threadIdx.x == 0) {
+            for (int j = stop; j < min(stop + LM_STAGES, my_tiles); ++j)
+                mbar_wait_bounded(&full[j % LM_STAGES], (j / LM_STAGES) & 1, nullptr);
+            mbar_wait_bounded(xbar, 0, nullptr);
+        }
+        __syncthreads();
+        if (threadIdx.x < M) {
+            part_val[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = INFINITY;
+            part_idx[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = -1;
+        }
         return;
     }
     if (threadIdx.x < M) {

@@ -71,7 +71,9 @@ extern "C" int qwen3_op_lmhead_argmax_noalloc(const void *x_dev, int32_t B, int3
     DeviceScratch s;
     {
         // First call on this device: look up the array's device address with this device
-        // current. Done once per device; later calls reuse the cached address.
+        // current. Done once per device; later calls reuse the cached address (which is why
+        // the library must not outlive a cudaDeviceReset of that device: the reset unloads
+        // the module the address belongs to).
         std::lock_guard<std::mutex> lock(g_mu);
         if (!g_dev[dev].ready) {
             void *p = nullptr;
@@ -87,7 +89,8 @@ extern "C" int qwen3_op_lmhead_argmax_noalloc(const void *x_dev, int32_t B, int3
         s = g_dev[dev];
     }
     const int n_parts = std::min(lmhead_parts(s.num_sms), NOALLOC_PARTS);
-    // Pass 1 writes every (row, CTA) partial that pass 2 reads, so the previous call's
+    // Pass 1 writes every (row, CTA) partial that pass 2 reads -- a CTA whose bounded wait
+    // gave up writes (+inf, -1), which makes that row's token -1 -- so the previous call's
     // contents never leak into this one and nothing needs clearing first.
     float *part_val = static_cast<float *>(s.ptr);
     int32_t *part_idx = reinterpret_cast<int32_t *>(part_val + (size_t)NOALLOC_MAX_B * NOALLOC_PARTS);

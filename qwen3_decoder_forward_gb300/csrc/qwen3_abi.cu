@@ -364,7 +364,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
     Q3_TRY(launch_final_norm(lc, mlp ? res[k.n_layers & 1] : resid, rows.cu_seqlens, rows.B,
                              c->at<float>(L.o_gfinal), last, C, k.rms_eps));
     Q3_TRY(launch_lmhead_argmax(lc, last, rows.B, C, embed, k.vocab, logits, c->at<float>(L.o_pval),
-                                c->at<int32_t>(L.o_pidx), c->n_parts, next, rows));
+                                c->at<int32_t>(L.o_pidx), c->n_parts, next, rows, err));
     return draw_next(c, lc, logits, rows.B, next);
 }
 
@@ -815,6 +815,7 @@ int qwen3_get_status(qwen3_ctx *c) {
         std::string m = "device error word set:";
         if (word & ERR_TOKEN_RANGE) m += " token id out of range (clamped);";
         if (word & ERR_POSITION) m += " position beyond max_ctx (KV write skipped);";
+        if (word & ERR_TIMEOUT) m += " a bounded wait in a kernel gave up (outputs of that call are not valid);";
         return c->fail(QWEN3_E_DEVICE, m);
     }
     return QWEN3_OK;
@@ -993,6 +994,86 @@ int qwen3_op_lmhead_argmax(const void *x, int32_t B, int32_t C, const void *embe
                                          pval, pidx, n_parts, next_tok, r);
     if (e != cudaSuccess) {
         g_create_error = std::string("qwen3_op_lmhead_argmax: ") + cudaGetErrorString(e);
+        return QWEN3_E_CUDA;
+    }
+    return QWEN3_OK;
+}
+
+int qwen3_set_wait_limit(qwen3_ctx *c, uint32_t cycles) {
+    if (!c) return QWEN3_E_INVALID;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(c->arena + c->lay.o_err + 4, &cycles, 4, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_set_wait_limit");
+    return QWEN3_OK;
+}
+
+int qwen3_truncate_slot(qwen3_ctx *c, int32_t slot, int32_t length, void *stream) {
+    if (!c) return QWEN3_E_INVALID;
+    if (slot < 0 || slot >= c->cfg.max_seqs) return c->fail(QWEN3_E_INVALID, "qwen3_truncate_slot: slot out of range");
+    if (length < 0 || length > c->len_host[slot])
+        return c->fail(QWEN3_E_INVALID, "qwen3_truncate_slot: length outside [0, the slot's length]");
+    // pageable source: the copy is staged before the call returns
+    const cudaError_t e = cudaMemcpyAsync(c->at<int32_t>(c->lay.o_ctxlen) + slot, &length, sizeof(int32_t),
+                                          cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_truncate_slot");
+    c->len_host[slot] = length;
+    if (kv_paged(c)) {  // give back the blocks past the kept positions, last block first
+        const int bs = c->cfg.kv_block_tokens, mb = c->lay.kv_max_blocks;
+        const int keep = (length + bs - 1) / bs;
+        for (int i = c->kv_nblk[slot] - 1; i >= keep; --i) c->kv_free.push_back(c->kv_table[(size_t)slot * mb + i]);
+        c->kv_nblk[slot] = std::min(c->kv_nblk[slot], keep);
+    }
+    return QWEN3_OK;
+}
+
+size_t qwen3_op_attn_decode_workspace_bytes(int32_t B, int32_t n_q_heads, int32_t n_kv_heads) {
+    if (B < 1 || B > 1024 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads) return 0;
+    const size_t D = 128;
+    return align_up((size_t)B * n_q_heads * MAX_SPLIT * 2 * 4) + align_up((size_t)B * n_q_heads * MAX_SPLIT * D * 4) +
+           align_up((size_t)B * n_kv_heads * 4);
+}
+
+int qwen3_op_attn_decode(const float *qkv, int32_t B, const int32_t *slots, const int32_t *slots_host,
+                         const int32_t *positions, const int32_t *positions_host, const float *q_gain,
+                         const float *k_gain, const float *rope, void *k_cache, void *v_cache, int32_t n_slots,
+                         int32_t max_ctx, int32_t n_q_heads, int32_t n_kv_heads, float eps, int32_t n_split, void *out,
+                         void *ws, size_t ws_bytes, void *stream) {
+    g_create_error.clear();
+    const int g = n_kv_heads > 0 ? n_q_heads / n_kv_heads : 0;
+    if (!qkv || !slots || !slots_host || !positions || !positions_host || !q_gain || !k_gain || !rope || !k_cache ||
+        !v_cache || !out || !ws ||
+        B < 1 || n_slots < 1 || max_ctx < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads ||
+        (g != 1 && g != 2 && g != 4 && g != 8) || n_split < 0 || n_split > MAX_SPLIT || !(eps >= 0.0f) ||
+        reinterpret_cast<uintptr_t>(ws) % 256 || ws_bytes < qwen3_op_attn_decode_workspace_bytes(B, n_q_heads, n_kv_heads)) {
+        g_create_error = "qwen3_op_attn_decode: bad argument";
+        return QWEN3_E_INVALID;
+    }
+    for (int b = 0; b < B; ++b)
+        if (slots_host[b] < 0 || slots_host[b] >= n_slots || positions_host[b] < 0 || positions_host[b] >= max_ctx) {
+            g_create_error = "qwen3_op_attn_decode: slot or position out of range";
+            return QWEN3_E_INVALID;
+        }
+    const Launch lc = op_launch(stream);
+    if (n_split == 0) {  // one wave of CTAs, as a decode step plans it for contexts up to max_ctx
+        const int slots_all = lc.num_sms * attn_decode_ctas_per_sm(n_q_heads, n_kv_heads);
+        n_split = std::max(1, std::min({slots_all / (B * n_kv_heads), MAX_SPLIT, (max_ctx + 63) / 64}));
+    }
+    const size_t D = 128;
+    float *ws_ml = static_cast<float *>(ws);
+    float *ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + align_up((size_t)B * n_q_heads * MAX_SPLIT * 2 * 4));
+    int *counters = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ws_o) + align_up((size_t)B * n_q_heads * MAX_SPLIT * D * 4));
+    Rows r;
+    r.slots = slots;
+    r.row_slot = const_cast<int32_t *>(slots);
+    r.row_pos = const_cast<int32_t *>(positions);
+    r.B = B;
+    r.rows = B;
+    const cudaError_t e = launch_attn_decode_fused(lc, qkv, r, q_gain, k_gain, reinterpret_cast<const float2 *>(rope),
+                                                   static_cast<bf16 *>(k_cache), static_cast<bf16 *>(v_cache), n_split,
+                                                   ws_ml, ws_o, counters, static_cast<bf16 *>(out), n_q_heads,
+                                                   n_kv_heads, max_ctx, eps, nullptr);
+    if (e != cudaSuccess) {
+        g_create_error = std::string("qwen3_op_attn_decode: ") + cudaGetErrorString(e);
         return QWEN3_E_CUDA;
     }
     return QWEN3_OK;

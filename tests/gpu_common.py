@@ -9,6 +9,9 @@ Q and the KV cache to bf16 (relative step 2^-8); accumulations, norms and softma
 
 from __future__ import annotations
 
+import concurrent.futures
+import multiprocessing
+
 import numpy as np
 import torch
 
@@ -80,3 +83,23 @@ class Gate:
     def summary(self):
         return (f"worst hidden rel-L2 {self.worst_hidden:.2e}, worst logits rel-L2 {self.worst_logits:.2e}, "
                 f"tokens checked {self.tokens_checked}, skipped (margin <= {MARGIN}) {self.tokens_skipped}")
+
+
+def _oracle_prefill_job(shape, prompt):
+    """Worker: the oracle's prefill of one prompt with the synthetic weights of `shape`
+    (drawn again from their seeds in this process); hidden states as float32."""
+    from qwen3_decoder_forward_gb300 import synth
+    w = synth.make_weights(shape)
+    ref = oracle.forward(oracle_config(shape), oracle_weights(w), list(prompt), oracle.KVCache(shape.n_layers))
+    ref["hidden"] = ref["hidden"].astype(np.float32)
+    return ref
+
+
+def oracle_prefills(shape, prompts):
+    """The oracle's prefill of each prompt (lists of ids), one spawned process per prompt, so
+    long prompts run side by side on the host cores.  Spawned, not forked: the parent may
+    already hold a CUDA context."""
+    ctx = multiprocessing.get_context("spawn")
+    with concurrent.futures.ProcessPoolExecutor(max_workers=len(prompts), mp_context=ctx) as ex:
+        futs = [ex.submit(_oracle_prefill_job, shape, [int(t) for t in p]) for p in prompts]
+        return [f.result() for f in futs]

@@ -352,6 +352,30 @@ def check_cache_consistency(o):
     assert run["fed"][0] == prefill_next
 
 
+def check_cache_from_arrays(o):
+    """A cache rebuilt from another cache's rows (as the long-context test rebuilds one from the
+    GPU's rows) holds exactly those rows and continues exactly as the original: decode steps
+    from it equal the steps of the run that filled the original ("古法手撕简易LLM推理器",
+    prefill与predict: each step reads the cached K/V and appends one row)."""
+    cfg = tiny_cfg(o, layers=2)
+    w = tiny_weights(o, cfg, seed=21)
+    prompt = [9, 31, 4, 4, 60, 2]
+    run = o.generate(cfg, w, prompt, steps=3)
+    filled = o.KVCache(2)
+    o.forward(cfg, w, prompt, filled)
+    ks = [filled.keys(layer).copy() for layer in range(2)]
+    vs = [filled.values(layer).copy() for layer in range(2)]
+    c = o.KVCache.from_arrays(ks, vs, spare=3)
+    assert c.length == len(prompt)
+    for layer in range(2):
+        assert np.array_equal(c.keys(layer), ks[layer]) and np.array_equal(c.values(layer), vs[layer])
+    for s in range(3):
+        step = o.forward(cfg, w, [run["fed"][s]], c)
+        _close(step["logits"], run["calls"][s + 1]["logits"], tol=1e-12, what=f"rebuilt cache step {s}")
+        _close(step["hidden"], run["calls"][s + 1]["hidden"], tol=1e-12, what=f"rebuilt cache step {s} hidden")
+    assert c.length == len(prompt) + 3
+
+
 def check_greedy_ties_and_margin(o):
     tok, margin = o.greedy(np.array([0.5, 2.0, -1.0, 2.0, 1.5]))
     assert tok == 1, "ties resolve to the lowest index"
@@ -512,6 +536,7 @@ ALL_CHECKS = [
     check_embedding_rows,
     check_causality_prefix,
     check_cache_consistency,
+    check_cache_from_arrays,
     check_greedy_ties_and_margin,
     check_sample_frequencies_brute_force,
     check_sample_limits_and_invariance,

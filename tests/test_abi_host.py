@@ -129,6 +129,36 @@ def test_paged_kv_config_sizes_and_rejections(lib):
         assert binding.qwen3_arena_bytes(cfg) == 0, (bt, pool, flags, heads)
 
 
+def test_truncate_and_wait_limit_reject_null_context(lib):
+    assert lib.qwen3_truncate_slot(None, 0, 0, None) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_set_wait_limit(None, 16) == binding.QWEN3_E_INVALID
+
+
+def test_attn_decode_op_rejects_bad_arguments_before_any_launch(lib):
+    assert binding.qwen3_op_attn_decode_workspace_bytes(0, 16, 8) == 0
+    assert binding.qwen3_op_attn_decode_workspace_bytes(4, 16, 3) == 0
+    ws = binding.qwen3_op_attn_decode_workspace_bytes(4, 16, 8)
+    assert ws >= 4 * 16 * 64 * (2 + 128) * 4 + 4 * 8 * 4
+    p = 256  # any non-NULL, 256-byte aligned value: the checks return before a pointer is used
+    slots, pos = binding._i32_array([0, 1, 2, 3]), binding._i32_array([5, 6, 7, 8])
+
+    def call(**kw):
+        a = dict(qkv=p, B=4, slots=p, slots_host=slots, pos=p, pos_host=pos, qg=p, kg=p, rope=p, kc=p, vc=p,
+                 n_slots=4, max_ctx=64, hq=16, hkv=8, eps=1e-6, n_split=0, out=p, ws=p, ws_bytes=ws)
+        a.update(kw)
+        return lib.qwen3_op_attn_decode(a["qkv"], a["B"], a["slots"], a["slots_host"], a["pos"], a["pos_host"],
+                                        a["qg"], a["kg"], a["rope"], a["kc"], a["vc"], a["n_slots"], a["max_ctx"],
+                                        a["hq"], a["hkv"], a["eps"], a["n_split"], a["out"], a["ws"],
+                                        a["ws_bytes"], None)
+    for kw in ({"qkv": None}, {"slots_host": None}, {"out": None}, {"B": 0}, {"hkv": 3}, {"hq": 48, "hkv": 3},
+               {"n_split": 65}, {"ws_bytes": ws - 1}, {"ws": p + 16}, {"eps": -1.0},
+               {"slots_host": binding._i32_array([0, 1, 2, 4])},   # slot >= n_slots
+               {"pos_host": binding._i32_array([5, 6, 7, 64])},    # position >= max_ctx
+               {"pos_host": binding._i32_array([5, -1, 7, 8])}):
+        assert call(**kw) == binding.QWEN3_E_INVALID, kw
+        assert "qwen3_op_attn_decode" in binding.qwen3_last_error(None)
+
+
 def test_paged_kv_calls_reject_null(lib):
     assert lib.qwen3_kv_copy_rows(None, 0, 0, 0, 1, 16, 16, None) == binding.QWEN3_E_INVALID
     assert lib.qwen3_kv_free_blocks(None) == -1

@@ -1,0 +1,127 @@
+"""Edge shapes of the 28-layer model against the oracle, every row and every layer.
+
+These lengths and contexts reach the partial tiles, the diagonal mask and the split
+boundaries of the attention kernels:
+
+ * one packed prefill of sequences of 1, 127, 129 and 257 tokens (a one-row sequence, both
+   sides of a 128-row query tile and of a 128-key tile, one past a power of two) -- every
+   row of every sequence on every layer, and each last row's logits and token
+   ("第 3 章 前向与生成（代码走读）", 5: position i reads keys 0..i only, checked on the
+   packed shape table);
+ * a one-token prompt decoded from position 1 ("从零开始写Qwen3", Attn: a one-row query
+   after the cache must see every cached key; a causal flag would hide all but the first);
+ * decode batches of 3, 5 and 9 sequences whose contexts cross the 64-key chunks and the
+   128-key tiles (2^k - 1, 2^k, 2^k + 1), teacher-forced: every layer, logits and token of
+   every row of every step.  Three, five and nine rows take the three decode projection
+   paths (fused MLP up to 4 rows, separate gate/up and down up to 8, tensor-core GEMV from 9).
+"""
+
+import pytest
+import torch
+
+import gpu_common as gc
+from oracle import qwen3_oracle as oracle
+from qwen3_decoder_forward_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+S = synth.QWEN3_0P6B
+
+
+@pytest.fixture(scope="module")
+def model_weights():
+    gc.ensure_library()
+    w = synth.make_weights(S)
+    return w, gc.oracle_weights(w)
+
+
+def _prompts(lengths, seed):
+    return [synth.make_tokens(n, S.vocab, seed + 7919 * i) for i, n in enumerate(lengths)]
+
+
+def test_packed_prefill_of_edge_lengths(model_weights):
+    w, ow = model_weights
+    cfg = gc.oracle_config(S)
+    lengths = [1, 127, 129, 257]
+    prompts = _prompts(lengths, 101)
+    N = sum(lengths)
+    cu = synth.cu_seqlens(lengths)
+    m = binding.Model(S, w, max_seqs=len(lengths), max_ctx=max(lengths), max_prefill_tokens=N)
+    dump = torch.zeros((S.n_layers + 1) * N * S.hidden, dtype=torch.float32, device="cuda")
+    m.set_debug_dump(dump)
+    nxt, logits = m.prefill(torch.cat(prompts).cuda(), lengths, list(range(len(lengths))), want_logits=True)
+    hid = dump.view(S.n_layers + 1, N, S.hidden).cpu().numpy()
+    m.set_debug_dump(None)
+    gate = gc.Gate()
+    for i, p in enumerate(prompts):
+        ref = oracle.forward(cfg, ow, p.tolist(), oracle.KVCache(S.n_layers))
+        for layer in range(S.n_layers + 1):
+            gate.hidden(hid[layer, cu[i]: cu[i + 1]], ref["hidden"][layer], f"len {lengths[i]} h_{layer}")
+        gate.logits(logits[i].cpu().numpy(), ref["logits"], f"len {lengths[i]}")
+        gate.token(int(nxt[i]), ref["token"], ref["margin"], f"len {lengths[i]}")
+    assert m.status() == 0
+    m.close()
+    print(gate.summary())
+    gate.check()
+
+
+def _decode_batch(w, ow, lengths, steps, seed):
+    """Prefill `lengths`, then `steps` teacher-forced decode steps of all rows at once; every
+    row of every call is gated against the oracle's own run of that sequence."""
+    cfg = gc.oracle_config(S)
+    prompts = _prompts(lengths, seed)
+    B = len(lengths)
+    refs = [oracle.generate(cfg, ow, p.tolist(), steps) for p in prompts]
+    m = binding.Model(S, w, max_seqs=B, max_ctx=max(lengths) + steps, max_prefill_tokens=sum(lengths))
+    gate = gc.Gate()
+    nxt, logits = m.prefill(torch.cat(prompts).cuda(), lengths, list(range(B)), want_logits=True)
+    for i in range(B):
+        r = refs[i]["calls"][0]
+        gate.logits(logits[i].cpu().numpy(), r["logits"], f"len {lengths[i]} prefill")
+        gate.token(int(nxt[i]), r["token"], r["margin"], f"len {lengths[i]} prefill")
+    buf = torch.zeros((S.n_layers + 1) * B * S.hidden, dtype=torch.float32, device="cuda")
+    m.set_debug_dump(buf)
+    slots = list(range(B))
+    slots_d = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    lg = torch.zeros(B, S.vocab, dtype=torch.float32, device="cuda")
+    for t in range(steps):
+        inp = torch.tensor([refs[i]["fed"][t] for i in range(B)], dtype=torch.int32, device="cuda")
+        out = torch.zeros(B, dtype=torch.int32, device="cuda")
+        m.decode_step(inp, slots_d, slots, out, lg)
+        hid = buf.view(S.n_layers + 1, B, S.hidden).cpu().numpy()
+        for i in range(B):
+            r = refs[i]["calls"][t + 1]
+            what = f"B={B} len {lengths[i]} step {t} (position {lengths[i] + t})"
+            for layer in range(S.n_layers + 1):
+                gate.hidden(hid[layer, i], r["hidden"][layer, 0], f"{what} h_{layer}")
+            gate.logits(lg[i].cpu().numpy(), r["logits"], what)
+            gate.token(int(out[i]), r["token"], r["margin"], what)
+    assert m.status() == 0
+    for i in range(B):
+        assert binding.qwen3_slot_length(m.ctx, i) == lengths[i] + steps
+    m.close()
+    print(gate.summary())
+    gate.check()
+    return gate
+
+
+def test_one_token_prompt_decoded_from_position_1(model_weights):
+    w, ow = model_weights
+    gate = _decode_batch(w, ow, [1], 4, 202)
+    assert gate.tokens_checked + gate.tokens_skipped == 5
+
+
+def test_decode_three_rows_across_chunk_and_tile_boundaries(model_weights):
+    w, ow = model_weights
+    # positions 62..65, 127..130, 255..258: contexts 2^k - 1 .. 2^k + 2 at 64, 128 and 256
+    _decode_batch(w, ow, [62, 127, 255], 4, 303)
+
+
+def test_decode_five_rows_short_and_boundary_contexts(model_weights):
+    w, ow = model_weights
+    _decode_batch(w, ow, [1, 63, 64, 65, 129], 3, 404)
+
+
+def test_decode_nine_rows_tensor_core_path(model_weights):
+    w, ow = model_weights
+    _decode_batch(w, ow, [2, 17, 31, 32, 33, 95, 96, 97, 191], 3, 505)

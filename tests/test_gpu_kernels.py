@@ -116,3 +116,64 @@ def test_decode_mlp_vs_torch(M):
     with pytest.raises(binding.Qwen3Error):
         binding.qwen3_op_mlp_decode(h.data_ptr(), 5, C, gain.data_ptr(), eps, w_gu.data_ptr(), w_dt.data_ptr(), I,
                                     out.data_ptr(), 0)
+
+
+@pytest.mark.parametrize("positions,n_split", [([0, 64, 200], 0), ([63, 127, 129], 1), ([5, 250, 128], 7),
+                                               ([255, 1, 100], 64)])
+def test_decode_attention_op_vs_oracle(positions, n_split):
+    """qwen3_op_attn_decode against the oracle's per-head RMSNorm, rotate-half RoPE and causal
+    GQA attention, over cached rows drawn at random and the new row at `positions`."""
+    import numpy as np
+    from oracle import qwen3_oracle as oracle
+
+    gc.ensure_library()
+    B, Hq, Hkv, D, max_ctx, eps, theta = len(positions), 16, 8, 128, 256, 1e-6, 1e6
+    n_slots = B + 1
+    slots = [2, 0, 3][:B]
+    g = torch.Generator(device="cpu").manual_seed(sum(positions) + n_split)
+    qkv = torch.randn((B, (Hq + 2 * Hkv) * D), generator=g)
+    qg = 1 + 0.05 * torch.randn(D, generator=g)
+    kg = 1 + 0.05 * torch.randn(D, generator=g)
+    kc = torch.randn((n_slots, Hkv, max_ctx, D), generator=g).to(torch.bfloat16)
+    vc = torch.randn((n_slots, Hkv, max_ctx, D), generator=g).to(torch.bfloat16)
+    ang = np.arange(max_ctx)[:, None] * oracle.rope_inv_freq(D, theta)[None, :]
+    rope = torch.from_numpy(np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32))
+    dev = [t.cuda().contiguous() for t in (qkv, qg, kg, kc, vc, rope)]
+    qkv_d, qg_d, kg_d, kc_d, vc_d, rope_d = dev
+    slots_d = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    pos_d = torch.tensor(positions, dtype=torch.int32, device="cuda")
+    out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = binding.qwen3_op_attn_decode_workspace_bytes(B, Hq, Hkv)
+    ws = torch.zeros(ws_bytes + 256, dtype=torch.uint8, device="cuda")
+    ws_ptr = (ws.data_ptr() + 255) // 256 * 256
+    stream = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):  # the second call finds the workspace as the first left it
+        binding.qwen3_op_attn_decode(qkv_d.data_ptr(), B, slots_d.data_ptr(), slots, pos_d.data_ptr(), positions,
+                                     qg_d.data_ptr(), kg_d.data_ptr(), rope_d.data_ptr(), kc_d.data_ptr(),
+                                     vc_d.data_ptr(), n_slots, max_ctx, Hq, Hkv, eps, n_split, out.data_ptr(),
+                                     ws_ptr, ws_bytes, stream)
+    torch.cuda.synchronize()
+    got = out.float().cpu().numpy()
+    kc_after, vc_after = kc_d.float().cpu().numpy(), vc_d.float().cpu().numpy()
+    for b, (s, p) in enumerate(zip(slots, positions)):
+        row = qkv[b].double().numpy()
+        q = row[: Hq * D].reshape(1, Hq, D)
+        k = row[Hq * D: (Hq + Hkv) * D].reshape(1, Hkv, D)
+        v = row[(Hq + Hkv) * D:].reshape(1, Hkv, D)
+        q = oracle.apply_rope(oracle.rms_norm(q, qg.double().numpy(), eps), np.array([p]), theta)
+        k = oracle.apply_rope(oracle.rms_norm(k, kg.double().numpy(), eps), np.array([p]), theta)
+        # the cache row of the new position holds bf16(k), bf16(v)
+        assert gc.rel_l2(kc_after[s, :, p], k[0]) <= 8e-3
+        assert gc.rel_l2(vc_after[s, :, p], v[0]) <= 8e-3
+        keys = kc[s].double().numpy().transpose(1, 0, 2)[: p + 1].copy()   # [p+1, Hkv, D]
+        vals = vc[s].double().numpy().transpose(1, 0, 2)[: p + 1].copy()
+        keys[p], vals[p] = k[0], v[0]
+        ref = oracle.causal_gqa_attention(q, keys, vals, np.array([p]), np.arange(p + 1))
+        assert gc.rel_l2(got[b], ref[0]) <= gc.REL_L2, (b, p)
+    # rows of other positions and of the unused slot are untouched
+    for s in range(n_slots):
+        for p in range(max_ctx):
+            if (s, p) in zip(slots, positions):
+                continue
+            if p % 37 == 0 or s == 1:
+                assert np.array_equal(kc_after[s, :, p], kc[s, :, p].float().numpy())

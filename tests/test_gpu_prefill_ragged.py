@@ -1,7 +1,8 @@
 """Ragged prefill at full size: 8 sequences with lengths drawn from [512, 4096], packed into
-one [N, C] batch with cu_seqlens.  Sequence 1 (packed after sequence 0) is checked against
-the oracle on every layer of every row and on its last-row logits.  Every sequence is then
-prefilled alone, and the packed results must equal those (packing changes nothing)."""
+one [N, C] batch with cu_seqlens.  Sequence 1 (2,024 tokens, packed after sequence 0) and
+sequence 7 (4,032 tokens, the longest, packed last) are checked against the oracle on every
+layer of every row and on their last-row logits.  Every sequence is then prefilled alone, and
+the packed results must equal those (packing changes nothing)."""
 
 import numpy as np
 import pytest
@@ -14,7 +15,7 @@ from qwen3_decoder_forward_gb300 import binding, synth
 pytestmark = pytest.mark.gpu
 
 WL = synth.WORKLOADS["prefill_ragged"]
-SAMPLED = 1
+SAMPLED = (1, 7)
 
 
 def test_prefill_ragged_parity_and_packing():
@@ -23,22 +24,23 @@ def test_prefill_ragged_parity_and_packing():
     B, N = WL.n_seqs, WL.n_prompt_tokens
     w = synth.make_weights(s)
     prompts = WL.prompts()
-    ref = oracle.forward(gc.oracle_config(s), gc.oracle_weights(w), prompts[SAMPLED].tolist(),
-                         oracle.KVCache(s.n_layers))
+    refs = dict(zip(SAMPLED, gc.oracle_prefills(s, [prompts[i].tolist() for i in SAMPLED])))
 
     m = binding.Model(s, w, max_seqs=B, max_ctx=max(WL.lengths), max_prefill_tokens=N)
     cu = synth.cu_seqlens(list(WL.lengths))
     dump = torch.zeros((s.n_layers + 1) * N * s.hidden, dtype=torch.float32, device="cuda")
     m.set_debug_dump(dump)
     nxt, logits = m.prefill(torch.cat(prompts).cuda(), list(WL.lengths), list(range(B)), want_logits=True)
-    hid = dump.view(s.n_layers + 1, N, s.hidden)[:, cu[SAMPLED]: cu[SAMPLED + 1]].cpu().numpy()
+    gate = gc.Gate()
+    for i in SAMPLED:
+        ref = refs[i]
+        hid = dump.view(s.n_layers + 1, N, s.hidden)[:, cu[i]: cu[i + 1]].cpu().numpy()
+        for layer in range(s.n_layers + 1):
+            gate.hidden(hid[layer], ref["hidden"][layer], f"seq {i} h_{layer}")
+        gate.logits(logits[i].cpu().numpy(), ref["logits"], f"seq {i}")
+        gate.token(int(nxt[i]), ref["token"], ref["margin"], f"seq {i}")
     m.set_debug_dump(None)
     del dump
-    gate = gc.Gate()
-    for layer in range(s.n_layers + 1):
-        gate.hidden(hid[layer], ref["hidden"][layer], f"seq {SAMPLED} h_{layer}")
-    gate.logits(logits[SAMPLED].cpu().numpy(), ref["logits"], f"seq {SAMPLED}")
-    gate.token(int(nxt[SAMPLED]), ref["token"], ref["margin"], f"seq {SAMPLED}")
     print(gate.summary())
     gate.check()
 

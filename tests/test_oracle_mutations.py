@@ -45,6 +45,9 @@ MUTANTS = {
     "wq_transposed_heads": ('q = (u @ w["wq"].T).reshape(t, hq, d)',
                             'q = (u @ w["wq"].T).reshape(t, d, hq).transpose(0, 2, 1)'),
     "o_proj_head_order": ("h = h + o.reshape(t, hq * d)", "h = h + o.transpose(0, 2, 1).reshape(t, hq * d)"),
+    "from_arrays_kv_swapped": ("c._k[layer][:s] = k\n            c._v[layer][:s] = v",
+                               "c._k[layer][:s] = v\n            c._v[layer][:s] = k"),
+    "from_arrays_drops_last_row": ("c._n[layer] = s\n", "c._n[layer] = s - 1\n"),
     "sample_ascending_order": ("np.lexsort((np.arange(z.shape[0]), -z))", "np.lexsort((np.arange(z.shape[0]), z))"),
     "sample_no_temperature": ("z = z / DTYPE(temperature)", "z = z"),
     "sample_top_p_one_short": ("side=\"left\")) + 1", "side=\"left\"))"),

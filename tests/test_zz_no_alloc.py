@@ -27,7 +27,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     gc.ensure_library()
     C = 1024
     stream = torch.cuda.current_stream().cuda_stream
-    for B, V, seed in ((32, 151936, 21), (5, 50021, 22)):
+    # 32 rows (tensor-core pass), 5 rows (SIMT pass), then 17 rows on the tensor-core pass again:
+    # a smaller batch after a larger one must not pick up the earlier call's partials
+    for B, V, seed in ((32, 151936, 21), (5, 50021, 22), (17, 151936, 24)):
         x, e = _inputs(B, V, C, seed)
         ws_bytes = binding.qwen3_op_lmhead_workspace_bytes(B)
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
@@ -44,6 +46,14 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         assert torch.equal(tok, ref_tok)
         # the chosen token is the argmax of the logits, lowest index on ties
         assert torch.equal(tok.long(), torch.argmax(ref_log, dim=1))
+        # and, independently of both entry points, the argmax of x E^T in fp32 (torch) wherever
+        # its top-1/top-2 gap exceeds 0.1
+        ref = x.float() @ e.float().T
+        assert gc.rel_l2(log.cpu().numpy(), ref.cpu().numpy()) <= 1e-5
+        top2 = torch.topk(ref, 2, dim=1).values
+        clear = (top2[:, 0] - top2[:, 1]) > 0.1
+        assert int(clear.sum()) >= 1
+        assert torch.equal(tok.long()[clear], torch.argmax(ref, dim=1)[clear])
 
 
 def test_noalloc_refuses_batches_beyond_its_scratch():
