@@ -52,6 +52,30 @@ cudaError_t launch(const Launch &lc, void (*kern)(KArgs...), dim3 grid, dim3 blo
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// The same, for a kernel launched as clusters of `cluster` CTAs (grid a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(const Launch &lc, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           dim3 cluster, Args &&...args) {
+    cudaError_t pe = prefer_max_shared(reinterpret_cast<const void *>(kern));
+    if (pe != cudaSuccess) return pe;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = lc.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster.x;
+    attr[0].val.clusterDim.y = cluster.y;
+    attr[0].val.clusterDim.z = cluster.z;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = lc.pdl ? 2 : 1;
+    if (lc.counter) ++*lc.counter;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Where the cached K (or V) row of (slot, KV head g, position p) lives, in rows of D elements
 // from the layer's base.  Contiguous (table == nullptr): [slot][Hkv][max_ctx][D].  Paged:
 // blocks of bs positions, [block][Hkv][bs][D], the block of position p of a slot being
@@ -86,9 +110,10 @@ struct Rows {
 };
 
 // --- norm.cu ---------------------------------------------------------------------------
+// zero_buf (may be null): rows [rows, C] fp32 cleared for a kernel that accumulates into them.
 cudaError_t launch_embed_rmsnorm(const Launch &lc, const int32_t *tokens, const Rows &r,
                                  const bf16 *embed, const float *gamma, float *resid, bf16 *xn,
-                                 int C, int V, float eps, uint32_t *err);
+                                 int C, int V, float eps, uint32_t *err, float *zero_buf = nullptr);
 cudaError_t launch_rmsnorm(const Launch &lc, const float *resid, int rows, const float *gamma,
                            bf16 *xn, int C, float eps);
 // Final norm of each sequence's last row: row cu_seqlens[b+1]-1 (or b) -> out[b].
@@ -202,6 +227,45 @@ cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const R
                                      bf16 *k_layer, bf16 *v_layer, int n_split,
                                      float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
                                      int Hkv, int max_ctx, float eps, uint32_t *err);
+
+// --- decode_block.cu (decode of 1-2 rows: one attention-block and one MLP-block kernel per layer)
+// Hidden 1024, head_dim 128, two query heads per KV head.  Row b appends to slot slots[b] at
+// position ctx_len[slots[b]].
+struct AttnBlockParams {
+    const float *h_in;      // [B, C] residual entering the layer
+    float *h_out;           // [B, C] += h_in + o_proj(attention); zero on entry
+    float *zero_next;       // [B, C] cleared here (the MLP block's output)
+    const float *g_in;      // [C] input_layernorm gain
+    const bf16 *wqkv;       // [(Hq + 2 Hkv) D, C]
+    const bf16 *wog;        // [Hkv][C][2 D]: o_proj, the columns of each KV head's query heads together
+    const float *g_q, *g_k; // [D]
+    const float2 *rope;     // [max_ctx][D/2] (cos, sin)
+    bf16 *k_layer, *v_layer;
+    const int32_t *slots;   // [B]
+    const int32_t *ctx_len; // [max_seqs]
+    KvMap kv;
+    const bf16 *ahead_gu, *ahead_dt;  // this layer's MLP weights, asked of L2 (may be null)
+    int B, Hq, Hkv, max_ctx, I;
+    float eps, scale_log2;
+    uint32_t *err;
+};
+struct MlpBlockParams {
+    const float *h_in;      // [B, C] residual after attention
+    float *h_out;           // [B, C] += h_in + MLP(h_in); zero on entry
+    float *zero_next;       // [B, C] cleared here (the next attention block's output)
+    const float *gain;      // [C] post_attention_layernorm gain
+    const bf16 *wgu;        // [2I, C] gate/up rows interleaved
+    const bf16 *wdt;        // [I, C] down weight transposed
+    const bf16 *ahead_qkv, *ahead_og;  // the next layer's attention weights, asked of L2 (may be null)
+    int qkv_rows, og_cols;  // their sizes: rows of C elements
+    int B, C, I, NA;        // NA set by the launcher
+    float eps;
+    uint32_t *err;
+};
+bool decode_block_supported(int B, int C, int Hq, int Hkv, int head_dim, int I, int num_sms);
+size_t attn_block_smem(int B);
+cudaError_t launch_attn_block(const Launch &lc, const AttnBlockParams &p);
+cudaError_t launch_mlp_block(const Launch &lc, const MlpBlockParams &p);
 
 // --- decode_persistent.cu (one decode step as a single persistent kernel) ------------------
 struct DecodePersistentArgs {

@@ -38,10 +38,12 @@ __device__ __forceinline__ void norm_store(float4 x, const float *gamma, bf16 *d
 __global__ void k_embed_rmsnorm(const int32_t *__restrict__ tokens, Rows r,
                                 const bf16 *__restrict__ embed, const float *__restrict__ gamma,
                                 float *__restrict__ resid, bf16 *__restrict__ xn, int C, int V,
-                                float eps, uint32_t *err) {
+                                float eps, uint32_t *err, float *__restrict__ zero_buf) {
     __shared__ float red[32];
     pdl_wait();
     const int row = blockIdx.x;
+    if (zero_buf)  // this row of a buffer the next kernel accumulates into
+        reinterpret_cast<float4 *>(zero_buf + (size_t)row * C)[threadIdx.x] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     int id = tokens[row];
     if (id < 0 || id >= V) {
         if (threadIdx.x == 0) atomicOr(err, ERR_TOKEN_RANGE);
@@ -104,9 +106,9 @@ __global__ void k_bf16_to_f32(const bf16 *__restrict__ src, float *__restrict__ 
 
 cudaError_t launch_embed_rmsnorm(const Launch &lc, const int32_t *tokens, const Rows &r,
                                  const bf16 *embed, const float *gamma, float *resid, bf16 *xn,
-                                 int C, int V, float eps, uint32_t *err) {
+                                 int C, int V, float eps, uint32_t *err, float *zero_buf) {
     return launch(lc, k_embed_rmsnorm, dim3(r.rows), dim3(C / 4), 0, tokens, r, embed, gamma,
-                  resid, xn, C, V, eps, err);
+                  resid, xn, C, V, eps, err, zero_buf);
 }
 
 cudaError_t launch_rmsnorm(const Launch &lc, const float *resid, int rows, const float *gamma,

@@ -225,6 +225,72 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
                                cudaMemcpyDeviceToDevice, lc.stream);
     };
 
+    // decode of 1-2 rows: two kernels per layer over three rotating residual buffers
+    const bool block = decode && !(k.flags & QWEN3_FLAG_DECODE_CHAIN) &&
+                       decode_block_supported(R, C, Hq, Hkv, D, I, lc.num_sms);
+    if (block) {
+        float *rb[3];
+        for (int i = 0; i < 3; ++i) rb[i] = c->at<float>(L.o_pres) + (size_t)i * k.max_seqs * C;
+        Q3_TRY(launch_embed_rmsnorm(lc, tokens, rows, embed, (const float *)(c->layer(0) + L.o_gin), rb[0], xn, C,
+                                    k.vocab, k.rms_eps, err, rb[1]));
+        Q3_TRY(dump(0, rb[0]));
+        const float scale_log2 = 1.4426950408889634f / std::sqrt((float)D);
+        for (int l = 0; l < k.n_layers; ++l) {
+            const uint8_t *lw = c->layer(l);
+            const uint8_t *nw = c->layer((l + 1) % k.n_layers);  // the next layer (the next step's first)
+            AttnBlockParams a;
+            a.h_in = rb[(2 * l) % 3];
+            a.h_out = rb[(2 * l + 1) % 3];
+            a.zero_next = rb[(2 * l + 2) % 3];
+            a.g_in = (const float *)(lw + L.o_gin);
+            a.wqkv = (const bf16 *)(lw + L.o_wqkv);
+            a.wog = (const bf16 *)(lw + L.o_wog);
+            a.g_q = (const float *)(lw + L.o_gq);
+            a.g_k = (const float *)(lw + L.o_gk);
+            a.rope = rope;
+            a.k_layer = c->kcache(l);
+            a.v_layer = c->vcache(l);
+            a.slots = rows.slots;
+            a.ctx_len = rows.ctx_len;
+            a.kv = rows.kv;
+            a.ahead_gu = (const bf16 *)(lw + L.o_wgu);
+            a.ahead_dt = (const bf16 *)(lw + L.o_wdownT);
+            a.B = R;
+            a.Hq = Hq;
+            a.Hkv = Hkv;
+            a.max_ctx = k.max_ctx;
+            a.I = I;
+            a.eps = k.rms_eps;
+            a.scale_log2 = scale_log2;
+            a.err = err;
+            Q3_TRY(launch_attn_block(lc, a));
+            MlpBlockParams m;
+            m.h_in = a.h_out;
+            m.h_out = rb[(2 * l + 2) % 3];
+            m.zero_next = rb[(2 * l + 3) % 3];
+            m.gain = (const float *)(lw + L.o_gpost);
+            m.wgu = (const bf16 *)(lw + L.o_wgu);
+            m.wdt = (const bf16 *)(lw + L.o_wdownT);
+            m.ahead_qkv = (const bf16 *)(nw + L.o_wqkv);
+            m.ahead_og = (const bf16 *)(nw + L.o_wog);
+            m.qkv_rows = qkv_n;
+            m.og_cols = Hq * D;
+            m.B = R;
+            m.C = C;
+            m.I = I;
+            m.NA = 0;
+            m.eps = k.rms_eps;
+            m.err = err;
+            Q3_TRY(launch_mlp_block(lc, m));
+            Q3_TRY(dump(l + 1, m.h_out));
+        }
+        bf16 *last = c->at<bf16>(L.o_last);
+        Q3_TRY(launch_final_norm(lc, rb[(2 * k.n_layers) % 3], nullptr, rows.B, c->at<float>(L.o_gfinal), last, C,
+                                 k.rms_eps));
+        Q3_TRY(launch_lmhead_argmax(lc, last, rows.B, C, embed, k.vocab, logits, c->at<float>(L.o_pval),
+                                    c->at<int32_t>(L.o_pidx), c->n_parts, next, rows, err));
+        return draw_next(c, lc, logits, rows.B, next);
+    }
     Q3_TRY(launch_embed_rmsnorm(lc, tokens, rows, embed, (const float *)(c->layer(0) + L.o_gin),
                                 resid, xn, C, k.vocab, k.rms_eps, err));
     Q3_TRY(dump(0, resid));
