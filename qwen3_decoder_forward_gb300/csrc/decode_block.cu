@@ -50,52 +50,60 @@ namespace q3 {
 namespace {
 
 constexpr int D = 128;
-constexpr int AB_CL = 16;       // CTAs per KV-head group (cluster size of the attention block)
+constexpr int AB_CL = 8;        // CTAs per KV-head group (cluster size of the attention block)
 constexpr int AB_C = 1024;      // hidden size this path is built for
 constexpr int AB_G = 2;         // query heads per KV head
-constexpr int AB_ROWS = (AB_G + 2) * D / AB_CL;  // q/k/v weight rows per CTA: 32
-constexpr int AB_OROWS = AB_C / AB_CL;           // o_proj output rows per CTA: 64
+constexpr int AB_ROWS = (AB_G + 2) * D / AB_CL;  // q/k/v weight rows per CTA: 64, in two halves
+constexpr int AB_HALF = AB_ROWS / 2;             // rows per pass through the weight buffer: 32
+constexpr int AB_OROWS = AB_C / AB_CL;           // o_proj output rows per CTA: 128
 constexpr int AB_WARPS = 8;
 constexpr int KV_KEYS = 16;     // keys per K/V stage
 constexpr int KV_STAGES = 2;
-constexpr int MLP_CL = 8;       // cluster size of the MLP block
 constexpr int MLP_WARPS = 8;
 
 // Shared-memory layout of the attention block for nb rows (byte offsets).
 struct AbLayout {
     size_t w, kv, xs, qkvx, qv, knew, vnew, wpart, part, obuf, total;
     __host__ __device__ explicit AbLayout(int nb) {
-        w = 128;                                               // q/k/v rows, then o_proj rows
-        kv = w + (size_t)AB_ROWS * AB_C * 2;                   // [stage][K | V][KV_KEYS][D] bf16
-        xs = kv + (size_t)KV_STAGES * 2 * KV_KEYS * D * 2;     // [nb][C] bf16: RMSNorm(h) * g
+        w = 128;                                               // 32 q/k/v rows at a time, then o_proj rows
+        kv = w + (size_t)AB_HALF * AB_C * 2;                   // [stage][K | V][KV_KEYS][D] bf16
+        // once every key is consumed, the stages' space takes the partial softmaxes:
+        wpart = kv;                                            // [warps][nb][G][D + 2] per warp
+        part = wpart + (size_t)AB_WARPS * nb * AB_G * (D + 2) * 4;  // [nb][G][D + 2] this CTA's
+        obuf = part + (size_t)nb * AB_G * (D + 2) * 4;         // [nb][G D] merged attention output
+        const size_t stages = (size_t)KV_STAGES * 2 * KV_KEYS * D * 2;
+        const size_t partials = obuf + (size_t)nb * AB_G * D * 4 - kv;
+        xs = kv + (stages > partials ? stages : partials);    // [nb][C] bf16: RMSNorm(h) * g
         qkvx = xs + (size_t)nb * AB_C * 2;                     // [nb][(G+2) D] fp32: the group's q|k|v
         qv = qkvx + (size_t)nb * (AB_G + 2) * D * 4;           // [nb][G][D] normed, rotated, scaled q
         knew = qv + (size_t)nb * AB_G * D * 4;                 // [nb][D] the new key (bf16-rounded)
         vnew = knew + (size_t)nb * D * 4;                      // [nb][D] the new value (bf16-rounded)
         total = vnew + (size_t)nb * D * 4;
-        // in the upper half of w, free once the q/k/v dot products are done (o_proj rows
-        // take the lower half):
-        wpart = w + (size_t)AB_OROWS * AB_G * D * 2;           // [warps][nb][G][D + 2] per warp
-        part = wpart + (size_t)AB_WARPS * nb * AB_G * (D + 2) * 4;  // [nb][G][D + 2] this CTA's
-        obuf = part + (size_t)nb * AB_G * (D + 2) * 4;         // [nb][G D] merged attention output
     }
 };
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16(x)); }
 
-// Bulk copies of `rows` consecutive rows of `bytes_per_row` bytes, one copy per row issued by
-// the lanes of one warp, completing on `bar` (which the caller armed for the total).
-__device__ __forceinline__ void copy_rows(void *dst, const void *src, int rows, uint32_t bytes_per_row,
-                                          uint64_t *bar, int lane) {
-    for (int r = lane; r < rows; r += 32)
-        bulk_g2s(static_cast<uint8_t *>(dst) + (size_t)r * bytes_per_row,
-                 static_cast<const uint8_t *>(src) + (size_t)r * bytes_per_row, bytes_per_row, bar);
+// A contiguous block of `bytes` (a multiple of 16) as `parts` bulk copies of about equal size,
+// issued by lanes 0 .. parts-1 of one warp, completing on `bar` (armed by the caller for the
+// total).  A few large copies: each copy takes the issuing lane tens of cycles, so one copy per
+// 2 KB row would spend microseconds just issuing.
+__device__ __forceinline__ void copy_split(void *dst, const void *src, uint32_t bytes, int parts, uint64_t *bar,
+                                           int lane) {
+    const uint32_t per = ((bytes / parts) + 15) & ~15u;
+    if (lane < parts) {
+        const uint32_t off = per * lane;
+        if (off < bytes)
+            bulk_g2s(static_cast<uint8_t *>(dst) + off, static_cast<const uint8_t *>(src) + off, min(per, bytes - off),
+                     bar);
+    }
 }
 
 __device__ __forceinline__ float exp2_or_zero(float x) { return x == -INFINITY ? 0.0f : exp2f(x); }
 
+// At most 168 registers a thread: with the MLP block's 80, one CTA of each fits an SM's 64 K.
 template <int NB>
-__global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams p) {
+__global__ void __maxnreg__(168) k_attn_block(AttnBlockParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const AbLayout L(NB);
     cg::cluster_group cluster = cg::this_cluster();
@@ -128,7 +136,7 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
     for (int b = 0; b < NB; ++b) {
         slot[b] = __ldcg(p.slots + b);
         pos[b] = __ldcg(p.ctx_len + slot[b]);
-        const int per = (pos[b] + AB_CL) / AB_CL;  // ceil((pos + 1) / 16)
+        const int per = (pos[b] + AB_CL) / AB_CL;  // ceil((pos + 1) / AB_CL)
         k0[b] = rank * per;
         k1[b] = min(pos[b] + 1, k0[b] + per);
         cend[b] = max(k0[b], min(k1[b], pos[b]));  // cached keys [k0, cend)
@@ -163,21 +171,28 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
             done += run;
         }
     };
-    // this CTA's q/k/v rows: the group's rows are [q_2g | q_2g+1 | k_g | v_g], 128 each
+    // this CTA's q/k/v rows: the group's rows are [q_2g | q_2g+1 | k_g | v_g], 128 each; local
+    // row lr of the group is weight row wrow(lr)
     const int lr0 = rank * AB_ROWS;
-    const int wrow0 = lr0 < AB_G * D ? g * AB_G * D + lr0
-                                     : (lr0 < (AB_G + 1) * D ? Hq * D + g * D + (lr0 - AB_G * D)
-                                                             : (Hq + Hkv) * D + g * D + (lr0 - (AB_G + 1) * D));
+    auto wrow = [&](int lr) {
+        return lr < AB_G * D ? g * AB_G * D + lr
+                             : (lr < (AB_G + 1) * D ? Hq * D + g * D + (lr - AB_G * D)
+                                                    : (Hq + Hkv) * D + g * D + (lr - (AB_G + 1) * D));
+    };
     if (threadIdx.x == 0) {
         mbar_init(wbar, 1);
         mbar_init(obar, 1);
         for (int s = 0; s < KV_STAGES; ++s) mbar_init(&kvfull[s], 1);
     }
     __syncthreads();
+    // The next kernel may launch now: it only reads, before its own dependency wait, what is
+    // final already (weights, cached K/V rows, slot lengths), and waits for this grid to
+    // complete before it touches anything this kernel writes.
+    pdl_trigger();
     if (warp == 0) {
-        if (lane == 0) mbar_expect_tx(wbar, AB_ROWS * AB_C * 2);
+        if (lane == 0) mbar_expect_tx(wbar, AB_HALF * AB_C * 2);
         __syncwarp();
-        copy_rows(w4, p.wqkv + (size_t)wrow0 * AB_C, AB_ROWS, AB_C * 2, wbar, lane);
+        copy_split(w4, p.wqkv + (size_t)wrow(lr0) * AB_C, AB_HALF * AB_C * 2, 4, wbar, lane);
     } else if (warp == 1 && lane == 0) {
         for (int c = 0; c < min(KV_STAGES, n_chunks); ++c) issue(c);
     } else if (warp == 2 && lane == 0 && p.ahead_gu) {
@@ -191,15 +206,48 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
             prefetch_l2(reinterpret_cast<const uint8_t *>(p.ahead_dt) + (size_t)cta * s_dt,
                         (uint32_t)min(s_dt, dt - (size_t)cta * s_dt));
     }
-    cluster.sync();  // every CTA of the cluster is running before any writes into another's memory
+    // the second half of this CTA's q/k/v rows goes to registers: warp w, rows 4w .. 4w+3 of it,
+    // the lane's four 16-byte pieces of each (64 registers)
+    uint4 wreg[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const bf16 *src = p.wqkv + (size_t)wrow(lr0 + AB_HALF + warp * 4 + r) * AB_C;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) wreg[r][i] = ld_stream(src + (i * 32 + lane) * 8);
+    }
+    // constants: the input norm's gains (warps 0 .. NB-1, the lane's 32 elements) and those of
+    // the per-head norm + RoPE phase (warp (b, h), lane's dims lane + 32 k)
+    float4 gin[8];
+    if (warp < NB) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            gin[2 * i] = __ldg(reinterpret_cast<const float4 *>(p.g_in) + i * 64 + lane * 2);
+            gin[2 * i + 1] = __ldg(reinterpret_cast<const float4 *>(p.g_in) + i * 64 + lane * 2 + 1);
+        }
+    }
+    float gain4[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+    float2 cs0 = make_float2(1.0f, 0.0f), cs1 = make_float2(1.0f, 0.0f);
+    if (warp < NB * (AB_G + 2)) {
+        const int b = warp / (AB_G + 2), h = warp % (AB_G + 2);
+        const int ps = b ? pos[NB - 1] : pos[0];
+        if (h <= AB_G) {
+            const float *gn = h < AB_G ? p.g_q : p.g_k;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) gain4[k] = __ldg(gn + lane + 32 * k);
+            cs0 = __ldg(p.rope + (size_t)ps * (D / 2) + lane);
+            cs1 = __ldg(p.rope + (size_t)ps * (D / 2) + lane + 32);
+        }
+    }
+    // every CTA of the cluster must be running before any writes into another's memory: arrive
+    // now, wait right before the first such write
+    cluster.barrier_arrive();
     pdl_wait();
-    pdl_trigger();
 
     // residual: this CTA's share of h into the output row (other CTAs add their o_proj rows);
     // the MLP block's output buffer cleared
-    {
+    if (warp == AB_WARPS - 1) {  // the last warp, so that it overlaps the norm of warps 0 .. NB-1
         const int per = (NB * AB_C + n_cta - 1) / n_cta;
-        for (int i = threadIdx.x; i < per; i += blockDim.x) {
+        for (int i = lane; i < per; i += 32) {
             const int e = cta * per + i;
             if (e < NB * AB_C) {
                 atomicAdd(p.h_out + e, __ldcg(p.h_in + e));
@@ -223,8 +271,7 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
         const float inv = rsqrtf(warp_sum(ss) / (float)AB_C + p.eps);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float4 ga = reinterpret_cast<const float4 *>(p.g_in)[i * 64 + lane * 2];
-            const float4 gb = reinterpret_cast<const float4 *>(p.g_in)[i * 64 + lane * 2 + 1];
+            const float4 ga = gin[2 * i], gb = gin[2 * i + 1];
             const float4 a = v[2 * i], c = v[2 * i + 1];
             uint4 o;
             o.x = pack_bf16x2(a.x * inv * ga.x, a.y * inv * ga.y);
@@ -235,11 +282,12 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
         }
     }
     __syncthreads();
+    cluster.barrier_wait();  // (0) every CTA of the cluster runs
     bool ok = __syncthreads_and(mbar_wait_ctx(wbar, 0, p.err, lim));
-
-    // q/k/v rows: warp w takes rows 4w .. 4w+3 of this CTA's 32; every lane ends with the sums,
-    // and lanes 0..15 store them into the exchange buffer of CTA `lane` of the cluster
-    if (ok) {
+    // q/k/v rows: warp w takes rows 4w .. 4w+3 of each half (the first half from shared memory,
+    // the second from registers); every lane ends with the sums, and lanes 0..7 store them into
+    // the exchange buffer of CTA `lane` of the cluster
+    auto qkv_rows = [&](int half, auto wget) {
         float acc[4][NB];
 #pragma unroll
         for (int r = 0; r < 4; ++r)
@@ -252,7 +300,7 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
             for (int b = 0; b < NB; ++b) xv[b] = xs4[b * (AB_C / 8) + i * 32 + lane];
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
-                const uint4 wv = w4[(size_t)(warp * 4 + r) * (AB_C / 8) + i * 32 + lane];
+                const uint4 wv = wget(r, i);
 #pragma unroll
                 for (int b = 0; b < NB; ++b) acc[r][b] = dot8(wv, xv[b], acc[r][b]);
             }
@@ -266,17 +314,18 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
 #pragma unroll
             for (int b = 0; b < NB; ++b)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) dst[b * (AB_G + 2) * D + lr0 + warp * 4 + r] = acc[r][b];
+                for (int r = 0; r < 4; ++r) dst[b * (AB_G + 2) * D + lr0 + half * AB_HALF + warp * 4 + r] = acc[r][b];
         }
+    };
+    if (ok) qkv_rows(0, [&](int r, int i) { return w4[(size_t)(warp * 4 + r) * (AB_C / 8) + i * 32 + lane]; });
+    __syncthreads();  // every warp is done with the buffer: this CTA's o_proj rows go in
+    if (warp == 0) {
+        if (lane == 0) mbar_expect_tx(obar, AB_OROWS * AB_G * D * 2);
+        __syncwarp();
+        copy_split(w4, p.wog + ((size_t)g * AB_C + (size_t)rank * AB_OROWS) * AB_G * D, AB_OROWS * AB_G * D * 2, 4,
+                   obar, lane);
     }
-    __syncthreads();  // every warp is done with the q/k/v rows: the lower half of w takes o_proj
-    if (threadIdx.x == 0) {
-        mbar_expect_tx(obar, AB_OROWS * AB_G * D * 2);
-    }
-    __syncthreads();
-    if (warp == 0)
-        copy_rows(w4, p.wog + ((size_t)g * AB_C + (size_t)rank * AB_OROWS) * AB_G * D, AB_OROWS, AB_G * D * 2,
-                  obar, lane);
+    if (ok) qkv_rows(1, [&](int r, int i) { return wreg[r][i]; });
     cluster.sync();  // (1) every CTA's q/k/v rows have landed in every CTA
 
     // per-head RMSNorm + rotate-half RoPE: warp (b, h) for h in q_0, q_1, k, v; lane holds
@@ -291,11 +340,9 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
         if (h <= AB_G) {  // q heads and k: RMSNorm, then rotate
             float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
             const float inv = rsqrtf(warp_sum(ss) * (1.0f / D) + p.eps);
-            const float *gn = h < AB_G ? p.g_q : p.g_k;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) x[k] *= inv * __ldg(gn + lane + 32 * k);
-            const float2 c0 = __ldg(p.rope + (size_t)ps * (D / 2) + lane);
-            const float2 c1 = __ldg(p.rope + (size_t)ps * (D / 2) + lane + 32);
+            for (int k = 0; k < 4; ++k) x[k] *= inv * gain4[k];
+            const float2 c0 = cs0, c1 = cs1;
             const float r0 = x[0] * c0.x - x[2] * c0.y, r2 = x[2] * c0.x + x[0] * c0.y;
             const float r1 = x[1] * c1.x - x[3] * c1.y, r3 = x[3] * c1.x + x[1] * c1.y;
             x[0] = r0; x[1] = r1; x[2] = r2; x[3] = r3;
@@ -447,44 +494,48 @@ __global__ void __launch_bounds__(AB_WARPS * 32, 1) k_attn_block(AttnBlockParams
     __syncthreads();
     ok = __syncthreads_and(ok && mbar_wait_ctx(obar, 0, p.err, lim));
 
-    // o_proj: warp w takes output rows 8w .. 8w+7 of this CTA's 64; lane holds 8 of the 256
+    // o_proj: warp w takes output rows 16w .. 16w+15 of this CTA's 128; lane holds 8 of the 256
     // columns of the group (its two heads' outputs)
     if (ok) {
-        float acc2[8][NB];
+        float4 o0[NB], o1[NB];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const uint4 wv = w4[(size_t)(warp * 8 + r) * (AB_G * D / 8) + lane];
+        for (int b = 0; b < NB; ++b) {
+            o0[b] = reinterpret_cast<const float4 *>(obuf + b * AB_G * D)[lane * 2];
+            o1[b] = reinterpret_cast<const float4 *>(obuf + b * AB_G * D)[lane * 2 + 1];
+        }
+        float acc2[16][NB];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const uint4 wv = w4[(size_t)(warp * 16 + r) * (AB_G * D / 8) + lane];
+            const __nv_bfloat162 *pw = reinterpret_cast<const __nv_bfloat162 *>(&wv);
+            const float2 w0 = __bfloat1622float2(pw[0]), w1 = __bfloat1622float2(pw[1]);
+            const float2 w2 = __bfloat1622float2(pw[2]), w3 = __bfloat1622float2(pw[3]);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const float4 o0 = reinterpret_cast<const float4 *>(obuf + b * AB_G * D)[lane * 2];
-                const float4 o1 = reinterpret_cast<const float4 *>(obuf + b * AB_G * D)[lane * 2 + 1];
-                const __nv_bfloat162 *pw = reinterpret_cast<const __nv_bfloat162 *>(&wv);
-                const float2 w0 = __bfloat1622float2(pw[0]), w1 = __bfloat1622float2(pw[1]);
-                const float2 w2 = __bfloat1622float2(pw[2]), w3 = __bfloat1622float2(pw[3]);
-                float s = o0.x * w0.x;
-                s = fmaf(o0.y, w0.y, s);
-                s = fmaf(o0.z, w1.x, s);
-                s = fmaf(o0.w, w1.y, s);
-                s = fmaf(o1.x, w2.x, s);
-                s = fmaf(o1.y, w2.y, s);
-                s = fmaf(o1.z, w3.x, s);
-                s = fmaf(o1.w, w3.y, s);
+                float s = o0[b].x * w0.x;
+                s = fmaf(o0[b].y, w0.y, s);
+                s = fmaf(o0[b].z, w1.x, s);
+                s = fmaf(o0[b].w, w1.y, s);
+                s = fmaf(o1[b].x, w2.x, s);
+                s = fmaf(o1[b].y, w2.y, s);
+                s = fmaf(o1[b].z, w3.x, s);
+                s = fmaf(o1[b].w, w3.y, s);
                 acc2[r][b] = s;
             }
         }
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 16; ++r)
 #pragma unroll
             for (int b = 0; b < NB; ++b) acc2[r][b] = warp_sum(acc2[r][b]);
-        if (lane < 8 * NB) {
-            const int r = lane % 8, b = lane / 8;
+        if (lane < 16 * NB) {
+            const int r = lane % 16, b = lane / 16;
             float v = 0.0f;
 #pragma unroll
-            for (int rr = 0; rr < 8; ++rr)
+            for (int rr = 0; rr < 16; ++rr)
 #pragma unroll
                 for (int bb = 0; bb < NB; ++bb)
                     if (rr == r && bb == b) v = acc2[rr][bb];
-            atomicAdd(p.h_out + (size_t)b * AB_C + rank * AB_OROWS + warp * 8 + r, v);
+            atomicAdd(p.h_out + (size_t)b * AB_C + rank * AB_OROWS + warp * 16 + r, v);
         }
     }
     if (!ok && threadIdx.x == 0) {  // let every copy this CTA issued land before it exits
@@ -503,25 +554,28 @@ __global__ void __launch_bounds__(MLP_WARPS * 32, 1) k_mlp_block(MlpBlockParams 
     constexpr int C = KV * 256;
     constexpr int M = NB;
     cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
     const int NA = p.NA;
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
     uint4 *wgu = reinterpret_cast<uint4 *>(smem + 128);     // [2*NA][C/8]; later the partial sums
+    float *part = reinterpret_cast<float *>(wgu);           // [M][C], once the gate/up rows are done
     uint4 *wd = wgu + (size_t)2 * NA * (C / 8);             // [NA][C/8]
     uint4 *xs = wd + (size_t)NA * (C / 8);                  // [M][C/8]
     float *act = reinterpret_cast<float *>(xs + (size_t)M * (C / 8));  // [M][NA]
-    float *part = reinterpret_cast<float *>(wgu);           // [M][C], once the gate/up rows are done
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = (int)cluster.block_rank();
     const int a0 = blockIdx.x * NA;
     const int na = max(0, min(NA, p.I - a0));
     const long long lim = wait_limit(p.err);
     if (threadIdx.x == 0) mbar_init(bar, 1);
     __syncthreads();
+    pdl_trigger();  // the next attention block may launch (its early reads are final already)
     if (warp == 0) {
         if (lane == 0) mbar_expect_tx(bar, (uint32_t)na * 3 * C * 2);
         __syncwarp();
-        copy_rows(wgu, p.wgu + (size_t)2 * a0 * C, 2 * na, C * 2, bar, lane);
-        copy_rows(wd, p.wdt + (size_t)a0 * C, na, C * 2, bar, lane);
+        if (na > 0) {
+            copy_split(wgu, p.wgu + (size_t)2 * a0 * C, (uint32_t)na * 2 * C * 2, 4, bar, lane);
+            if (lane >= 4) copy_split(wd, p.wdt + (size_t)a0 * C, (uint32_t)na * C * 2, 2, bar, lane - 4);
+        }
     } else if (warp == 1 && lane == 0 && p.ahead_qkv) {
         // this CTA's share of the next layer's attention weights into L2
         const size_t qkv = (size_t)p.qkv_rows * C * 2, og = (size_t)p.og_cols * C * 2;
@@ -533,11 +587,15 @@ __global__ void __launch_bounds__(MLP_WARPS * 32, 1) k_mlp_block(MlpBlockParams 
             prefetch_l2(reinterpret_cast<const uint8_t *>(p.ahead_og) + (size_t)blockIdx.x * s_o,
                         (uint32_t)min(s_o, og - (size_t)blockIdx.x * s_o));
     }
+    float4 gpost[2 * KV];  // the post-attention norm's gains (warps 0 .. M-1), read before the wait
+    if (warp < M) {
+#pragma unroll
+        for (int i = 0; i < 2 * KV; ++i) gpost[i] = __ldg(reinterpret_cast<const float4 *>(p.gain) + i * 32 + lane);
+    }
     pdl_wait();
-    pdl_trigger();
-    {  // residual share into the output; the next attention block's output cleared
+    if (warp == MLP_WARPS - 1) {  // residual share into the output; the next attention block's output cleared
         const int per = (M * C + gridDim.x - 1) / gridDim.x;
-        for (int i = threadIdx.x; i < per; i += blockDim.x) {
+        for (int i = lane; i < per; i += 32) {
             const int e = blockIdx.x * per + i;
             if (e < M * C) {
                 atomicAdd(p.h_out + e, __ldcg(p.h_in + e));
@@ -558,7 +616,7 @@ __global__ void __launch_bounds__(MLP_WARPS * 32, 1) k_mlp_block(MlpBlockParams 
         uint2 *dst = reinterpret_cast<uint2 *>(xs + (size_t)warp * (C / 8));
 #pragma unroll
         for (int i = 0; i < 2 * KV; ++i) {
-            const float4 gv = reinterpret_cast<const float4 *>(p.gain)[i * 32 + lane];
+            const float4 gv = gpost[i];
             uint2 o;
             o.x = pack_bf16x2(v[i].x * inv * gv.x, v[i].y * inv * gv.y);
             o.y = pack_bf16x2(v[i].z * inv * gv.z, v[i].w * inv * gv.w);
@@ -591,11 +649,14 @@ __global__ void __launch_bounds__(MLP_WARPS * 32, 1) k_mlp_block(MlpBlockParams 
         }
     }
     __syncthreads();  // the gate/up rows are done: their space takes the partial sums
-    if (ok) {
+    // this CTA's share of the down projection (its act indices), 4 outputs per thread; the two
+    // CTAs of a cluster add their partial sums through distributed shared memory and each adds
+    // half of the row into the next residual with vector atomics (half the atomics)
 #pragma unroll
-        for (int b = 0; b < M; ++b) {  // this CTA's share of the down projection, 4 outputs per thread
-            const int n0 = threadIdx.x * 4;
-            float4 a4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int b = 0; b < M; ++b) {
+        const int n0 = threadIdx.x * 4;
+        float4 a4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (ok) {
             for (int j = 0; j < na; ++j) {
                 const float a = act[b * NA + j];
                 const uint2 w = *reinterpret_cast<const uint2 *>(reinterpret_cast<const bf16 *>(wd) + (size_t)j * C + n0);
@@ -606,30 +667,23 @@ __global__ void __launch_bounds__(MLP_WARPS * 32, 1) k_mlp_block(MlpBlockParams 
                 a4.z = fmaf(a, w23.x, a4.z);
                 a4.w = fmaf(a, w23.y, a4.w);
             }
-            reinterpret_cast<float4 *>(part + (size_t)b * C)[threadIdx.x] = a4;
         }
-    } else {
-        for (int i = threadIdx.x; i < M * C / 4; i += blockDim.x)
-            reinterpret_cast<float4 *>(part)[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        reinterpret_cast<float4 *>(part + (size_t)b * C)[threadIdx.x] = a4;
     }
-    cluster.sync();  // every CTA's partial sums are in its shared memory
-    // CTA `rank` adds up columns [rank * C/8, (rank+1) * C/8) of the cluster's 8 partials
-    for (int i = threadIdx.x; i < M * (C / MLP_CL) / 4; i += blockDim.x) {
-        const int b = i / ((C / MLP_CL) / 4), q = i % ((C / MLP_CL) / 4);
-        const int n = rank * (C / MLP_CL) + q * 4;
-        float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-        for (int r = 0; r < MLP_CL; ++r) {
-            const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(part, r) + (size_t)b * C + n);
-            s.x += v.x;
-            s.y += v.y;
-            s.z += v.z;
-            s.w += v.w;
+    cluster.sync();  // both partials are in place
+    {
+        const float *peer = cluster.map_shared_rank(part, rank ^ 1);
+        for (int i = threadIdx.x; i < M * (C / 2) / 4; i += blockDim.x) {
+            const int b = i / ((C / 2) / 4), n = rank * (C / 2) + (i % ((C / 2) / 4)) * 4;
+            const float4 u = *reinterpret_cast<const float4 *>(part + (size_t)b * C + n);
+            const float4 v = *reinterpret_cast<const float4 *>(peer + (size_t)b * C + n);
+            atomicAdd(reinterpret_cast<float4 *>(p.h_out + (size_t)b * C + n),
+                      make_float4(u.x + v.x, u.y + v.y, u.z + v.z, u.w + v.w));
         }
-        atomicAdd(reinterpret_cast<float4 *>(p.h_out + (size_t)b * C + n), s);
     }
-    if (!ok && threadIdx.x == 0) mbar_wait_bounded(bar, 0, nullptr);
-    cluster.sync();  // no CTA leaves while another may read its partial sums
+    cluster.barrier_arrive();  // done reading the peer's partial sums
+    if (!ok) mbar_wait_bounded(bar, 0, nullptr);  // let the copies land before the CTA exits
+    cluster.barrier_wait();    // the peer is done reading ours
 }
 
 template <int NB>
@@ -644,14 +698,11 @@ cudaError_t run_attn_block(const Launch &lc, const AttnBlockParams &p) {
 
 }  // namespace
 
-size_t attn_block_smem(int B) {
-    const AbLayout L(B);
-    return std::max(L.total, L.obuf + (size_t)B * AB_G * D * 4);
-}
+size_t attn_block_smem(int B) { return AbLayout(B).total; }
 
 int mlp_block_na(int I, int num_sms) { return (I + num_sms - 1) / num_sms; }
 
-// barrier, gate/up rows (later the partial sums [B][C] fp32), down rows, m [B][C] bf16, act [B][NA]
+// barrier, gate/up rows, down rows, m [B][C] bf16, act [B][NA]
 size_t mlp_block_smem(int B, int C, int I, int num_sms) {
     const int NA = mlp_block_na(I, num_sms);
     return 128 + (size_t)NA * 3 * C * 2 + (size_t)B * C * 2 + (size_t)B * NA * 4;
@@ -688,10 +739,18 @@ int attn_block_max_clusters(int Hkv) {
 bool decode_block_supported(int B, int C, int Hq, int Hkv, int head_dim, int I, int num_sms) {
     if (B < 1 || B > 2 || C != AB_C || head_dim != D || Hq != AB_G * Hkv || Hkv < 1 || Hkv > 64) return false;
     if (I % 256 || I > 4096) return false;
-    const int NA = mlp_block_na(I, num_sms);
-    if ((num_sms / MLP_CL) * MLP_CL * NA < I || NA < B) return false;  // the partial sums fit the gate/up rows
-    // one CTA of each kernel fits an SM together (228 KB, 1 KB reserved per CTA)
+
+    // one CTA of each kernel fits an SM together: shared memory (228 KB, 1 KB reserved per CTA)
+    // and registers (64 K)
     if (attn_block_smem(B) + mlp_block_smem(B, C, I, num_sms) + 2048 > 228 * 1024) return false;
+    cudaFuncAttributes fa, fm;
+    if (cudaFuncGetAttributes(&fa, B == 1 ? k_attn_block<1> : k_attn_block<2>) != cudaSuccess ||
+        cudaFuncGetAttributes(&fm, B == 1 ? k_mlp_block<1> : k_mlp_block<2>) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    auto regs = [](int per_thread, int threads) { return ((per_thread + 7) / 8 * 8) * threads; };
+    if (regs(fa.numRegs, AB_WARPS * 32) + regs(fm.numRegs, MLP_WARPS * 32) > 65536) return false;
     // and the device holds a cluster per KV head at once
     return (B == 1 ? attn_block_max_clusters<1>(Hkv) : attn_block_max_clusters<2>(Hkv)) >= Hkv;
 }
@@ -705,14 +764,13 @@ cudaError_t launch_attn_block(const Launch &lc, const AttnBlockParams &p) {
 cudaError_t launch_mlp_block(const Launch &lc, const MlpBlockParams &p0) {
     MlpBlockParams p = p0;
     p.NA = mlp_block_na(p.I, lc.num_sms);
-    const int grid = (lc.num_sms / MLP_CL) * MLP_CL;
-    if (p.C != 1024 || grid * p.NA < p.I) return cudaErrorInvalidValue;
+    if (p.C != 1024 || p.B < 1 || p.B > 2) return cudaErrorInvalidValue;
+    const int grid = ((p.I + p.NA - 1) / p.NA + 1) & ~1;  // pairs of CTAs
     const size_t smem = mlp_block_smem(p.B, p.C, p.I, lc.num_sms);
     auto kern = p.B == 1 ? k_mlp_block<1> : k_mlp_block<2>;
-    if (p.B < 1 || p.B > 2) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_cluster(lc, kern, dim3(grid), dim3(MLP_WARPS * 32), smem, dim3(MLP_CL, 1, 1), p);
+    return launch_cluster(lc, kern, dim3(grid), dim3(MLP_WARPS * 32), smem, dim3(2, 1, 1), p);
 }
 
 }  // namespace q3
