@@ -1,4 +1,4 @@
-// Decode of one or two rows as two kernels per layer: the attention block and the MLP block.
+// Decode of one row as two kernels per layer: the attention block and the MLP block.
 //
 // A decoder layer is h' = h + o_proj(attn(RMSNorm(h))), then out = h' + MLP(RMSNorm(h'))
 // ("手写Qwen3-0.6B推理", Qwen3DecoderLayer; "第 3 章 前向与生成（代码走读）", 3.2-3.4).  Each RMSNorm
@@ -7,25 +7,28 @@
 // between the two norms runs inside one kernel, with the KV-head groups as thread-block
 // clusters:
 //
-//   k_attn_block   grid (16, Hkv), cluster (16, 1, 1): cluster g = KV head g and its two query
+//   k_attn_block   grid (8, Hkv), cluster (8, 1, 1): cluster g = KV head g and its two query
 //                  heads ("手写Qwen3-0.6B推理", Attention: the K/V of a group shared by its query
-//                  heads).  CTA i of the cluster owns 32 of the group's 512 q/k/v weight rows,
-//                  the keys [i*per, (i+1)*per) of every row's sequence, and 64 of the 1024 o_proj
-//                  output rows.  Norm of h -> its q/k/v rows -> exchanged through distributed
-//                  shared memory -> per-head RMSNorm + rotate-half RoPE (+ the KV-cache write)
-//                  -> online softmax over its keys -> the 16 partial softmaxes merged through
-//                  distributed shared memory -> its o_proj rows, added into the next residual.
-//   k_mlp_block    grid 8k, cluster (8, 1, 1): CTA c owns act indices [c*NA, c*NA + NA): the
-//                  norm of h', its gate/up rows, SwiGLU, and its rows of the transposed down
-//                  weight (a split of the down projection over its reduction dimension); the
-//                  8 partial sums of a cluster are added through distributed shared memory,
-//                  then into the next residual with vector atomics.
+//                  heads).  CTA i of the cluster owns 64 of the group's 512 q/k/v weight rows (32
+//                  in shared memory, 32 in registers), the keys [i*per, (i+1)*per) of the row's
+//                  sequence, and 128 of the 1024 o_proj output rows.  Norm of h -> its q/k/v
+//                  rows -> exchanged through distributed shared memory -> per-head RMSNorm +
+//                  rotate-half RoPE (+ the KV-cache write) -> online softmax over its keys -> the
+//                  8 partial softmaxes merged through distributed shared memory -> its o_proj
+//                  rows, added into the next residual.
+//   k_mlp_block    grid of CTA pairs (clusters of 2): CTA c owns act indices [c*NA, c*NA + NA):
+//                  the norm of h', its gate/up rows, SwiGLU, and its rows of the transposed down
+//                  weight (a split of the down projection over its reduction dimension); a pair
+//                  adds its two partial sums through distributed shared memory, then each CTA
+//                  adds half of the row into the next residual with vector atomics.
 //
-// Both bulk-copy their weight rows (and the attention block its first cached K/V rows) into
-// shared memory before the dependency wait, and ask L2 for the other kernel's weights of the
-// layer, so HBM streams while the dependency chain runs.  Sized so that one CTA of each fits
-// an SM together (about 90 + 130 KB of shared memory): the next kernel's weights land while
-// the current one computes.
+// Sized for one CTA of each kernel on an SM together (about 88 + 131 KB of shared memory,
+// 168 + 88 registers a thread): each kernel lets the next one launch at its start, the next
+// one's CTAs take their place on the SMs as soon as the kernel before the current one leaves,
+// bulk-copy their weight rows (and the attention block its cached K/V rows) into shared memory
+// and ask L2 for the other kernel's weights of the layer -- all before their dependency wait --
+// so HBM streams while the dependency chain runs.  Clusters of 8 (and pairs) because this
+// GPU's GPCs hold 15 clusters of 8 but only 7 of 16 at one CTA per SM: all CTAs run in one wave.
 //
 // Residual buffers: three, rotating.  Layer l's attention block reads R[2l % 3] and adds into
 // R[(2l+1) % 3]; its MLP block reads that and adds into R[(2l+2) % 3].  A buffer something adds
