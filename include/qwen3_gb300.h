@@ -56,7 +56,7 @@ extern "C" {
 #define QWEN3_FLAG_NO_PDL 2u     /* launch kernels without programmatic dependent launch (for profilers) */
 #define QWEN3_FLAG_PERSISTENT 4u /* decode steps of up to 8 sequences as one persistent kernel
                                     (Qwen3-0.6B widths only; see qwen3_decode_step) */
-#define QWEN3_FLAG_DECODE_CHAIN 8u /* decode steps of 1-2 sequences as the four-kernel-per-layer
+#define QWEN3_FLAG_DECODE_CHAIN 8u /* decode steps of one sequence as the four-kernel-per-layer
                                       chain instead of two kernels per layer (see qwen3_decode_step) */
 
 /* Model and capacity.  Supported: head_dim == 128; n_q_heads a multiple of n_kv_heads with
@@ -157,9 +157,9 @@ int qwen3_prefill_append(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_
  * With QWEN3_FLAG_PERSISTENT, B <= 8 and the Qwen3-0.6B widths (hidden 1024, 16/8 heads,
  * head_dim 128) the whole step is one persistent kernel with one CTA per SM (cooperative
  * launch; it needs the whole GPU, so other work on the device waits for it).  Otherwise a
- * step of 1 or 2 sequences at hidden 1024, head_dim 128 and two query heads per KV head runs
- * each layer as two kernels (the attention block as clusters of 16 CTAs per KV head, then the
- * MLP block), unless QWEN3_FLAG_DECODE_CHAIN is set; other steps run four or more kernels per
+ * step of one sequence at hidden 1024, head_dim 128 and two query heads per KV head runs each
+ * layer as two kernels (the attention block as clusters of 8 CTAs per KV head, then the MLP
+ * block), unless QWEN3_FLAG_DECODE_CHAIN is set; other steps run four or more kernels per
  * layer.  Unless QWEN3_FLAG_NO_GRAPH is set, the step's kernels are recorded once per (B,
  * pointers, split plan) as a CUDA graph and replayed.  Errors: E_INVALID (NULL, B < 1,
  * repeated slot, slot never prefilled), E_CAPACITY (B > max_seqs, a slot already holding

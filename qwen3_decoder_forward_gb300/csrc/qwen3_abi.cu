@@ -225,7 +225,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
                                cudaMemcpyDeviceToDevice, lc.stream);
     };
 
-    // decode of 1-2 rows: two kernels per layer over three rotating residual buffers
+    // decode of one row: two kernels per layer over three rotating residual buffers
     const bool block = decode && !(k.flags & QWEN3_FLAG_DECODE_CHAIN) &&
                        decode_block_supported(R, C, Hq, Hkv, D, I, lc.num_sms);
     if (block) {

@@ -12,9 +12,9 @@ boundaries of the attention kernels:
    after the cache must see every cached key; a causal flag would hide all but the first);
  * decode batches of 2, 3, 5 and 9 sequences whose contexts cross the 16-key stages, the
    64-key chunks and the 128-key tiles (2^k - 1, 2^k, 2^k + 1), teacher-forced: every layer,
-   logits and token of every row of every step.  Two, three, five and nine rows take the
-   four decode paths (two kernels per layer up to 2 rows, fused MLP up to 4, separate gate/up
-   and down up to 8, tensor-core GEMV from 9).
+   logits and token of every row of every step.  One, three, five and nine rows take the four
+   decode paths (two kernels per layer for one row, fused MLP up to 4, separate gate/up and
+   down up to 8, tensor-core GEMV from 9).
 """
 
 import pytest
@@ -112,35 +112,36 @@ def test_one_token_prompt_decoded_from_position_1(model_weights):
     assert gate.tokens_checked + gate.tokens_skipped == 5
 
 
-def test_decode_two_rows_two_kernel_layer(model_weights):
-    # two rows take the two-kernel layer; 15, 16, 17 keys per CTA of a 16-CTA cluster around
-    # the 16-key stages, and a context ending on a stage boundary
+def test_decode_two_rows_around_stage_boundaries(model_weights):
+    # contexts 255..258 and 33..36: key ranges ending on and just past 16-key stages and 64-key
+    # chunks
     w, ow = model_weights
     _decode_batch(w, ow, [254, 32], 4, 250)
 
 
-def test_decode_two_rows_chain_matches_layer(model_weights):
-    """The same two-row steps on the four-kernel chain and on the two-kernel layer agree."""
+def test_decode_one_row_layer_matches_chain(model_weights):
+    """The same one-row steps (a 300-token prompt, seeded tokens fed) on the two-kernel layer
+    and on the four-kernel chain agree, both with CUDA graphs and kernel by kernel."""
     w, _ = model_weights
-    lengths, steps = [100, 300], 5
-    prompts = _prompts(lengths, 260)
+    prompt = _prompts([300], 260)[0]
     outs = []
-    for flags in (0, binding.QWEN3_FLAG_DECODE_CHAIN):
-        m = binding.Model(S, w, max_seqs=2, max_ctx=400, max_prefill_tokens=400, flags=flags)
-        nxt, _ = m.prefill(torch.cat(prompts).cuda(), lengths, [0, 1])
-        slots = torch.tensor([0, 1], dtype=torch.int32, device="cuda")
-        lg = torch.zeros(2, S.vocab, device="cuda")
+    for flags in (0, binding.QWEN3_FLAG_DECODE_CHAIN, binding.QWEN3_FLAG_NO_GRAPH):
+        m = binding.Model(S, w, max_seqs=1, max_ctx=320, max_prefill_tokens=300, flags=flags)
+        m.prefill(prompt.cuda(), [300], [0])
+        slots = torch.zeros(1, dtype=torch.int32, device="cuda")
+        lg = torch.zeros(1, S.vocab, device="cuda")
         got = []
-        for t in range(steps):  # the same seeded tokens fed to both paths
-            inp = synth.make_tokens(2, S.vocab, 270 + t).cuda()
-            out = torch.zeros(2, dtype=torch.int32, device="cuda")
-            m.decode_step(inp, slots, [0, 1], out, lg)
+        for t in range(6):
+            inp = synth.make_tokens(1, S.vocab, 270 + t).cuda()
+            out = torch.zeros(1, dtype=torch.int32, device="cuda")
+            m.decode_step(inp, slots, [0], out, lg)
             got.append(lg.cpu().numpy().copy())
         assert m.status() == 0
         m.close()
         outs.append(got)
-    for a, b in zip(*outs):
+    for a, b, c in zip(*outs):
         assert gc.rel_l2(a, b) <= 5e-3
+        assert gc.rel_l2(a, c) <= 1e-3
 
 
 def test_decode_three_rows_across_chunk_and_tile_boundaries(model_weights):
