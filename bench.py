@@ -218,7 +218,7 @@ def decode_positions(wl):
 class GpuRunner:
     """Holds the model and the device buffers of one replica and runs steps of the workload."""
 
-    def __init__(self, wl, device, flags=0, weights=None):
+    def __init__(self, wl, device, flags=0, weights=None, kv_block_tokens=0):
         import torch
         from qwen3_decoder_forward_gb300 import binding, synth
 
@@ -227,8 +227,12 @@ class GpuRunner:
         self.max_prefill = min(max(wl.lengths) if wl.n_seqs == 1 else 32768, wl.n_prompt_tokens)
         self.max_prefill = max(self.max_prefill, max(wl.lengths))
         w = weights if weights is not None else synth.make_weights(s)
+        pool = 0
+        if kv_block_tokens:  # a pool holding every slot at the workload's longest context
+            pool = wl.n_seqs * ((wl.max_ctx + kv_block_tokens - 1) // kv_block_tokens)
         self.model = binding.Model(s, w, max_seqs=wl.n_seqs, max_ctx=wl.max_ctx,
-                                   max_prefill_tokens=self.max_prefill, flags=flags, device=str(device))
+                                   max_prefill_tokens=self.max_prefill, flags=flags, device=str(device),
+                                   kv_block_tokens=kv_block_tokens, kv_pool_blocks=pool)
         del w
         prompts = wl.prompts()
         self.groups = chunk_prefills(wl.lengths, self.max_prefill)
@@ -646,13 +650,30 @@ def prefill_once_timed(torch, runner):
     return e0.elapsed_time(e1)
 
 
-def run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, weights=None, cpu=True):
+def step_roofline(wl, step_s, peaks, peak_kind, what):
+    """The whole step against its roofline: decode steps' HBM bytes, or a prefill's flops."""
+    if wl.decode_steps:
+        achieved = decode_step_bytes(wl) / (step_s / wl.decode_steps) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"kernel": f"whole decode step ({what})", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "algorithmic_bytes_per_step": int(decode_step_bytes(wl)),
+                "peak_source": _peak_source(peak_kind, "hbm_gbs")}
+    achieved = prefill_flops(wl) / step_s / 1e12
+    peak = float(peaks["bf16_tflops"])
+    return {"kernel": f"whole prefill ({what})", "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+            "algorithmic_flops_per_step": int(prefill_flops(wl)), "peak_source": _peak_source(peak_kind, "bf16_tflops")}
+
+
+def run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, weights=None, cpu=True,
+                 kv_block_tokens=0):
     """Runs one workload: warm-up, the timed steps, the end-to-end steps, the roofline kernel
     and (rank 0, one GPU) the CPU oracle sample.  Returns the fields of its JSON object."""
     import torch
     from qwen3_decoder_forward_gb300 import binding
 
-    runner = GpuRunner(wl, device, flags, weights)
+    runner = GpuRunner(wl, device, flags, weights, kv_block_tokens)
     units, unit = units_per_step(wl)
     out = {}
     if wl.decode_steps:
@@ -676,7 +697,11 @@ def run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, w
     runner.model.close()
     del runner
     torch.cuda.empty_cache()
-    roofline = roofline_for(torch, binding, wl, peaks, peak_kind)
+    if kv_block_tokens:  # the kernels read the cache through the block table: the whole step
+        roofline = step_roofline(wl, ms / 1e3 / args.steps, peaks, peak_kind,
+                                 f"paged KV cache, {kv_block_tokens}-token blocks")
+    else:
+        roofline = roofline_for(torch, binding, wl, peaks, peak_kind)
     torch.cuda.empty_cache()
     out.update({"value": units_all / (ms_max / 1e3), "unit": unit, "ms_per_step": ms_max / args.steps,
                 "units_per_step": units, "launches": launches, "clocks": clocks,
@@ -694,6 +719,150 @@ def run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, w
     rank = dist_env()[0]
     out["cpu_baseline"] = cpu_baseline(wl, unit) if (cpu and rank == 0 and world == 1) else None
     return out
+
+
+def run_prefill_chunked(args, device, flags, peaks, peak_kind, world, local_rank, weights):
+    """One 16,384-token prompt fed as chunks of 2,048 through qwen3_prefill (the first) and
+    qwen3_prefill_append (the rest), one step = the whole prompt; beside it the same prompt as
+    one qwen3_prefill call."""
+    import dataclasses
+    import torch
+    from qwen3_decoder_forward_gb300 import binding, synth
+
+    s = synth.QWEN3_0P6B
+    n, chunk = synth.CHUNKED_PROMPT, synth.CHUNKED_CHUNK
+    wl = synth.Workload("prefill_chunked", s, (n,), 0, synth.KV_FILL_SEED)
+    prompt = wl.prompts()[0]
+    prompt_d = prompt.to(device)
+    prompt_h = prompt.pin_memory()
+    m = binding.Model(s, weights, max_seqs=1, max_ctx=n, max_prefill_tokens=n, flags=flags, device=str(device))
+    nxt = torch.zeros(1, dtype=torch.int32, device=device)
+    nxt_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    stream = torch.cuda.current_stream(device)
+
+    def chunked(toks):
+        for c0 in range(0, n, chunk):
+            m.prefill(toks[c0: c0 + chunk], [min(chunk, n - c0)], [0], next_out=nxt, append=c0 > 0)
+
+    def whole(toks):
+        m.prefill(toks, [n], [0], next_out=nxt)
+
+    def timed(fn, steps):
+        for _ in range(max(args.warmup, 3)):
+            fn(prompt_d)
+        torch.cuda.synchronize()
+        n0 = binding.qwen3_launch_count(m.ctx)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn(prompt_d)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), binding.qwen3_launch_count(m.ctx) - n0
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    sampler.mark(True)
+    ms, launches = timed(chunked, args.steps)
+    sampler.mark(False)
+    sampler.stop()
+    ms_whole, _ = timed(whole, args.steps)
+    # end to end: the prompt copied in from pinned host memory, the next token read back
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        toks = torch.empty_like(prompt_h, device=device)
+        toks.copy_(prompt_h, non_blocking=True)
+        chunked(toks)
+        nxt_h.copy_(nxt, non_blocking=True)
+        stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    assert m.status() == 0, binding.qwen3_last_error(m.ctx)
+    m.close()
+    step_s = ms / 1e3 / args.steps
+    flops = prefill_flops(wl) + 2 * s.hidden * s.vocab * (n // chunk - 1)  # one head row per chunk
+    return {"workload": (f"prefill_chunked: one {n}-token prompt (28-layer Qwen3-0.6B shape) as {n // chunk} chunks of "
+                         f"{chunk} (prefill, then prefill_append)"),
+            "value": n * args.steps / (ms / 1e3), "unit": "tokens/s", "ms_per_step": step_s * 1e3,
+            "launches": launches, "clocks": dict(sampler.summary(), retried=False),
+            "e2e": {"value": round(n * args.steps / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": n * 4 + 16,
+                    "d2h_bytes_per_step": 4},
+            "roofline": step_roofline(dataclasses.replace(wl), step_s, peaks, peak_kind, "8 chunk calls")
+            | {"algorithmic_flops_per_step": int(flops), "achieved": round(flops / step_s / 1e12, 1),
+               "frac": round(flops / step_s / 1e12 / float(peaks["bf16_tflops"]), 4)},
+            "one_call": {"ms": round(ms_whole / args.steps, 3), "tokens_s": round(n * args.steps / (ms_whole / 1e3), 1)},
+            "chunking_cost": round(ms / ms_whole, 3)}
+
+
+def run_engine_mixed(args, device, flags, peaks, peak_kind, world, local_rank, weights):
+    """48 requests through the continuous-batching engine, one step = submit all, run to the
+    last one's end.  Units: generated tokens (prompt tokens reported beside them)."""
+    import torch
+    from qwen3_decoder_forward_gb300 import binding, synth
+
+    s = synth.QWEN3_0P6B
+    reqs = synth.engine_requests(s.vocab)
+    max_ctx = 2048 + 128
+    m = binding.Model(s, weights, max_seqs=synth.ENGINE_SLOTS, max_ctx=max_ctx,
+                      max_prefill_tokens=synth.ENGINE_BUDGET, flags=flags, device=str(device))
+    eng = binding.Engine(m, token_budget=synth.ENGINE_BUDGET)
+    gen_tokens = sum(n for _, n in reqs)
+    prompt_tokens = sum(int(p.numel()) for p, _ in reqs)
+    lists = [(p.tolist(), n) for p, n in reqs]
+    rid = [0]
+
+    def one_step():
+        ids = []
+        for prompt, n in lists:
+            rid[0] += 1
+            eng.submit(rid[0], prompt, n)
+            ids.append(rid[0])
+        steps = eng.run()
+        got = 0
+        for i in ids:
+            toks, why = eng.result(i)
+            got += len(toks)
+            eng.forget(i)
+        return steps, got
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        one_step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    sampler.mark(True)
+    n0 = binding.qwen3_launch_count(m.ctx)
+    st0 = eng.stats()
+    t0 = time.perf_counter()
+    steps_total = 0
+    K = max(1, min(args.steps, 3))
+    for _ in range(K):
+        st, got = one_step()
+        steps_total += st
+        assert got == gen_tokens, (got, gen_tokens)
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    sampler.mark(False)
+    sampler.stop()
+    st1 = eng.stats()
+    launches = binding.qwen3_launch_count(m.ctx) - n0
+    assert m.status() == 0, binding.qwen3_last_error(m.ctx)
+    eng.close()
+    m.close()
+    return {"workload": (f"engine_mixed: {len(reqs)} requests (28-layer Qwen3-0.6B shape), prompts uniform in "
+                         f"[256, 2048] tokens ({prompt_tokens} in all), 16..128 new tokens each ({gen_tokens} in all), "
+                         f"{synth.ENGINE_SLOTS} slots, {synth.ENGINE_BUDGET} tokens a step"),
+            "value": gen_tokens * K / dt, "unit": "tokens/s", "ms_per_step": dt * 1e3 / K,
+            "launches": launches, "clocks": dict(sampler.summary(), retried=False),
+            "e2e": {"value": round(gen_tokens * K / dt, 2), "unit": "tokens/s",
+                    "h2d_bytes_per_step": prompt_tokens * 4, "d2h_bytes_per_step": gen_tokens * 4},
+            "prompt_tokens_s": round(prompt_tokens * K / dt, 1),
+            "engine_steps_per_run": steps_total / K,
+            "mixed_steps": (st1["mixed_steps"] - st0["mixed_steps"]) / K,
+            "decode_steps": (st1["decode_steps"] - st0["decode_steps"]) / K,
+            "roofline": None}
 
 
 def gpu_arm(args, wl):
@@ -719,6 +888,8 @@ def gpu_arm(args, wl):
         if rank == 0:
             print(json.dumps({"roofline_only": True, "workload": wl.name, "roofline": r}), flush=True)
         return 0
+    if args.workload in synth.EXTRA_WORKLOADS:
+        return gpu_extra(args, wl, device, flags, peaks, peak_kind, world, local_rank)
 
     weights = synth.make_weights(wl.shape)
     main = run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, weights,
@@ -772,10 +943,54 @@ def gpu_arm(args, wl):
     return 0
 
 
+def gpu_extra(args, wl, device, flags, peaks, peak_kind, world, local_rank):
+    """The lines of the feature workloads: chunked prefill, decode over a paged KV cache, and the
+    continuous-batching engine."""
+    from qwen3_decoder_forward_gb300 import synth
+
+    rank = dist_env()[0]
+    weights = synth.make_weights(synth.QWEN3_0P6B)
+    extra = {}
+    if args.workload == "decode_long_paged":
+        res = run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, weights,
+                           cpu=not args.no_cpu_baseline, kv_block_tokens=synth.PAGED_BLOCK_TOKENS)
+        desc = workload_desc(wl) + f"; paged KV cache of {synth.PAGED_BLOCK_TOKENS}-token blocks"
+        extra = {"breakdown": {k: res[k] for k in ("kv_fill", "decode_step_hbm_frac", "decode_step_bytes")}}
+    elif args.workload == "prefill_chunked":
+        res = run_prefill_chunked(args, device, flags, peaks, peak_kind, world, local_rank, weights)
+        desc = res["workload"]
+        extra = {"one_call": res["one_call"], "chunking_cost": res["chunking_cost"]}
+    else:
+        res = run_engine_mixed(args, device, flags, peaks, peak_kind, world, local_rank, weights)
+        desc = res["workload"]
+        extra = {k: res[k] for k in ("prompt_tokens_s", "engine_steps_per_run", "mixed_steps", "decode_steps")}
+    import torch
+    ms_all = res["ms_per_step"] * args.steps
+    ms_max, units_all = reduce_over_ranks(torch, world, ms_all, res["value"] * ms_all / 1e3)
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(units_all / (ms_max / 1e3), 2), "unit": res["unit"],
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(res["ms_per_step"], 4), "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded random-init bf16 weights N(0,0.02), gains 1+N(0,0.05), uniform token ids)",
+                "config": {"workload": desc, "replicas": world, "launch": args.launch},
+                "clocks": res["clocks"], "e2e": res["e2e"], "gpu_launches": int(res["launches"]),
+                "roofline": res["roofline"], "cpu_baseline": res.get("cpu_baseline")}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     from qwen3_decoder_forward_gb300 import synth
-    wl = synth.WORKLOADS[args.workload]
+    # the feature workloads time the workload they extend in the reference arm
+    base = {"decode_long_paged": "decode_long", "prefill_chunked": "prefill_long",
+            "engine_mixed": "decode_b32"}.get(args.workload, args.workload)
+    if base == "prefill_long":
+        wl = synth.Workload("prefill_long", synth.QWEN3_0P6B, (synth.CHUNKED_PROMPT,), 0, synth.KV_FILL_SEED)
+    else:
+        wl = synth.WORKLOADS[base]
     if args.decode_steps is not None:
         import dataclasses
         wl = dataclasses.replace(wl, name=f"{wl.name} (decode steps {args.decode_steps})",

@@ -203,3 +203,26 @@ WORKLOADS = {
     # 16 sequences, 16384-token prompts (the KV fill), then 32 steps
     "decode_long": Workload("decode_long", QWEN3_0P6B, (16384,) * 16, 32, KV_FILL_SEED),
 }
+
+# Workloads of the features beyond the plain forward, each measured with its own runner:
+#  - prefill_chunked: one 16,384-token prompt fed as 8 chunks of 2,048 (the first a prefill,
+#    the others prefill_append calls continuing the slot);
+#  - decode_long_paged: decode_long over a paged KV cache of 256-token blocks;
+#  - engine_mixed: 48 requests through the continuous-batching engine, prompts uniform in
+#    [256, 2048] tokens and 16..128 new tokens each (seed ENGINE_SEED), 16 slots, 2,048 tokens
+#    a step.
+CHUNKED_PROMPT = 16384
+CHUNKED_CHUNK = 2048
+PAGED_BLOCK_TOKENS = 256
+ENGINE_SEED = 4
+ENGINE_REQUESTS = 48
+ENGINE_SLOTS = 16
+ENGINE_BUDGET = 2048
+EXTRA_WORKLOADS = ("prefill_chunked", "decode_long_paged", "engine_mixed")
+
+
+def engine_requests(vocab: int, n: int = ENGINE_REQUESTS, seed: int = ENGINE_SEED):
+    """(prompt int32 tensor, max_new_tokens) of each request of engine_mixed."""
+    lengths = make_lengths(n, 256, 2048, seed)
+    new = make_lengths(n, 16, 128, seed + 1)
+    return [(make_tokens(L, vocab, seed + 100 + 7919 * i), m) for i, (L, m) in enumerate(zip(lengths, new))]
