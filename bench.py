@@ -44,10 +44,11 @@ L2_BYTES = 129 * 2 ** 20
 # capture of the current kernel exists.  The fused decode MLP at one row reads exactly its
 # 18.9 MB of weights; the prefill gate_up GEMM at 23,460 rows reads A (48 MB) and W (12.6 MB)
 # once and writes 86 MB of its 144 MB output before it ends (the rest leaves L2 later).
-# "attn_decode_per_key_row": bytes per (sequence, position) row of one layer's K and V that a
-# decode attention launch reads, measured on a smaller case and scaled by the rows a launch
-# reads (the traffic grows in proportion).
-TRAFFIC_BYTES = {"gemm_gate_up": 147362304, "mlp_fused": 18910976, "attn_decode_per_key_row": None}
+# "attn_decode_per_key_row": DRAM bytes per (sequence, position) row of one layer's K and V of a
+# decode attention launch, measured at 16 rows x 4,097 positions (268.9 MB per launch against
+# 268.5 MB of K/V rows: 4,102 B a row for 4,096 algorithmic) and scaled by the rows a launch
+# reads (the traffic grows in proportion with the rows).
+TRAFFIC_BYTES = {"gemm_gate_up": 147362304, "mlp_fused": 18910976, "attn_decode_per_key_row": 4102.3}
 
 
 def parse_args():

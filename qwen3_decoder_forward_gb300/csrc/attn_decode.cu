@@ -70,6 +70,10 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
         reinterpret_cast<float(*)[ATTN_DECODE_MAX_SPLIT]>(ring + NW * G * (D + 2) * 4);  // [G]
     __shared__ float s_lsum[G];
     __shared__ int s_last;
+    // paged cache: the block-table entries of this CTA's key range, read once before the first
+    // copy (a lookup per copy would put an L2 round trip in front of every refill of the ring)
+    constexpr int MAX_BLK = PAGED ? 1024 : 1;
+    __shared__ int32_t s_blk[MAX_BLK];
 
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int n_split = gridDim.x;
@@ -88,6 +92,17 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
     const int n_chunks = (cache_end - k_begin + CHUNK - 1) / CHUNK;
     KvMap kv = r.kv;
     if (!PAGED) kv.table = nullptr;  // the contiguous form compiles to plain slot-major offsets
+    const int blk0 = PAGED ? k_begin / kv.bs : 0;
+    const bool blk_cached = PAGED && cache_end > k_begin && (cache_end - 1) / kv.bs - blk0 < MAX_BLK;
+    if (blk_cached) {
+        for (int i = blk0 + threadIdx.x; i <= (cache_end - 1) / kv.bs; i += blockDim.x)
+            s_blk[i - blk0] = __ldcg(kv.table + (size_t)slot * kv.max_blocks + i);
+        __syncthreads();
+    }
+    auto cache_row = [&](int p) -> size_t {  // row of position p (< cache_end) of (slot, g)
+        if (blk_cached) return ((size_t)s_blk[p / kv.bs - blk0] * Hkv + g) * kv.bs + p % kv.bs;
+        return kv_row(kv, slot, Hkv, g, max_ctx, p);
+    };
     auto issue = [&](int c) {  // chunk c of this split into stage c % STAGES
         const int st = c % STAGES;
         const int j0 = k_begin + c * CHUNK;
@@ -98,7 +113,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_fused(
         for (int done = 0; done < n;) {
             const int p = j0 + done;
             const int run = PAGED ? min(n - done, kv.bs - p % kv.bs) : n - done;
-            const size_t row = kv_row(kv, slot, Hkv, g, max_ctx, p);
+            const size_t row = cache_row(p);
             const uint32_t bytes = (uint32_t)run * D * 2;
             bulk_g2s(ring + st * STAGE_BYTES + (size_t)done * D * 2, k_layer + row * D, bytes, &full[st]);
             bulk_g2s(ring + st * STAGE_BYTES + CHUNK * D * 2 + (size_t)done * D * 2, v_layer + row * D, bytes,
