@@ -273,8 +273,9 @@ int qwen3_truncate_slot(qwen3_ctx *ctx, int32_t slot, int32_t length, void *stre
  * last row; it finishes on its eos_id (kept as its last token), after max_new_tokens
  * tokens, or when its slot is full, and its slot is released for the waiting requests.
  * The step synchronises `stream` once, to read the next tokens.
- * The engine owns every slot of the context while it exists, and leaves the context's
- * sampling setting off (a context with qwen3_set_sampling on makes the steps fail). */
+ * The engine owns every slot of the context, and its sampling setting, while it exists: a step
+ * with a sampling request (qwen3_engine_submit_sampled) sets the per-row settings for that call
+ * and clears them after it. */
 typedef struct qwen3_engine qwen3_engine;
 
 #define QWEN3_FINISH_NONE 0     /* waiting or running */
@@ -312,6 +313,18 @@ int qwen3_engine_step(qwen3_engine *e, void *stream, int32_t *n_finished);
 
 /* Requests submitted and not finished. */
 int32_t qwen3_engine_unfinished(const qwen3_engine *e);
+
+/* qwen3_engine_submit for a request that samples ("第 3 章", 4.3 Sampler): its tokens are drawn
+ * by the rule of qwen3_sample with this temperature, top_k and top_p (temperature <= 0: greedy,
+ * as qwen3_engine_submit).  The uniform draw of its t-th generated token (t = 0, 1, ...) is
+ * output t + 1 of the SplitMix64 generator started at state `seed` (state += 0x9E3779B97F4A7C15;
+ * z = state; z = (z ^ z>>30) * 0xBF58476D1CE4E5B9; z = (z ^ z>>27) * 0x94D049BB133111EB;
+ * z ^= z>>31), taken as (z >> 40) / 2^24, so a request's tokens depend only on its own
+ * settings and seed, not on what it was batched with.  Errors: those of qwen3_engine_submit,
+ * E_INVALID for a NaN temperature or top_p. */
+int qwen3_engine_submit_sampled(qwen3_engine *e, int64_t request_id, const int32_t *prompt_host,
+                                int32_t prompt_len, int32_t max_new_tokens, int32_t eos_id, float temperature,
+                                int32_t top_k, float top_p, uint64_t seed);
 
 /* Tokens generated so far for request_id (up to capacity of them into tokens_host, which may
  * be NULL when capacity is 0), their count and the finish reason (QWEN3_FINISH_*).

@@ -107,6 +107,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_engine_workspace_bytes": (sz, [_P, i32]),
         "qwen3_engine_create": (ctypes.c_int, [_P, i32, _P, sz, ctypes.POINTER(_P)]),
         "qwen3_engine_submit": (ctypes.c_int, [_P, i64, pi32, i32, i32, i32]),
+        "qwen3_engine_submit_sampled": (ctypes.c_int, [_P, i64, pi32, i32, i32, i32, ctypes.c_float, i32,
+                                                       ctypes.c_float, ctypes.c_uint64]),
         "qwen3_engine_step": (ctypes.c_int, [_P, _P, pi32]),
         "qwen3_engine_unfinished": (i32, [_P]),
         "qwen3_engine_result": (ctypes.c_int, [_P, i64, pi32, i32, pi32, pi32]),
@@ -238,6 +240,13 @@ def qwen3_engine_create(ctx, token_budget: int, workspace_ptr: int, nbytes: int)
 def qwen3_engine_submit(eng, request_id: int, prompt: Sequence[int], max_new_tokens: int, eos_id: int = -1):
     _engine_check(load_library().qwen3_engine_submit(eng, request_id, _i32_array(prompt), len(prompt),
                                                      max_new_tokens, eos_id), eng)
+
+
+def qwen3_engine_submit_sampled(eng, request_id: int, prompt: Sequence[int], max_new_tokens: int, eos_id: int,
+                                temperature: float, top_k: int, top_p: float, seed: int):
+    _engine_check(load_library().qwen3_engine_submit_sampled(eng, request_id, _i32_array(prompt), len(prompt),
+                                                             max_new_tokens, eos_id, temperature, top_k, top_p,
+                                                             seed), eng)
 
 
 def qwen3_engine_step(eng, stream: int = 0) -> int:
@@ -531,8 +540,14 @@ class Engine:
         ptr = (self.ws.data_ptr() + 255) // 256 * 256
         self.eng = qwen3_engine_create(model.ctx, token_budget, ptr, nbytes)
 
-    def submit(self, request_id: int, prompt: Sequence[int], max_new_tokens: int, eos_id: int = -1):
-        qwen3_engine_submit(self.eng, request_id, [int(t) for t in prompt], max_new_tokens, eos_id)
+    def submit(self, request_id: int, prompt: Sequence[int], max_new_tokens: int, eos_id: int = -1,
+               temperature: float = 0.0, top_k: int = 0, top_p: float = 1.0, seed: int = 0):
+        """Queues a request; a positive temperature makes it sample (qwen3_engine_submit_sampled)."""
+        if temperature > 0:
+            qwen3_engine_submit_sampled(self.eng, request_id, [int(t) for t in prompt], max_new_tokens, eos_id,
+                                        temperature, top_k, top_p, seed)
+        else:
+            qwen3_engine_submit(self.eng, request_id, [int(t) for t in prompt], max_new_tokens, eos_id)
 
     def step(self) -> int:
         return qwen3_engine_step(self.eng, self.model._stream())

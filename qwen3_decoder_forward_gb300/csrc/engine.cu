@@ -10,6 +10,11 @@
 // A step whose rows are all single generated tokens runs as one decode step (GEMV kernels and
 // the per-batch-size CUDA graphs); any prompt chunk makes it one prefill_append call over all
 // rows, where a generated token is a one-token chunk at its slot's length.
+//
+// A request may sample instead of taking the greedy token ("第 3 章", 4.3 Sampler: temperature
+// and Top-k / Top-p): a step with such a row sets the context's per-row sampling arrays for
+// that call (greedy rows get temperature 0), with the uniform draw of the request's t-th token
+// taken from its seed by a counter-based generator (below), so a run is reproducible.
 
 #include <cuda_runtime.h>
 
@@ -29,28 +34,54 @@ constexpr size_t WS_ALIGN = 256;
 size_t ws_align(size_t x) { return (x + WS_ALIGN - 1) / WS_ALIGN * WS_ALIGN; }
 
 struct WsLayout {
-    size_t tokens = 0, cu = 0, slots = 0, next = 0, total = 0;
+    size_t tokens = 0, cu = 0, slots = 0, next = 0, temp = 0, topk = 0, topp = 0, unif = 0, logits = 0, total = 0;
 };
 
 WsLayout ws_layout(const qwen3_config &cfg, int budget) {
     WsLayout w;
     size_t off = 0;
+    const size_t rows = (size_t)cfg.max_seqs * 4;
     w.tokens = off;
     off = ws_align(off + (size_t)budget * 4);
     w.cu = off;
     off = ws_align(off + (size_t)(cfg.max_seqs + 1) * 4);
     w.slots = off;
-    off = ws_align(off + (size_t)cfg.max_seqs * 4);
+    off = ws_align(off + rows);
     w.next = off;
-    off = ws_align(off + (size_t)cfg.max_seqs * 4);
+    off = ws_align(off + rows);
+    // per-row sampling settings of one call and the logits they draw from
+    w.temp = off;
+    off = ws_align(off + rows);
+    w.topk = off;
+    off = ws_align(off + rows);
+    w.topp = off;
+    off = ws_align(off + rows);
+    w.unif = off;
+    off = ws_align(off + rows);
+    w.logits = off;
+    off = ws_align(off + (size_t)cfg.max_seqs * cfg.vocab * 4);
     w.total = off;
     return w;
+}
+
+// The uniform draw of token t of a request with seed s: output t + 1 of the SplitMix64
+// generator (Steele, Lea and Flood, "Fast splittable pseudorandom number generators", 2014)
+// started at state s, its top 24 bits scaled to [0, 1) (exact in fp32).
+float uniform_draw(uint64_t seed, int64_t t) {
+    uint64_t z = seed + (uint64_t)(t + 1) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return (float)(z >> 40) * (1.0f / 16777216.0f);
 }
 
 struct Request {
     int64_t id = 0;
     std::vector<int32_t> prompt;
     int32_t max_new = 0, eos = -1;
+    float temperature = 0.0f, top_p = 1.0f;  // temperature <= 0: greedy
+    int32_t top_k = 0;
+    uint64_t seed = 0;
     int32_t slot = -1;
     int32_t consumed = 0;  // prompt tokens already run
     std::vector<int32_t> out;
@@ -78,7 +109,8 @@ struct qwen3_engine {
     qwen3_engine_stats stats = {};
     std::string err;
     // host staging of one step
-    std::vector<int32_t> h_tokens, h_cu, h_slots, h_next;
+    std::vector<int32_t> h_tokens, h_cu, h_slots, h_next, h_topk;
+    std::vector<float> h_temp, h_topp, h_unif;
 
     int fail(int code, const std::string &m) {
         err = m;
@@ -129,7 +161,16 @@ int qwen3_engine_create(qwen3_ctx *ctx, int32_t token_budget, void *workspace_de
 
 int qwen3_engine_submit(qwen3_engine *e, int64_t request_id, const int32_t *prompt_host, int32_t prompt_len,
                         int32_t max_new_tokens, int32_t eos_id) {
+    return qwen3_engine_submit_sampled(e, request_id, prompt_host, prompt_len, max_new_tokens, eos_id, 0.0f, 0, 1.0f,
+                                       0);
+}
+
+int qwen3_engine_submit_sampled(qwen3_engine *e, int64_t request_id, const int32_t *prompt_host, int32_t prompt_len,
+                                int32_t max_new_tokens, int32_t eos_id, float temperature, int32_t top_k, float top_p,
+                                uint64_t seed) {
     if (!e) return QWEN3_E_INVALID;
+    if (!(temperature == temperature) || !(top_p == top_p))
+        return e->fail(QWEN3_E_INVALID, "qwen3_engine_submit: temperature or top_p is NaN");
     if (!prompt_host || prompt_len < 1 || max_new_tokens < 1)
         return e->fail(QWEN3_E_INVALID, "qwen3_engine_submit: empty prompt or max_new_tokens < 1");
     if (prompt_len > e->cfg.max_ctx) return e->fail(QWEN3_E_CAPACITY, "qwen3_engine_submit: prompt longer than max_ctx");
@@ -139,6 +180,10 @@ int qwen3_engine_submit(qwen3_engine *e, int64_t request_id, const int32_t *prom
     r->prompt.assign(prompt_host, prompt_host + prompt_len);
     r->max_new = max_new_tokens;
     r->eos = eos_id;
+    r->temperature = temperature;
+    r->top_k = top_k;
+    r->top_p = top_p;
+    r->seed = seed;
     e->waiting.push_back(r.get());
     e->requests.emplace(request_id, std::move(r));
     return QWEN3_OK;
@@ -189,12 +234,22 @@ int qwen3_engine_step(qwen3_engine *e, void *stream, int32_t *n_finished) {
     }
 
     const int32_t B = (int32_t)rows.size();
-    bool mixed = false;
+    bool mixed = false, sampled = false;
     e->h_tokens.clear();
     e->h_cu.assign(1, 0);
     e->h_slots.clear();
+    e->h_temp.clear();
+    e->h_topk.clear();
+    e->h_topp.clear();
+    e->h_unif.clear();
     for (const Row &w : rows) {
         Request *r = w.req;
+        // the draw of the token this row produces (index = tokens generated so far)
+        sampled = sampled || r->temperature > 0.0f;
+        e->h_temp.push_back(r->temperature);
+        e->h_topk.push_back(r->top_k);
+        e->h_topp.push_back(r->top_p);
+        e->h_unif.push_back(uniform_draw(r->seed, (int64_t)r->out.size()));
         if (w.generated) {
             e->h_tokens.push_back(r->out.back());
         } else {
@@ -213,18 +268,38 @@ int qwen3_engine_step(qwen3_engine *e, void *stream, int32_t *n_finished) {
     if (ce == cudaSuccess) ce = cudaMemcpyAsync(d_slots, e->h_slots.data(), (size_t)B * 4, cudaMemcpyHostToDevice, st);
     if (ce == cudaSuccess && mixed)
         ce = cudaMemcpyAsync(d_cu, e->h_cu.data(), (size_t)(B + 1) * 4, cudaMemcpyHostToDevice, st);
+    qwen3_sampling sp = {};
+    float *d_logits = nullptr;
+    if (sampled) {  // this call draws: per-row settings (greedy rows have temperature 0)
+        sp.temperature = reinterpret_cast<float *>(e->ws + e->lay.temp);
+        sp.top_k = reinterpret_cast<int32_t *>(e->ws + e->lay.topk);
+        sp.top_p = reinterpret_cast<float *>(e->ws + e->lay.topp);
+        sp.uniform = reinterpret_cast<float *>(e->ws + e->lay.unif);
+        d_logits = reinterpret_cast<float *>(e->ws + e->lay.logits);
+        if (ce == cudaSuccess)
+            ce = cudaMemcpyAsync((void *)sp.temperature, e->h_temp.data(), (size_t)B * 4, cudaMemcpyHostToDevice, st);
+        if (ce == cudaSuccess)
+            ce = cudaMemcpyAsync((void *)sp.top_k, e->h_topk.data(), (size_t)B * 4, cudaMemcpyHostToDevice, st);
+        if (ce == cudaSuccess)
+            ce = cudaMemcpyAsync((void *)sp.top_p, e->h_topp.data(), (size_t)B * 4, cudaMemcpyHostToDevice, st);
+        if (ce == cudaSuccess)
+            ce = cudaMemcpyAsync((void *)sp.uniform, e->h_unif.data(), (size_t)B * 4, cudaMemcpyHostToDevice, st);
+    }
     if (ce != cudaSuccess) return e->cuda_fail(ce, "qwen3_engine_step: upload");
-    int rc;
+    int rc = qwen3_set_sampling(e->ctx, sampled ? &sp : nullptr);
+    if (rc != QWEN3_OK) return e->ctx_fail(rc, "qwen3_engine_step: set_sampling");
     if (mixed) {
-        rc = qwen3_prefill_append(e->ctx, d_tokens, d_cu, e->h_cu.data(), d_slots, e->h_slots.data(), B, nullptr,
+        rc = qwen3_prefill_append(e->ctx, d_tokens, d_cu, e->h_cu.data(), d_slots, e->h_slots.data(), B, d_logits,
                                   d_next, stream);
         if (rc != QWEN3_OK) return e->ctx_fail(rc, "qwen3_engine_step: prefill_append");
         ++e->stats.mixed_steps;
     } else {
-        rc = qwen3_decode_step(e->ctx, d_tokens, d_slots, e->h_slots.data(), B, nullptr, d_next, stream);
+        rc = qwen3_decode_step(e->ctx, d_tokens, d_slots, e->h_slots.data(), B, d_logits, d_next, stream);
         if (rc != QWEN3_OK) return e->ctx_fail(rc, "qwen3_engine_step: decode_step");
         ++e->stats.decode_steps;
     }
+    if (sampled && (rc = qwen3_set_sampling(e->ctx, nullptr)) != QWEN3_OK)
+        return e->ctx_fail(rc, "qwen3_engine_step: set_sampling");
     ++e->stats.steps;
     e->h_next.resize(B);
     ce = cudaMemcpyAsync(e->h_next.data(), d_next, (size_t)B * 4, cudaMemcpyDeviceToHost, st);

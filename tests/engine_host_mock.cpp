@@ -20,6 +20,7 @@
 
 struct qwen3_ctx {
     qwen3_config cfg;
+    qwen3_sampling sampling = {};            // as set by qwen3_set_sampling ("device" = host arrays)
     std::vector<std::vector<int32_t>> hist;  // tokens cached per slot
     std::vector<int32_t> log;                // see mock_log
     std::string err;
@@ -31,13 +32,29 @@ struct qwen3_ctx {
 
 namespace {
 
-int32_t next_token(const std::vector<int32_t> &h, int32_t vocab) {
+uint64_t fnv(const std::vector<int32_t> &h) {
     uint64_t x = 14695981039346656037ull;
     for (int32_t t : h) {
         x ^= (uint64_t)(uint32_t)t;
         x *= 1099511628211ull;
     }
-    return (int32_t)(x % (uint64_t)vocab);
+    return x;
+}
+
+int32_t next_token(const std::vector<int32_t> &h, int32_t vocab) { return (int32_t)(fnv(h) % (uint64_t)vocab); }
+
+// Row b's next token: greedy (the hash) unless the call samples and the row's temperature is
+// positive; then the hash mixed with the row's uniform draw (a multiple of 2^-24) and settings,
+// so a test can tell whether each row got its own draw and settings.
+int32_t row_token(const qwen3_ctx *c, const std::vector<int32_t> &h, int b) {
+    const qwen3_sampling &s = c->sampling;
+    if (!s.temperature || !(s.temperature[b] > 0.0f)) return next_token(h, c->cfg.vocab);
+    uint64_t x = fnv(h);
+    x ^= (uint64_t)(s.uniform[b] * 16777216.0f) << 32;
+    x ^= (uint64_t)(uint32_t)s.top_k[b] << 8;
+    x ^= (uint64_t)(int64_t)(s.temperature[b] * 1000.0f + 0.5f) << 16;
+    x ^= (uint64_t)(int64_t)(s.top_p[b] * 1000.0f + 0.5f) << 40;
+    return (int32_t)(x % (uint64_t)c->cfg.vocab);
 }
 
 bool unique_slots(const qwen3_ctx *c, const int32_t *s, int B) {
@@ -84,7 +101,8 @@ int qwen3_prefill_append(qwen3_ctx *c, const int32_t *tokens, const int32_t *cu_
                          const int32_t *slots_dev, const int32_t *slots, int32_t B, float *logits, int32_t *next,
                          void *) {
     if (!c) return QWEN3_E_INVALID;
-    if (!tokens || !cu_dev || !cu || !slots_dev || !slots || !next || logits) return c->fail(QWEN3_E_INVALID, "args");
+    if (!tokens || !cu_dev || !cu || !slots_dev || !slots || !next || (logits == nullptr) != (c->sampling.temperature == nullptr))
+        return c->fail(QWEN3_E_INVALID, "args");
     if (B < 1 || B > c->cfg.max_seqs || !unique_slots(c, slots, B) || cu[0] != 0)
         return c->fail(QWEN3_E_INVALID, "rows");
     for (int b = 0; b < B; ++b) {
@@ -98,7 +116,7 @@ int qwen3_prefill_append(qwen3_ctx *c, const int32_t *tokens, const int32_t *cu_
     for (int b = 0; b < B; ++b) {
         std::vector<int32_t> &h = c->hist[slots[b]];
         h.insert(h.end(), tokens + cu[b], tokens + cu[b + 1]);
-        next[b] = next_token(h, c->cfg.vocab);
+        next[b] = row_token(c, h, b);
         c->log.insert(c->log.end(), {slots[b], cu[b + 1] - cu[b]});
         c->log.insert(c->log.end(), tokens + cu[b], tokens + cu[b + 1]);
     }
@@ -108,7 +126,8 @@ int qwen3_prefill_append(qwen3_ctx *c, const int32_t *tokens, const int32_t *cu_
 int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens, const int32_t *slots_dev, const int32_t *slots,
                       int32_t B, float *logits, int32_t *next, void *) {
     if (!c) return QWEN3_E_INVALID;
-    if (!tokens || !slots_dev || !slots || !next || logits) return c->fail(QWEN3_E_INVALID, "args");
+    if (!tokens || !slots_dev || !slots || !next || (logits == nullptr) != (c->sampling.temperature == nullptr))
+        return c->fail(QWEN3_E_INVALID, "args");
     if (B < 1 || B > c->cfg.max_seqs || !unique_slots(c, slots, B)) return c->fail(QWEN3_E_INVALID, "rows");
     for (int b = 0; b < B; ++b) {
         if (slots_dev[b] != slots[b]) return c->fail(QWEN3_E_INVALID, "upload");
@@ -119,13 +138,24 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens, const int32_t *slots_
     for (int b = 0; b < B; ++b) {
         std::vector<int32_t> &h = c->hist[slots[b]];
         h.push_back(tokens[b]);
-        next[b] = next_token(h, c->cfg.vocab);
+        next[b] = row_token(c, h, b);
         c->log.insert(c->log.end(), {slots[b], 1, tokens[b]});
     }
     return QWEN3_OK;
 }
 
 const char *qwen3_last_error(const qwen3_ctx *c) { return c ? c->err.c_str() : ""; }
+
+int qwen3_set_sampling(qwen3_ctx *c, const qwen3_sampling *sp) {
+    if (!c) return QWEN3_E_INVALID;
+    if (!sp || !sp->temperature) {
+        c->sampling = qwen3_sampling{};
+        return QWEN3_OK;
+    }
+    if (!sp->top_k || !sp->top_p || !sp->uniform) return c->fail(QWEN3_E_INVALID, "NULL sampling array");
+    c->sampling = *sp;
+    return QWEN3_OK;
+}
 
 // ---- test hooks ------------------------------------------------------------------------
 qwen3_ctx *mock_ctx_create(int32_t max_seqs, int32_t max_ctx, int32_t max_prefill_tokens, int32_t vocab) {

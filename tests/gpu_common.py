@@ -103,3 +103,14 @@ def oracle_prefills(shape, prompts):
     with concurrent.futures.ProcessPoolExecutor(max_workers=len(prompts), mp_context=ctx) as ex:
         futs = [ex.submit(_oracle_prefill_job, shape, [int(t) for t in p]) for p in prompts]
         return [f.result() for f in futs]
+
+
+def splitmix64_draw(seed: int, t: int) -> float:
+    """The uniform draw of a sampling request's t-th token in the engine: output t + 1 of
+    SplitMix64 (Steele, Lea and Flood 2014) started at `seed`, its top 24 bits over 2^24."""
+    m = (1 << 64) - 1
+    z = (seed + (t + 1) * 0x9E3779B97F4A7C15) & m
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & m
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & m
+    z ^= z >> 31
+    return (z >> 40) / 16777216.0

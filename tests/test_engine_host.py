@@ -50,6 +50,8 @@ def lib(tmp_path_factory):
         "qwen3_engine_workspace_bytes": (ctypes.c_size_t, [P, I32]),
         "qwen3_engine_create": (ctypes.c_int, [P, I32, P, ctypes.c_size_t, ctypes.POINTER(P)]),
         "qwen3_engine_submit": (ctypes.c_int, [P, I64, ctypes.POINTER(I32), I32, I32, I32]),
+        "qwen3_engine_submit_sampled": (ctypes.c_int, [P, I64, ctypes.POINTER(I32), I32, I32, I32, ctypes.c_float, I32,
+                                                       ctypes.c_float, ctypes.c_uint64]),
         "qwen3_engine_step": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
         "qwen3_engine_unfinished": (I32, [P]),
         "qwen3_engine_result": (ctypes.c_int, [P, I64, ctypes.POINTER(I32), I32, ctypes.POINTER(I32),
@@ -74,8 +76,35 @@ def fnv_next(history, vocab):
     return x % vocab
 
 
-def expected(prompt, max_new, eos, max_ctx, vocab):
-    """(tokens, finish reason) the engine's rules give for one request on the stand-in model."""
+def splitmix64_draw(seed, t):
+    """Uniform draw of a sampling request's t-th token: output t + 1 of SplitMix64 (Steele, Lea
+    and Flood 2014) started at `seed`, top 24 bits over 2^24."""
+    m = (1 << 64) - 1
+    z = (seed + (t + 1) * 0x9E3779B97F4A7C15) & m
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & m
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & m
+    z ^= z >> 31
+    return (z >> 40) / 16777216.0
+
+
+def sampled_next(history, vocab, temperature, top_k, top_p, u):
+    """The stand-in model's token for a sampling row: the history's hash mixed with the row's
+    draw and settings (engine_host_mock.cpp, row_token)."""
+    import numpy as np
+    x = 14695981039346656037
+    for t in history:
+        x ^= t & 0xFFFFFFFF
+        x = (x * 1099511628211) % (1 << 64)
+    x ^= int(np.float32(u) * np.float32(16777216.0)) << 32
+    x ^= (top_k & 0xFFFFFFFF) << 8
+    x ^= int(np.float32(np.float32(temperature) * np.float32(1000.0) + np.float32(0.5))) << 16
+    x ^= int(np.float32(np.float32(top_p) * np.float32(1000.0) + np.float32(0.5))) << 40
+    return (x % (1 << 64)) % vocab
+
+
+def expected(prompt, max_new, eos, max_ctx, vocab, sampling=None):
+    """(tokens, finish reason) the engine's rules give for one request on the stand-in model;
+    sampling = (temperature, top_k, top_p, seed) for a request submitted with them."""
     gen = []
     while True:
         if gen:
@@ -85,7 +114,11 @@ def expected(prompt, max_new, eos, max_ctx, vocab):
                 return gen, binding.QWEN3_FINISH_LENGTH
             if len(prompt) + len(gen) - 1 >= max_ctx:  # the last token cannot be appended
                 return gen, binding.QWEN3_FINISH_CONTEXT
-        gen.append(fnv_next(prompt + gen, vocab))  # every earlier token has been fed
+        if sampling and sampling[0] > 0:
+            T, k, p, seed = sampling
+            gen.append(sampled_next(prompt + gen, vocab, T, k, p, splitmix64_draw(seed, len(gen))))
+        else:
+            gen.append(fnv_next(prompt + gen, vocab))  # every earlier token has been fed
 
 
 class Run:
@@ -100,8 +133,11 @@ class Run:
         rc = lib.qwen3_engine_create(self.ctx, budget, ptr, n, ctypes.byref(self.eng))
         assert rc == binding.QWEN3_OK
 
-    def submit(self, rid, prompt, max_new, eos=-1):
+    def submit(self, rid, prompt, max_new, eos=-1, sampling=None):
         arr = (I32 * len(prompt))(*prompt)
+        if sampling:
+            T, k, p, seed = sampling
+            return self.lib.qwen3_engine_submit_sampled(self.eng, rid, arr, len(prompt), max_new, eos, T, k, p, seed)
         return self.lib.qwen3_engine_submit(self.eng, rid, arr, len(prompt), max_new, eos)
 
     def run(self, max_steps=10000):
@@ -299,3 +335,40 @@ def test_engine_argument_checks(lib):
     assert lib.qwen3_engine_result(eng, 1, None, 0, ctypes.byref(n_out), ctypes.byref(why)) == binding.QWEN3_E_INVALID
     lib.qwen3_engine_free(eng)
     lib.mock_ctx_free(ctx)
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13])
+def test_engine_sampling_requests(lib, seed):
+    """Sampling requests mixed with greedy ones: each sampling row gets its own settings and the
+    draw of its own token index from its own seed, whatever else shares the step; greedy rows of
+    a sampling step stay greedy."""
+    rng = random.Random(seed)
+    vocab, max_ctx = 97, 60
+    run = Run(lib, max_seqs=4, max_ctx=max_ctx, max_prefill=64, vocab=vocab, budget=16)
+    reqs = {}
+    for rid in range(12):
+        prompt = [rng.randrange(vocab) for _ in range(rng.randint(1, 30))]
+        max_new = rng.randint(1, 25)
+        eos = rng.choice([-1, -1, rng.randrange(vocab)])
+        sampling = None
+        if rid % 3:
+            sampling = (rng.choice([0.6, 1.0, 1.7]), rng.choice([0, 5, 40]), rng.choice([1.0, 0.9, 0.5]),
+                        rng.randrange(1 << 64))
+        assert run.submit(rid, prompt, max_new, eos, sampling) == binding.QWEN3_OK
+        reqs[rid] = (prompt, max_new, eos, sampling)
+    run.run()
+    for rid, (prompt, max_new, eos, sampling) in reqs.items():
+        assert run.result(rid) == expected(prompt, max_new, eos, max_ctx, vocab, sampling), rid
+    run.close()
+
+
+def test_splitmix64_reference_values():
+    """The draw generator against the published SplitMix64 outputs for state 0 (the first
+    output of seed 0 is 0xE220A8397B1DCDAF)."""
+    m = (1 << 64) - 1
+    z = 0x9E3779B97F4A7C15
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & m
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & m
+    z ^= z >> 31
+    assert z == 0xE220A8397B1DCDAF
+    assert splitmix64_draw(0, 0) == (0xE220A8397B1DCDAF >> 40) / 16777216.0
