@@ -61,10 +61,9 @@ def parse_args():
                    help="workload of the line's 'prefill' object when the main workload decodes ('none': skip)")
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--launch", default="graph", choices=["graph", "graph-nopdl", "direct", "persistent"],
-                   help="graph: decode steps as a CUDA graph of the kernel chain; direct: kernel by kernel "
-                        "without PDL (for profilers); persistent: steps of up to 8 sequences as one "
-                        "persistent kernel")
+    p.add_argument("--launch", default="graph", choices=["graph", "graph-nopdl", "direct", "chain"],
+                   help="graph: decode steps as CUDA graphs with programmatic dependent launch; direct: kernel "
+                        "by kernel without it (for profilers); chain: one-row steps as the four-kernel chain")
     p.add_argument("--decode-steps", type=int, default=None,
                    help="override the workload's decode steps (shorter runs for profilers)")
     p.add_argument("--roofline-only", action="store_true",
@@ -881,7 +880,7 @@ def gpu_arm(args, wl):
     peaks, peak_kind = load_peaks()
     flags = {"graph": 0, "graph-nopdl": binding.QWEN3_FLAG_NO_PDL,
              "direct": binding.QWEN3_FLAG_NO_GRAPH | binding.QWEN3_FLAG_NO_PDL,
-             "persistent": binding.QWEN3_FLAG_PERSISTENT}[args.launch]
+             "chain": binding.QWEN3_FLAG_DECODE_CHAIN}[args.launch]
     args.warmup = max(args.warmup, 3)  # at least three untimed steps
 
     if args.roofline_only:

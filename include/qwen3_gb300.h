@@ -54,8 +54,6 @@ extern "C" {
 /* qwen3_config.flags */
 #define QWEN3_FLAG_NO_GRAPH 1u   /* launch decode steps one kernel at a time instead of a CUDA graph */
 #define QWEN3_FLAG_NO_PDL 2u     /* launch kernels without programmatic dependent launch (for profilers) */
-#define QWEN3_FLAG_PERSISTENT 4u /* decode steps of up to 8 sequences as one persistent kernel
-                                    (Qwen3-0.6B widths only; see qwen3_decode_step) */
 #define QWEN3_FLAG_DECODE_CHAIN 8u /* decode steps of one sequence as the four-kernel-per-layer
                                       chain instead of two kernels per layer (see qwen3_decode_step) */
 
@@ -76,14 +74,14 @@ typedef struct qwen3_config {
     int32_t max_seqs;            /* KV-cache slots; also the largest decode batch */
     int32_t max_ctx;             /* tokens per slot (prompt + generated) */
     int32_t max_prefill_tokens;  /* largest N of one qwen3_prefill call */
-    uint32_t flags;              /* QWEN3_FLAG_* */
+    uint32_t flags;              /* QWEN3_FLAG_* (other bits: E_UNSUPPORTED) */
     /* KV cache layout.  kv_block_tokens == 0: every slot owns max_ctx positions (max_seqs *
      * max_ctx rows per layer).  kv_block_tokens > 0 (a multiple of 128): a paged cache ("第 3 章",
      * the engine's KV-cache blocks) -- a pool of kv_pool_blocks blocks of kv_block_tokens
      * positions shared by all slots; a slot takes blocks as its length grows (any block of the
      * pool, in any order) and gives them back when it restarts or is released.  A call that
      * needs more blocks than are free fails with E_CAPACITY before it launches anything.
-     * Paged needs n_q_heads == 2 * n_kv_heads and is not combined with QWEN3_FLAG_PERSISTENT. */
+     * Paged needs n_q_heads == 2 * n_kv_heads. */
     int32_t kv_block_tokens;
     int32_t kv_pool_blocks;
 } qwen3_config;
@@ -154,10 +152,7 @@ int qwen3_prefill_append(qwen3_ctx *ctx, const int32_t *tokens_dev, const int32_
  * slots[b] at position = the slot's current length, attends to keys 0..position, and
  * next_tok_dev[b] receives the greedy next token (logits_dev[B, V] too if not NULL).  Each
  * slot's length grows by one.  next_tok_dev may be passed as the next step's tokens_dev.
- * With QWEN3_FLAG_PERSISTENT, B <= 8 and the Qwen3-0.6B widths (hidden 1024, 16/8 heads,
- * head_dim 128) the whole step is one persistent kernel with one CTA per SM (cooperative
- * launch; it needs the whole GPU, so other work on the device waits for it).  Otherwise a
- * step of one sequence at hidden 1024, head_dim 128 and two query heads per KV head runs each
+ * A step of one sequence at hidden 1024, head_dim 128 and two query heads per KV head runs each
  * layer as two kernels (the attention block as clusters of 8 CTAs per KV head, then the MLP
  * block), unless QWEN3_FLAG_DECODE_CHAIN is set; other steps run four or more kernels per
  * layer.  Unless QWEN3_FLAG_NO_GRAPH is set, the step's kernels are recorded once per (B,
@@ -191,8 +186,7 @@ typedef struct qwen3_sampling {
 /* Next tokens drawn by sampling ("第 3 章", 4.3 Sampler): while set, every qwen3_prefill,
  * qwen3_prefill_append and qwen3_decode_step writes its logits and then replaces the greedy
  * next_tok_dev[b] by the qwen3_sample draw from them, in the same stream (inside the decode
- * graph).  Those calls then need a logits_dev buffer (E_INVALID otherwise), and the
- * persistent decode kernel is followed by one more launch.  sampling == NULL, or a NULL
+ * graph).  Those calls then need a logits_dev buffer (E_INVALID otherwise).  sampling == NULL, or a NULL
  * temperature, returns to greedy next tokens.  The structure is copied; the arrays are
  * borrowed until the setting is replaced.  Errors: E_INVALID (a NULL array),
  * E_UNSUPPORTED (a vocabulary the sampler cannot hold). */

@@ -23,7 +23,6 @@ QWEN3_E_CUDA = -4
 QWEN3_E_DEVICE = -5
 QWEN3_FLAG_NO_GRAPH = 1
 QWEN3_FLAG_NO_PDL = 2
-QWEN3_FLAG_PERSISTENT = 4
 QWEN3_FLAG_DECODE_CHAIN = 8
 QWEN3_EPI_F32 = 0
 QWEN3_EPI_RESID_ADD = 1

@@ -267,31 +267,6 @@ size_t attn_block_smem(int B);
 cudaError_t launch_attn_block(const Launch &lc, const AttnBlockParams &p);
 cudaError_t launch_mlp_block(const Launch &lc, const MlpBlockParams &p);
 
-// --- decode_persistent.cu (one decode step as a single persistent kernel) ------------------
-struct DecodePersistentArgs {
-    int L, C, Hq, Hkv, head_dim, I, V, max_ctx, B;
-    float eps;
-    const uint8_t *layers;  // layer l at layers + l * layer_bytes; members at the o_* offsets
-    // o_wog: o_proj regrouped by KV head, [Hkv][C][(Hq/Hkv) * head_dim] (the columns of group g)
-    size_t layer_bytes, o_wqkv, o_wog, o_wgu, o_wdownT, o_gin, o_gpost, o_gq, o_gk;
-    const bf16 *embed;
-    const float *g_final;
-    const float2 *rope;
-    bf16 *kcache, *vcache;     // layer l at + l * kv_layer_elems
-    size_t kv_layer_elems;
-    const int32_t *tokens, *slots;
-    int32_t *ctx_len, *next_tok;
-    float *logits, *dump;      // optional
-    float *res[3];             // fp32 [B, C] each; res[1] zero at creation (and after each step)
-    float *qkv;                // fp32 [B, (Hq + 2 Hkv) * head_dim]
-    float *part_val;           // [B, num_sms]
-    int32_t *part_idx;
-    uint32_t *arrive, *grp, *counter;  // [1], [Hkv], [1]: zero at creation (and after each step)
-    uint32_t *err;
-};
-bool decode_persistent_supported(int C, int Hq, int Hkv, int head_dim, int I, int B, int num_sms);
-cudaError_t launch_decode_persistent(const Launch &lc, const DecodePersistentArgs &p);
-
 // --- sample.cu ---------------------------------------------------------------------------
 // Temperature / top-k / top-p draw of next_tok[b] from logits fp32 [B, V] (the rule of
 // qwen3_sample); launched without programmatic dependent launch, after the lm_head.

@@ -20,7 +20,6 @@ namespace {
 constexpr size_t ALIGN = 1024;
 constexpr int MAX_SPLIT = ATTN_DECODE_MAX_SPLIT;  // decode attention: key ranges per (sequence, head)
 constexpr int MAX_PARTS = 1024; // lm_head partial results per row
-constexpr int PFLAG_WORDS = 64;  // persistent decode: [0] all-CTA arrivals, [1] argmax counter, [8, 8+Hkv) groups
 
 size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
 
@@ -32,7 +31,7 @@ struct Layout {
            kv_layer_bytes = 0, o_ctxlen = 0, o_err = 0, o_kvtable = 0;
     int32_t kv_max_blocks = 0;  // paged cache: table entries per slot
     size_t o_resid = 0, o_xn = 0, o_qkv = 0, o_q = 0, o_attn = 0, o_act = 0, o_rowslot = 0,
-           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0, o_pflags = 0, o_pres = 0,
+           o_rowpos = 0, o_last = 0, o_pval = 0, o_pidx = 0, o_wsml = 0, o_wso = 0, o_counters = 0, o_pres = 0,
            o_resid2 = 0, o_ssp = 0;
     size_t total = 0;
 };
@@ -58,13 +57,14 @@ bool config_supported(const qwen3_config &c, std::string *why) {
         (2 * c.intermediate) % 128)
         return fail("config: projection widths must be multiples of 128");
     if (c.max_seqs > 1024) return fail("config: max_seqs must be at most 1024");
+    if (c.flags & ~(QWEN3_FLAG_NO_GRAPH | QWEN3_FLAG_NO_PDL | QWEN3_FLAG_DECODE_CHAIN))
+        return fail("config: unknown flag bits");
     if (c.kv_block_tokens < 0 || (c.kv_block_tokens > 0 && (c.kv_block_tokens % 128 || c.kv_pool_blocks < 1)))
         return fail("config: kv_block_tokens must be 0 or a multiple of 128, with kv_pool_blocks >= 1");
     if (c.kv_block_tokens > 0) {
         if (c.n_q_heads != 2 * c.n_kv_heads) return fail("config: a paged KV cache needs n_q_heads == 2 * n_kv_heads");
         if (((c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim) % 256 || c.hidden % 64)
             return fail("config: a paged KV cache needs the tensor-core QKV projection shape");
-        if (c.flags & QWEN3_FLAG_PERSISTENT) return fail("config: a paged KV cache does not run the persistent decode kernel");
         if ((size_t)c.kv_pool_blocks * c.n_kv_heads * c.kv_block_tokens > (size_t)INT32_MAX)
             return fail("config: kv_pool_blocks too large");
     }
@@ -84,7 +84,7 @@ Layout make_layout(const qwen3_config &c) {
     // one layer's block
     L.o_wqkv = take(qkv_n * C * 2);
     L.o_wo = take(C * Hq * D * 2);
-    L.o_wog = take(C * Hq * D * 2);  // o_proj regrouped by KV head [Hkv][C][Hq/Hkv*D] (persistent decode)
+    L.o_wog = take(C * Hq * D * 2);  // o_proj regrouped by KV head [Hkv][C][Hq/Hkv*D] (one-row decode layer)
     L.o_wgu = take(2 * I * C * 2);
     L.o_wdown = take(C * I * 2);
     L.o_wdownT = take(C * I * 2);  // down weight transposed [I, C] for the split-K decode MLP
@@ -126,8 +126,7 @@ Layout make_layout(const qwen3_config &c) {
     L.o_wso = take((size_t)c.max_seqs * Hq * MAX_SPLIT * D * 4);
     L.o_counters = take((size_t)c.max_seqs * Hkv * 4);
     L.o_resid2 = take((size_t)c.max_seqs * C * 4);  // second residual buffer of the decode ping-pong
-    L.o_pflags = take(PFLAG_WORDS * 4);  // persistent decode: arrival counters, argmax counter
-    L.o_pres = take((size_t)3 * c.max_seqs * C * 4);  // persistent decode: three residual buffers
+    L.o_pres = take((size_t)3 * c.max_seqs * C * 4);  // one-row decode layer: three residual buffers
     L.o_ssp = take(2 * R * (C / 128) * 4);  // prefill: per-128-column sums of squares of h, two norms
     L.total = off;
     return L;
@@ -627,7 +626,6 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
             Q3_TRY(cudaMemsetAsync(c->arena + lay.o_kvtable, 0, (size_t)cfg->max_seqs * lay.kv_max_blocks * 4, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_err, 0, 16, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_counters, 0, (size_t)cfg->max_seqs * cfg->n_kv_heads * 4, st));
-        Q3_TRY(cudaMemsetAsync(c->arena + lay.o_pflags, 0, PFLAG_WORDS * 4, st));
         Q3_TRY(cudaMemsetAsync(c->arena + lay.o_pres, 0, (size_t)3 * cfg->max_seqs * C * 4, st));
         Q3_TRY(cudaStreamSynchronize(st));
         return cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
@@ -744,49 +742,6 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
         std::vector<int> new_len(B);
         for (int b = 0; b < B; ++b) new_len[b] = c->len_host[slots_host[b]] + 1;
         if (int rc = kv_reserve(c, slots_host, new_len.data(), B, false, st)) return rc;
-    }
-    const qwen3_config &k = c->cfg;
-    if ((k.flags & QWEN3_FLAG_PERSISTENT) && c->num_sms <= MAX_PARTS && k.n_kv_heads <= PFLAG_WORDS - 8 &&
-        decode_persistent_supported(k.hidden, k.n_q_heads, k.n_kv_heads, k.head_dim, k.intermediate, B, c->num_sms)) {
-        const Layout &L = c->lay;
-        DecodePersistentArgs p;
-        p.L = k.n_layers; p.C = k.hidden; p.Hq = k.n_q_heads; p.Hkv = k.n_kv_heads; p.head_dim = k.head_dim;
-        p.I = k.intermediate; p.V = k.vocab; p.max_ctx = k.max_ctx; p.B = B;
-        p.eps = k.rms_eps;
-        p.layers = c->layer(0);
-        p.layer_bytes = L.layer_bytes;
-        p.o_wqkv = L.o_wqkv; p.o_wog = L.o_wog; p.o_wgu = L.o_wgu; p.o_wdownT = L.o_wdownT;
-        p.o_gin = L.o_gin; p.o_gpost = L.o_gpost; p.o_gq = L.o_gq; p.o_gk = L.o_gk;
-        p.embed = c->at<bf16>(L.o_embed);
-        p.g_final = c->at<float>(L.o_gfinal);
-        p.rope = c->at<float2>(L.o_rope);
-        p.kcache = c->kcache(0);
-        p.vcache = c->vcache(0);
-        p.kv_layer_elems = L.kv_layer_bytes / 2;
-        p.tokens = tokens_dev; p.slots = slots_dev;
-        p.ctx_len = c->at<int32_t>(L.o_ctxlen);
-        p.next_tok = next_tok_dev;
-        p.logits = logits_dev;
-        p.dump = c->dump;
-        for (int i = 0; i < 3; ++i) p.res[i] = c->at<float>(L.o_pres) + (size_t)i * k.max_seqs * k.hidden;
-        p.qkv = c->at<float>(L.o_qkv);
-        p.part_val = c->at<float>(L.o_pval);
-        p.part_idx = c->at<int32_t>(L.o_pidx);
-        uint32_t *pf = c->at<uint32_t>(L.o_pflags);
-        p.arrive = pf;
-        p.counter = pf + 1;
-        p.grp = pf + 8;
-        p.err = c->at<uint32_t>(L.o_err);
-        Launch lc;
-        lc.stream = st;
-        lc.pdl = false;
-        lc.num_sms = c->num_sms;
-        lc.counter = &c->launches;
-        cudaError_t e = launch_decode_persistent(lc, p);
-        if (e == cudaSuccess) e = draw_next(c, lc, logits_dev, B, next_tok_dev);
-        if (e != cudaSuccess) return c->cuda_fail(e, "qwen3_decode_step (persistent)");
-        for (int b = 0; b < B; ++b) c->len_host[slots_host[b]] += 1;
-        return QWEN3_OK;
     }
     const Rows rows = make_rows(c, nullptr, slots_dev, B, B);
     const bool use_graph = !(c->cfg.flags & QWEN3_FLAG_NO_GRAPH) && !c->dump;

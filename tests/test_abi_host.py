@@ -54,6 +54,13 @@ def test_unsupported_config_sizes_to_zero(lib, field, value):
     assert binding.qwen3_arena_bytes(cfg) == 0
 
 
+def test_unknown_flag_bits_are_unsupported(lib):
+    for flags in (4, 16, 1 << 31):
+        assert binding.qwen3_arena_bytes(binding.make_config(synth.QWEN3_TINY, 1, 64, 64, flags)) == 0
+    ok = binding.QWEN3_FLAG_NO_GRAPH | binding.QWEN3_FLAG_NO_PDL | binding.QWEN3_FLAG_DECODE_CHAIN
+    assert binding.qwen3_arena_bytes(binding.make_config(synth.QWEN3_TINY, 1, 64, 64, ok)) > 0
+
+
 def test_create_rejects_null_and_unsupported(lib):
     cfg = binding.make_config(synth.QWEN3_TINY, 1, 64, 64)
     w = binding.qwen3_weights()
@@ -123,7 +130,7 @@ def test_paged_kv_config_sizes_and_rejections(lib):
     assert 0 < paged < flat
     assert abs((flat - paged) - (kv_flat - kv_paged)) < 2 ** 20  # the pool replaces the per-slot rows
     for bt, pool, flags, heads in ((100, 8, 0, 8), (64, 8, 0, 8), (128, 0, 0, 8), (-128, 8, 0, 8),
-                                   (128, 8, binding.QWEN3_FLAG_PERSISTENT, 8), (128, 8, 0, 4)):
+                                   (128, 8, 4, 8), (128, 8, 0, 4)):
         cfg = binding.make_config(s, 4, 512, 512, flags, bt, pool)
         cfg.n_kv_heads = heads
         assert binding.qwen3_arena_bytes(cfg) == 0, (bt, pool, flags, heads)

@@ -24,11 +24,9 @@ def setup():
     return w, prompt, ref
 
 
-@pytest.mark.parametrize("flags", [0, binding.QWEN3_FLAG_DECODE_CHAIN, binding.QWEN3_FLAG_PERSISTENT],
-                         ids=["layer", "chain", "persistent"])
+@pytest.mark.parametrize("flags", [0, binding.QWEN3_FLAG_DECODE_CHAIN], ids=["layer", "chain"])
 def test_decode_b1_teacher_forced_parity(setup, flags):
-    """Decode steps as two kernels per layer (the default), as the four-kernel chain and as the
-    single persistent kernel."""
+    """Decode steps as two kernels per layer (the default) and as the four-kernel chain."""
     w, prompt, ref = setup
     s = WL.shape
     m = binding.Model(s, w, max_seqs=1, max_ctx=WL.max_ctx, max_prefill_tokens=WL.lengths[0], flags=flags)
