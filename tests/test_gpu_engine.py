@@ -188,42 +188,15 @@ SAMPLING = [(1.0, 40, 0.9, 7), None, (0.7, 0, 1.0, 12345678901234567), (1.3, 5, 
             (1.0, 0, 0.95, 2 ** 63 + 5)]
 
 
-def _direct_sampled(w, prompt, n_new, settings, logits_out):
-    """One request alone on the prefill + decode path with the same per-token draws the engine
-    uses: the context's sampling set to the request's settings, uniform[0] rewritten to draw t
-    before the call that produces token t.  Returns the tokens and each call's logits."""
-    T, k, p, seed = settings
-    m = binding.Model(TINY, w, max_seqs=1, max_ctx=64, max_prefill_tokens=48)
-    temp = torch.tensor([T], dtype=torch.float32, device="cuda")
-    topk = torch.tensor([k], dtype=torch.int32, device="cuda")
-    topp = torch.tensor([p], dtype=torch.float32, device="cuda")
-    unif = torch.tensor([gc.splitmix64_draw(seed, 0)], dtype=torch.float32, device="cuda")
-    m.set_sampling(temp, topk, topp, unif)
-    nxt, lg = m.prefill(torch.tensor(prompt, dtype=torch.int32, device="cuda"), [len(prompt)], [0],
-                        want_logits=True)
-    toks, logits = [int(nxt[0])], [lg[0].cpu().numpy()]
-    slots = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = torch.zeros(1, dtype=torch.int32, device="cuda")
-    buf = torch.zeros(1, TINY.vocab, dtype=torch.float32, device="cuda")
-    for t in range(1, n_new):
-        unif.fill_(gc.splitmix64_draw(seed, t))
-        m.decode_step(nxt, slots, [0], out, buf)
-        toks.append(int(out[0]))
-        logits.append(buf[0].cpu().numpy())
-        nxt = out.clone()
-    assert m.status() == 0
-    m.close()
-    return toks, logits
-
-
 def test_engine_sampling_requests(tiny):
-    """Sampling and greedy requests in one engine: a sampling request's tokens equal those of the
-    same request run alone on the prefill + decode path with the same settings and draws, and
-    each of them is the oracle sampler's draw from the logits it was drawn from; greedy
-    requests keep matching the oracle's greedy tokens.  (Both runs compute the logits with the
-    same kernels in a different batching, so they may differ in the last bits; a draw within
-    1e-4 of a boundary of the cumulative distribution may then land on the neighbour -- that
-    request's comparison stops there.)"""
+    """Sampling and greedy requests in one engine.  Greedy requests keep matching the oracle's
+    greedy tokens (the parity gate's margin rule).  A sampling request's token t must be the
+    oracle sampler's draw, with the request's temperature / top-k / top-p, from the oracle's
+    logits of the same prefix (teacher-forced on the engine's tokens), for a uniform within
+    0.02 of the request's own draw t (SplitMix64 from its seed): the engine's logits differ
+    from the oracle's by up to the 1e-2 gate, which moves the cumulative distribution by about
+    that much.  The window decides the token alone for most draws, so a wrong draw, setting or
+    row would show."""
     w, prompts = tiny
     cfg, ow = gc.oracle_config(TINY), gc.oracle_weights(w)
     m = binding.Model(TINY, w, max_seqs=3, max_ctx=64, max_prefill_tokens=48)
@@ -239,21 +212,20 @@ def test_engine_sampling_requests(tiny):
     assert m.status() == 0
     eng.close()
     m.close()
-    compared = 0
+    window = np.linspace(-0.02, 0.02, 41)
+    sampled, decided = 0, 0
     for i, ((toks, why), s) in enumerate(zip(results, SAMPLING)):
-        n_new = REQUESTS[i][1]
-        assert len(toks) == n_new and why == binding.QWEN3_FINISH_LENGTH
+        assert len(toks) == REQUESTS[i][1] and why == binding.QWEN3_FINISH_LENGTH
         if s is None:
             _oracle_check(cfg, ow, prompts[i], toks, f"greedy request {i}")
             continue
-        ref, logits = _direct_sampled(w, prompts[i], n_new, s, None)
-        for t, (a, b, lg) in enumerate(zip(toks, ref, logits)):
-            u = gc.splitmix64_draw(s[3], t)
-            drawn = oracle.sample(lg, s[0], s[1], s[2], u)
-            near = {oracle.sample(lg, s[0], s[1], s[2], min(max(u + d, 0.0), 1.0 - 2 ** -24)) for d in (-1e-4, 1e-4)}
-            assert b == drawn or b in near, (i, t, b, drawn)  # the direct path draws as the oracle does
-            if a != b:
-                assert a in near | {drawn}, (i, t, a, b)
-                break
-            compared += 1
-    assert compared >= 20
+        T, k, p, seed = s
+        ref = oracle.generate(cfg, ow, prompts[i], len(toks) - 1, forced=toks[:-1])
+        for t, (tok, call) in enumerate(zip(toks, ref["calls"])):
+            u = gc.splitmix64_draw(seed, t)
+            cands = {oracle.sample(call["logits"], T, k, p, float(min(max(u + d, 0.0), 1.0 - 2 ** -24)))
+                     for d in window}
+            assert tok in cands, (i, t, tok, sorted(cands))
+            sampled += 1
+            decided += len(cands) == 1
+    assert sampled >= 20 and decided >= sampled // 2, (sampled, decided)
