@@ -331,6 +331,14 @@ int qwen3_engine_forget(qwen3_engine *e, int64_t request_id);
 
 int qwen3_engine_get_stats(const qwen3_engine *e, qwen3_engine_stats *out);
 
+/* The last step that ran the model: the request id of each of its rows (in row order; up to
+ * capacity of them into ids_host, which may be NULL when capacity is 0), their count, and, if
+ * a request of that step samples, *logits_dev = the fp32 logits [rows, V] its draws were taken
+ * from (in the engine's workspace, valid until the next step; NULL for an all-greedy step).
+ * For inspecting the distribution a token was drawn from.  Errors: E_INVALID. */
+int qwen3_engine_last_step(const qwen3_engine *e, int64_t *ids_host, int32_t capacity, int32_t *n_rows,
+                           const float **logits_dev);
+
 /* Message of the engine's last failed call. */
 const char *qwen3_engine_last_error(const qwen3_engine *e);
 

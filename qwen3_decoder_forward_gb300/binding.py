@@ -113,6 +113,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_engine_result": (ctypes.c_int, [_P, i64, pi32, i32, pi32, pi32]),
         "qwen3_engine_forget": (ctypes.c_int, [_P, i64]),
         "qwen3_engine_get_stats": (ctypes.c_int, [_P, ctypes.POINTER(qwen3_engine_stats)]),
+        "qwen3_engine_last_step": (ctypes.c_int, [_P, ctypes.POINTER(i64), i32, pi32, ctypes.POINTER(_P)]),
         "qwen3_engine_last_error": (ctypes.c_char_p, [_P]),
         "qwen3_engine_free": (None, [_P]),
         "qwen3_free": (None, [_P]),
@@ -570,6 +571,22 @@ class Engine:
 
     def stats(self) -> Dict[str, int]:
         return qwen3_engine_get_stats(self.eng)
+
+    def last_step(self):
+        """(request ids of the last model step's rows, their fp32 logits [rows, V] as a view of the
+        workspace -- or None for an all-greedy step)."""
+        lib = load_library()
+        n = ctypes.c_int32(0)
+        ptr = _P()
+        _engine_check(lib.qwen3_engine_last_step(self.eng, None, 0, ctypes.byref(n), None), self.eng)
+        ids = (ctypes.c_int64 * max(1, n.value))()
+        _engine_check(lib.qwen3_engine_last_step(self.eng, ids, n.value, ctypes.byref(n), ctypes.byref(ptr)), self.eng)
+        logits = None
+        if ptr.value:
+            V = self.model.shape.vocab
+            off = ptr.value - self.ws.data_ptr()
+            logits = self.ws[off: off + n.value * V * 4].view(self.model.torch.float32).view(n.value, V)
+        return [int(ids[i]) for i in range(n.value)], logits
 
     def close(self):
         if getattr(self, "eng", None) is not None:

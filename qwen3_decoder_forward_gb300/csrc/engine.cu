@@ -111,6 +111,9 @@ struct qwen3_engine {
     // host staging of one step
     std::vector<int32_t> h_tokens, h_cu, h_slots, h_next, h_topk;
     std::vector<float> h_temp, h_topp, h_unif;
+    // the last step that ran the model: the request of each row, and whether it sampled
+    std::vector<int64_t> last_ids;
+    bool last_sampled = false;
 
     int fail(int code, const std::string &m) {
         err = m;
@@ -242,8 +245,10 @@ int qwen3_engine_step(qwen3_engine *e, void *stream, int32_t *n_finished) {
     e->h_topk.clear();
     e->h_topp.clear();
     e->h_unif.clear();
+    e->last_ids.clear();
     for (const Row &w : rows) {
         Request *r = w.req;
+        e->last_ids.push_back(r->id);
         // the draw of the token this row produces (index = tokens generated so far)
         sampled = sampled || r->temperature > 0.0f;
         e->h_temp.push_back(r->temperature);
@@ -300,6 +305,7 @@ int qwen3_engine_step(qwen3_engine *e, void *stream, int32_t *n_finished) {
     }
     if (sampled && (rc = qwen3_set_sampling(e->ctx, nullptr)) != QWEN3_OK)
         return e->ctx_fail(rc, "qwen3_engine_step: set_sampling");
+    e->last_sampled = sampled;
     ++e->stats.steps;
     e->h_next.resize(B);
     ce = cudaMemcpyAsync(e->h_next.data(), d_next, (size_t)B * 4, cudaMemcpyDeviceToHost, st);
@@ -356,6 +362,16 @@ int qwen3_engine_forget(qwen3_engine *e, int64_t request_id) {
     if (it == e->requests.end() || it->second->finish == QWEN3_FINISH_NONE)
         return e->fail(QWEN3_E_INVALID, "qwen3_engine_forget: unknown or unfinished request");
     e->requests.erase(it);
+    return QWEN3_OK;
+}
+
+int qwen3_engine_last_step(const qwen3_engine *e, int64_t *ids_host, int32_t capacity, int32_t *n_rows,
+                           const float **logits_dev) {
+    if (!e || capacity < 0 || (capacity > 0 && !ids_host)) return QWEN3_E_INVALID;
+    const int32_t n = (int32_t)e->last_ids.size();
+    std::copy(e->last_ids.begin(), e->last_ids.begin() + std::min(n, capacity), ids_host);
+    if (n_rows) *n_rows = n;
+    if (logits_dev) *logits_dev = e->last_sampled ? reinterpret_cast<const float *>(e->ws + e->lay.logits) : nullptr;
     return QWEN3_OK;
 }
 

@@ -113,6 +113,7 @@ def test_engine_calls_reject_null_before_any_work(lib):
     assert lib.qwen3_engine_result(None, 1, None, 0, None, None) == binding.QWEN3_E_INVALID
     assert lib.qwen3_engine_forget(None, 1) == binding.QWEN3_E_INVALID
     assert lib.qwen3_engine_get_stats(None, None) == binding.QWEN3_E_INVALID
+    assert lib.qwen3_engine_last_step(None, None, 0, None, None) == binding.QWEN3_E_INVALID
     assert lib.qwen3_engine_last_error(None) == b""
     lib.qwen3_engine_free(None)
     cfg = binding.qwen3_config()

@@ -190,42 +190,55 @@ SAMPLING = [(1.0, 40, 0.9, 7), None, (0.7, 0, 1.0, 12345678901234567), (1.3, 5, 
 
 def test_engine_sampling_requests(tiny):
     """Sampling and greedy requests in one engine.  Greedy requests keep matching the oracle's
-    greedy tokens (the parity gate's margin rule).  A sampling request's token t must be the
-    oracle sampler's draw, with the request's temperature / top-k / top-p, from the oracle's
-    logits of the same prefix (teacher-forced on the engine's tokens), for a uniform within
-    0.02 of the request's own draw t (SplitMix64 from its seed): the engine's logits differ
-    from the oracle's by up to the 1e-2 gate, which moves the cumulative distribution by about
-    that much.  The window decides the token alone for most draws, so a wrong draw, setting or
-    row would show."""
+    greedy tokens (the parity gate's margin rule).  Every token a sampling request gets is the
+    oracle sampler's draw -- with the request's temperature / top-k / top-p and the uniform of
+    its own token index from its own seed (SplitMix64) -- from the logits of its row in the step
+    that produced it (qwen3_engine_last_step), token-exact except where the fp32 draw sits
+    within 1e-5 of a boundary of the cumulative distribution (the rule of the sampler tests)."""
     w, prompts = tiny
     cfg, ow = gc.oracle_config(TINY), gc.oracle_weights(w)
     m = binding.Model(TINY, w, max_seqs=3, max_ctx=64, max_prefill_tokens=48)
     eng = binding.Engine(m, 16)
+    ids = {}
     for i, (p, (_, n_new)) in enumerate(zip(prompts, REQUESTS)):
         s = SAMPLING[i]
+        ids[200 + i] = i
         if s:
             eng.submit(200 + i, p, n_new, temperature=s[0], top_k=s[1], top_p=s[2], seed=s[3])
         else:
             eng.submit(200 + i, p, n_new)
-    eng.run(max_steps=500)
+    checked, near = 0, 0
+    seen = {rid: 0 for rid in ids}
+    steps = 0
+    while eng.unfinished() and steps < 500:
+        eng.step()
+        steps += 1
+        rows, logits = eng.last_step()
+        lg = logits.cpu().numpy() if logits is not None else None
+        for r, rid in enumerate(rows):
+            toks, _ = eng.result(rid)
+            if len(toks) == seen[rid]:
+                continue  # a prompt chunk that did not end the prompt
+            t = len(toks) - 1
+            seen[rid] = len(toks)
+            s = SAMPLING[ids[rid]]
+            if s is None:
+                continue
+            assert lg is not None
+            T, k, p, seed = s
+            u = gc.splitmix64_draw(seed, t)
+            drawn = oracle.sample(lg[r], T, k, p, u)
+            if toks[t] != drawn:
+                alt = {oracle.sample(lg[r], T, k, p, min(max(u + d, 0.0), 1.0 - 2 ** -24)) for d in (-1e-5, 1e-5)}
+                assert toks[t] in alt, (rid, t, toks[t], drawn)
+                near += 1
+            checked += 1
     results = [eng.result(200 + i) for i in range(len(prompts))]
     assert m.status() == 0
     eng.close()
     m.close()
-    window = np.linspace(-0.02, 0.02, 41)
-    sampled, decided = 0, 0
     for i, ((toks, why), s) in enumerate(zip(results, SAMPLING)):
         assert len(toks) == REQUESTS[i][1] and why == binding.QWEN3_FINISH_LENGTH
         if s is None:
             _oracle_check(cfg, ow, prompts[i], toks, f"greedy request {i}")
-            continue
-        T, k, p, seed = s
-        ref = oracle.generate(cfg, ow, prompts[i], len(toks) - 1, forced=toks[:-1])
-        for t, (tok, call) in enumerate(zip(toks, ref["calls"])):
-            u = gc.splitmix64_draw(seed, t)
-            cands = {oracle.sample(call["logits"], T, k, p, float(min(max(u + d, 0.0), 1.0 - 2 ** -24)))
-                     for d in window}
-            assert tok in cands, (i, t, tok, sorted(cands))
-            sampled += 1
-            decided += len(cands) == 1
-    assert sampled >= 20 and decided >= sampled // 2, (sampled, decided)
+    assert checked == sum(REQUESTS[i][1] for i, s in enumerate(SAMPLING) if s) and near <= 1
