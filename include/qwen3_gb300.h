@@ -439,8 +439,10 @@ size_t qwen3_op_attn_decode_workspace_bytes(int32_t B, int32_t n_q_heads, int32_
  * v_cache_dev bf16 [n_slots][Hkv][max_ctx][128] (rows 0..p-1 of each used slot hold the
  * cached keys and values; row p is written); out_dev bf16 [B, Hq, 128].  slots and positions
  * are given on the device and on the host (same values; slots distinct, 0 <= slot < n_slots,
- * 0 <= position < max_ctx).  n_split key ranges per (row, KV head), 1..64, or 0 for one wave
- * of CTAs as a decode step plans it.  workspace_dev: qwen3_op_attn_decode_workspace_bytes
+ * 0 <= position < max_ctx).  n_split key ranges per (row, KV head), 1..64; or 0 as a decode
+ * step runs it: with Hq == 2 Hkv, one wave of CTAs each taking an equal share of all the
+ * launch's keys (the keys of all (row, KV head) pairs laid end to end, a pair split over the
+ * CTAs its keys fall in), otherwise one wave of equal ranges per pair.  workspace_dev: qwen3_op_attn_decode_workspace_bytes
  * bytes, 256-byte aligned, zero-filled before its first use (calls leave it reusable).
  * head_dim 128; Hq/Hkv in {1, 2, 4, 8}.  Errors: E_INVALID (NULL, bad size or index), E_CUDA. */
 int qwen3_op_attn_decode(const float *qkv_dev, int32_t B, const int32_t *slots_dev,

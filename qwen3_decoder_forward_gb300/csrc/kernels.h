@@ -228,6 +228,16 @@ cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const R
                                      float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
                                      int Hkv, int max_ctx, float eps, uint32_t *err);
 
+// --- attn_decode_flat.cu (decode attention over equal shares of all keys; Hq == 2 Hkv) -----
+// Same contract as launch_attn_decode_fused, with n_ctas CTAs in all (at most
+// (ATTN_DECODE_MAX_SPLIT - 2) * Hkv) instead of n_split per (sequence, KV head).
+bool attn_decode_flat_supported(int B, int Hq, int Hkv);
+int attn_decode_flat_ctas_per_sm();
+cudaError_t launch_attn_decode_flat(const Launch &lc, const float *qkv, const Rows &r, const float *q_gain,
+                                    const float *k_gain, const float2 *rope, bf16 *k_layer, bf16 *v_layer,
+                                    int n_ctas, float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
+                                    int Hkv, int max_ctx, float eps, uint32_t *err);
+
 // --- decode_block.cu (decode of 1-2 rows: one attention-block and one MLP-block kernel per layer)
 // Hidden 1024, head_dim 128, two query heads per KV head.  Row b appends to slot slots[b] at
 // position ctx_len[slots[b]].

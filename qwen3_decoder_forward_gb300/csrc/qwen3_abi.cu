@@ -154,7 +154,7 @@ struct qwen3_ctx {
     Layout lay;
     uint8_t *arena = nullptr;
     std::vector<int32_t> len_host;
-    int num_sms = 0, n_parts = 0, attn_ctas_per_sm = 1;
+    int num_sms = 0, n_parts = 0, attn_ctas_per_sm = 1, flat_ctas = 0;
     float *dump = nullptr;
     size_t dump_bytes = 0;
     cudaStream_t cap_stream = nullptr;
@@ -199,6 +199,22 @@ cudaError_t draw_next(qwen3_ctx *c, const Launch &lc, const float *logits, int B
     ls.pdl = false;
     const qwen3_sampling &sp = c->sampling;
     return launch_sample(ls, logits, B, c->cfg.vocab, sp.temperature, sp.top_k, sp.top_p, sp.uniform, next);
+}
+
+// The decode attention of layer l: over equal shares of all keys of the step where the head
+// ratio allows (every CTA streams the same number of K/V rows), else n_split key ranges per
+// (sequence, KV head).
+cudaError_t decode_attention(qwen3_ctx *c, const Launch &lc, const float *qkv, const Rows &rows, const float *g_q,
+                             const float *g_k, const float2 *rope, int l, int n_split, bf16 *attn, uint32_t *err) {
+    const qwen3_config &k = c->cfg;
+    const Layout &L = c->lay;
+    if (c->flat_ctas > 0 && attn_decode_flat_supported(rows.B, k.n_q_heads, k.n_kv_heads))
+        return launch_attn_decode_flat(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), c->flat_ctas,
+                                       c->at<float>(L.o_wsml), c->at<float>(L.o_wso), c->at<int>(L.o_counters), attn,
+                                       k.n_q_heads, k.n_kv_heads, k.max_ctx, k.rms_eps, err);
+    return launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
+                                    c->at<float>(L.o_wsml), c->at<float>(L.o_wso), c->at<int>(L.o_counters), attn,
+                                    k.n_q_heads, k.n_kv_heads, k.max_ctx, k.rms_eps, err);
 }
 
 // Everything one call runs, in stream order.  `decode` selects the GEMV projections and the
@@ -312,9 +328,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
             float *r_cur = res[l & 1], *r_next = res[(l + 1) & 1];
             Q3_TRY(launch_gemv_fused(lc, r_cur, R, C, w_qkv, qkv_n, EPI_F32, qkv, g_in, k.rms_eps, err,
                                      (const bf16 *)(ahead + L.o_wqkv), mlp ? r_next : nullptr, R * C));
-            Q3_TRY(launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
-                                            c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
-                                            c->at<int>(L.o_counters), attn, Hq, Hkv, k.max_ctx, k.rms_eps, err));
+            Q3_TRY(decode_attention(c, lc, qkv, rows, g_q, g_k, rope, l, n_split, attn, err));
             Q3_TRY(launch_gemv_fused(lc, attn, R, Hq * D, w_o, C, EPI_RESID_ADD, r_cur, nullptr, 0.0f, err,
                                      (const bf16 *)(ahead + L.o_wo)));
             if (mlp) {  // gate_up + SwiGLU + down in one kernel, residual into the other buffer
@@ -343,9 +357,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
             };
             if (l > 0) Q3_TRY(launch_rmsnorm(lc, resid, R, g_in, xn, C, k.rms_eps));
             Q3_TRY(proj(xn, C, w_qkv, qkv_n, EPI_F32, qkv));
-            Q3_TRY(launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
-                                            c->at<float>(L.o_wsml), c->at<float>(L.o_wso),
-                                            c->at<int>(L.o_counters), attn, Hq, Hkv, k.max_ctx, k.rms_eps, err));
+            Q3_TRY(decode_attention(c, lc, qkv, rows, g_q, g_k, rope, l, n_split, attn, err));
             Q3_TRY(proj(attn, Hq * D, w_o, C, EPI_RESID_ADD, resid));
             Q3_TRY(launch_rmsnorm(lc, resid, R, g_post, xn, C, k.rms_eps));
             Q3_TRY(proj(xn, C, w_gu, 2 * I, EPI_SWIGLU, act));
@@ -561,6 +573,9 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
     c->num_sms = prop.multiProcessorCount;
     c->n_parts = std::min(lmhead_parts(c->num_sms), MAX_PARTS);
     c->attn_ctas_per_sm = attn_decode_ctas_per_sm(cfg->n_q_heads, cfg->n_kv_heads);
+    // the balanced decode attention: one wave of CTAs over all keys of a step
+    if (attn_decode_flat_supported(1, cfg->n_q_heads, cfg->n_kv_heads))
+        c->flat_ctas = std::min(c->num_sms * attn_decode_flat_ctas_per_sm(), (MAX_SPLIT - 2) * cfg->n_kv_heads);
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);
     Launch lc;
     lc.stream = st;
@@ -1075,7 +1090,8 @@ int qwen3_op_attn_decode(const float *qkv, int32_t B, const int32_t *slots, cons
             return QWEN3_E_INVALID;
         }
     const Launch lc = op_launch(stream);
-    if (n_split == 0) {  // one wave of CTAs, as a decode step plans it for contexts up to max_ctx
+    const bool flat = n_split == 0 && attn_decode_flat_supported(B, n_q_heads, n_kv_heads);
+    if (n_split == 0 && !flat) {  // one wave of CTAs, as a decode step plans it for contexts up to max_ctx
         const int slots_all = lc.num_sms * attn_decode_ctas_per_sm(n_q_heads, n_kv_heads);
         n_split = std::max(1, std::min({slots_all / (B * n_kv_heads), MAX_SPLIT, (max_ctx + 63) / 64}));
     }
@@ -1089,10 +1105,16 @@ int qwen3_op_attn_decode(const float *qkv, int32_t B, const int32_t *slots, cons
     r.row_pos = const_cast<int32_t *>(positions);
     r.B = B;
     r.rows = B;
-    const cudaError_t e = launch_attn_decode_fused(lc, qkv, r, q_gain, k_gain, reinterpret_cast<const float2 *>(rope),
-                                                   static_cast<bf16 *>(k_cache), static_cast<bf16 *>(v_cache), n_split,
-                                                   ws_ml, ws_o, counters, static_cast<bf16 *>(out), n_q_heads,
-                                                   n_kv_heads, max_ctx, eps, nullptr);
+    const cudaError_t e =
+        flat ? launch_attn_decode_flat(lc, qkv, r, q_gain, k_gain, reinterpret_cast<const float2 *>(rope),
+                                       static_cast<bf16 *>(k_cache), static_cast<bf16 *>(v_cache),
+                                       std::min(lc.num_sms * attn_decode_flat_ctas_per_sm(), (MAX_SPLIT - 2) * n_kv_heads),
+                                       ws_ml, ws_o, counters, static_cast<bf16 *>(out), n_q_heads, n_kv_heads, max_ctx,
+                                       eps, nullptr)
+             : launch_attn_decode_fused(lc, qkv, r, q_gain, k_gain, reinterpret_cast<const float2 *>(rope),
+                                        static_cast<bf16 *>(k_cache), static_cast<bf16 *>(v_cache), n_split, ws_ml,
+                                        ws_o, counters, static_cast<bf16 *>(out), n_q_heads, n_kv_heads, max_ctx, eps,
+                                        nullptr);
     if (e != cudaSuccess) {
         g_create_error = std::string("qwen3_op_attn_decode: ") + cudaGetErrorString(e);
         return QWEN3_E_CUDA;
