@@ -40,15 +40,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129 * 2 ** 20
 
 # DRAM bytes (read + write) per launch of the roofline kernels, from ncu captures
-# (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel as it stands; None where no
-# capture of the current kernel exists.  The fused decode MLP at one row reads exactly its
-# 18.9 MB of weights; the prefill gate_up GEMM at 23,460 rows reads A (48 MB) and W (12.6 MB)
-# once and writes 86 MB of its 144 MB output before it ends (the rest leaves L2 later).
-# "attn_decode_per_key_row": DRAM bytes per (sequence, position) row of one layer's K and V of a
-# decode attention launch, measured at 16 rows x 4,097 positions (268.9 MB per launch against
-# 268.5 MB of K/V rows: 4,102 B a row for 4,096 algorithmic) and scaled by the rows a launch
-# reads (the traffic grows in proportion with the rows).
-TRAFFIC_BYTES = {"gemm_gate_up": 147362304, "mlp_fused": 18910976, "attn_decode_per_key_row": 4102.3}
+# (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel as it stands; a kernel without
+# an entry reports traffic null.  The fused decode MLP at one row reads exactly its 18.9 MB of
+# weights; the prefill gate_up GEMM at 23,460 rows reads A (48 MB) and W (12.6 MB) once and
+# writes 86 MB of its 144 MB output before it ends (the rest leaves L2 later).  The decode
+# attention entries are DRAM bytes per (sequence, position) row of one layer's K and V, scaled
+# by the rows a launch reads (the traffic grows in proportion with the rows).
+TRAFFIC_BYTES = {"gemm_gate_up": 147362304, "mlp_fused": 18910976, "attn_decode_flat_per_key_row": 4099.9,
+                 "attn_decode_fused_per_key_row": 4108.2}
 
 
 def parse_args():
@@ -408,11 +407,12 @@ def measure_mlp_roofline(torch, binding, wl, peaks, peak_kind):
 
 
 def measure_attn_roofline(torch, binding, wl, peaks, peak_kind, ctx=None, reps=20):
-    """Average duration of the split-KV decode attention kernel (QK-norm + RoPE + KV write +
-    attention over keys 0..p), the kernel that streams the KV cache, at the workload's batch
-    and the positions of its middle decode step (or every row at position ctx - 1), over one
-    layer's K/V rows of the workload's size in their own buffer (larger than L2 for the long
-    contexts), through qwen3_op_attn_decode."""
+    """Average duration of the decode attention kernel (QK-norm + RoPE + KV write + attention
+    over keys 0..p), the kernel that streams the KV cache, as a decode step of the workload
+    plans it (qwen3_op_attn_decode_plan: equal shares of all keys, or key ranges per pair), at
+    the workload's batch and the positions of its middle decode step (or every row at position
+    ctx - 1), over one layer's K/V rows of the workload's size in their own buffer (larger than
+    L2 for the long contexts), through qwen3_op_attn_decode."""
     import math
     s = wl.shape
     dev = torch.device("cuda")
@@ -439,11 +439,12 @@ def measure_attn_roofline(torch, binding, wl, peaks, peak_kind, ctx=None, reps=2
     ws = torch.zeros(ws_bytes + 256, dtype=torch.uint8, device=dev)
     ws_ptr = (ws.data_ptr() + 255) // 256 * 256
     stream = torch.cuda.current_stream().cuda_stream
+    n_split = binding.qwen3_op_attn_decode_plan(B, Hq, Hkv, max_ctx, max(max_ctx, wl.max_ctx))
 
     def launch():
         binding.qwen3_op_attn_decode(qkv.data_ptr(), B, slots_d.data_ptr(), slots, pos_d.data_ptr(), positions,
                                      gain.data_ptr(), gain.data_ptr(), rope_d.data_ptr(), kc.data_ptr(),
-                                     vc.data_ptr(), B, max_ctx, Hq, Hkv, s.rms_eps, 0, out.data_ptr(), ws_ptr,
+                                     vc.data_ptr(), B, max_ctx, Hq, Hkv, s.rms_eps, n_split, out.data_ptr(), ws_ptr,
                                      ws_bytes, stream)
     for _ in range(3):
         launch()
@@ -452,9 +453,12 @@ def measure_attn_roofline(torch, binding, wl, peaks, peak_kind, ctx=None, reps=2
     algo_bytes = rows * Hkv * D * 2 * 2  # K and V rows 0..p of every (sequence, KV head), the new one written
     achieved = algo_bytes / avg_s / 1e9
     peak = float(peaks["hbm_gbs"])
-    per_row = TRAFFIC_BYTES.get("attn_decode_per_key_row")
+    key = "attn_decode_flat_per_key_row" if n_split == 0 else "attn_decode_fused_per_key_row"
+    per_row = TRAFFIC_BYTES.get(key)
     del kc, vc
-    return {"kernel": f"k_attn_decode_fused (split-KV decode attention + QK-norm + RoPE + KV write, {B} rows at "
+    name = ("k_attn_decode_flat (equal shares of all keys" if n_split == 0 else
+            f"k_attn_decode_fused ({n_split} key range{'s' if n_split > 1 else ''} per pair")
+    return {"kernel": f"{name}; QK-norm + RoPE + KV write + attention, {B} rows at "
                       f"positions {min(positions)}..{max(positions)}, {Hq}/{Hkv} heads, one layer)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": round(per_row * rows) if per_row else None,

@@ -426,6 +426,15 @@ int qwen3_op_lmhead_argmax_noalloc(const void *x_dev, int32_t B, int32_t C,
 /* Bytes of workspace qwen3_op_attn_decode needs for B rows. */
 size_t qwen3_op_attn_decode_workspace_bytes(int32_t B, int32_t n_q_heads, int32_t n_kv_heads);
 
+/* The n_split a decode step of B rows whose longest context is max_len tokens (the new one
+ * included; 1 <= max_len <= max_ctx) gives its decode attention on the current device: 0 for
+ * equal shares of all the step's keys (with Hq == 2 Hkv, where the (row, KV head) pairs times
+ * the context rounded up to a power of two reach 2^21 keys), else the key ranges per (row, KV
+ * head) of one wave of CTAs, 1..64.  Passed to qwen3_op_attn_decode it runs the kernel a
+ * step would.  Errors (negative): E_INVALID, E_CUDA. */
+int32_t qwen3_op_attn_decode_plan(int32_t B, int32_t n_q_heads, int32_t n_kv_heads, int32_t max_len,
+                                  int32_t max_ctx);
+
 /* Split-KV decode attention of B new rows, as decode steps run it ("古法手撕简易LLM推理器",
  * 核心计算函数与Transformer层: the new key appended, then attention over the whole cache;
  * "从零开始写Qwen3", Attn: a one-row query sees every cached key; "手写Qwen3-0.6B推理",

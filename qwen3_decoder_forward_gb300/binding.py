@@ -125,6 +125,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qwen3_op_lmhead_argmax_noalloc": (ctypes.c_int, [_P, i32, i32, _P, i32, _P, _P, _P]),
         "qwen3_sample": (ctypes.c_int, [_P, i32, i32, _P, _P, _P, _P, _P, _P]),
         "qwen3_op_attn_decode_workspace_bytes": (sz, [i32, i32, i32]),
+        "qwen3_op_attn_decode_plan": (i32, [i32, i32, i32, i32, i32]),
         "qwen3_op_attn_decode": (ctypes.c_int, [_P, i32, _P, pi32, _P, pi32, _P, _P, _P, _P, _P, i32, i32, i32, i32,
                                                 ctypes.c_float, i32, _P, _P, sz, _P]),
     }
@@ -345,6 +346,15 @@ def qwen3_op_mlp_decode(h_ptr: int, M: int, C: int, gain_ptr: int, eps: float, w
 
 def qwen3_op_attn_decode_workspace_bytes(B: int, n_q_heads: int, n_kv_heads: int) -> int:
     return int(load_library().qwen3_op_attn_decode_workspace_bytes(B, n_q_heads, n_kv_heads))
+
+
+def qwen3_op_attn_decode_plan(B: int, n_q_heads: int, n_kv_heads: int, max_len: int, max_ctx: int) -> int:
+    """n_split a decode step of B rows whose longest context is max_len gives its attention
+    (0: equal shares of all keys); raises on a bad argument."""
+    rc = int(load_library().qwen3_op_attn_decode_plan(B, n_q_heads, n_kv_heads, max_len, max_ctx))
+    if rc < 0:
+        raise Qwen3Error(rc, qwen3_last_error(None))
+    return rc
 
 
 def qwen3_op_attn_decode(qkv_ptr: int, B: int, slots_ptr: int, slots_host: Sequence[int], positions_ptr: int,

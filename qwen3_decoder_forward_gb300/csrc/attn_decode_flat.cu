@@ -38,7 +38,7 @@ constexpr int FLAT_MAX_B = 1024;                // rows of one launch
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16(x)); }
 
-// CTA of S that flattened key x falls in: the largest s with floor(s W / S) <= x.
+// CTA of S (S <= W) that flattened key x falls in: the largest s with floor(s W / S) <= x.
 __device__ __forceinline__ int cta_of(long long x, long long W, int S) { return (int)(((x + 1) * S - 1) / W); }
 
 template <int G, bool PAGED>
@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_flat(
     constexpr int MAX_BLK = PAGED ? 1024 : 1;
     __shared__ int32_t s_blk[MAX_BLK];
 
-    const int S = gridDim.x, s = blockIdx.x, B = r.B;
+    const int S = gridDim.x, s = blockIdx.x, B = r.B;  // S CTAs; the first Se of them take keys
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int sub = lane & 7, kg = lane >> 3;
     const long long lim = wait_limit(err);
@@ -107,8 +107,12 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_flat(
         }
         __syncthreads();
     }
+    // With fewer keys than CTAs only the first W CTAs take keys (one or more each): a pair's
+    // segments must be exactly the CTAs of the consecutive range its keys fall in, so no CTA
+    // may be left with an empty range inside it.
     const long long W = (long long)Hkv * s_cum[B];
-    const long long r0 = W * s / S, r1 = W * (s + 1) / S;
+    const int Se = (int)(W < S ? W : S);
+    const long long r0 = s < Se ? W * s / Se : 0, r1 = s < Se ? W * (s + 1) / Se : 0;
 
     // the pair holding flattened key x: row b (largest with Hkv * cum[b] <= x), head g, key j
     auto locate = [&](long long x, int &b, int &g, int &j) {
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(NW * 32, 2) k_attn_decode_flat(
         const int j1 = (int)min((long long)n_keys, j0 + (r1 - x));  // this segment: keys [j0, j1)
         const int pos = n_keys - 1;
         const long long off = (long long)Hkv * s_cum[b] + (long long)g * n_keys;
-        const int first = cta_of(off, W, S), n_seg = cta_of(off + n_keys - 1, W, S) - first + 1;
+        const int first = cta_of(off, W, Se), n_seg = cta_of(off + n_keys - 1, W, Se) - first + 1;
         const int seg = s - first;
         x += j1 - j0;
         seg_slot = __ldcg(r.row_slot + b);

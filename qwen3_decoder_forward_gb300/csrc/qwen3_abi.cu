@@ -19,6 +19,9 @@ namespace {
 
 constexpr size_t ALIGN = 1024;
 constexpr int MAX_SPLIT = ATTN_DECODE_MAX_SPLIT;  // decode attention: key ranges per (sequence, head)
+// Decode steps whose (sequence, KV head) pairs times the bucketed longest context reach this
+// many keys take the decode attention over equal shares of all keys.
+constexpr long long FLAT_MIN_KEYS = 1ll << 21;
 constexpr int MAX_PARTS = 1024; // lm_head partial results per row
 
 size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
@@ -201,14 +204,32 @@ cudaError_t draw_next(qwen3_ctx *c, const Launch &lc, const float *logits, int B
     return launch_sample(ls, logits, B, c->cfg.vocab, sp.temperature, sp.top_k, sp.top_p, sp.uniform, next);
 }
 
-// The decode attention of layer l: over equal shares of all keys of the step where the head
-// ratio allows (every CTA streams the same number of K/V rows), else n_split key ranges per
-// (sequence, KV head).
+// Plan of the decode attention for B rows whose longest context is max_len: from a
+// power-of-two bucket of it, so a recorded graph stays valid while contexts grow inside the
+// bucket.  Returns 0 for equal shares of all keys of the step (flat_ok: the head ratio allows),
+// where the step streams enough keys to pay for that kernel's fixed costs (prefix sums, pairs
+// split across CTAs and merged): measured on 16 x 16K contexts it streams K/V 11% faster than
+// two ranges per pair on 256 of the 304 CTA slots, while at 32 x 1K, 8 x 4K or 4 x 8K (134 MB of
+// K/V) the ranges per pair are 10-18% faster.  Otherwise the ranges per (sequence, KV head) of
+// one wave: as many as the SMs hold CTAs for all pairs at once, ranges of at least 64 keys (the
+// kernel divides the actual keys 0..pos of each sequence evenly over them).
+int plan_decode_attention(int num_sms, int ctas_per_sm, bool flat_ok, int B, int Hkv, int max_len, int max_ctx) {
+    int bucket = 64;
+    while (bucket < max_len) bucket <<= 1;
+    bucket = std::min(bucket, max_ctx);
+    const long long pairs = (long long)B * Hkv;
+    if (flat_ok && pairs * bucket >= FLAT_MIN_KEYS) return 0;
+    const long long slots = (long long)num_sms * ctas_per_sm;
+    return (int)std::max(1ll, std::min({slots / pairs, (long long)MAX_SPLIT, (long long)(bucket + 63) / 64}));
+}
+
+// The decode attention of layer l: n_split key ranges per (sequence, KV head), or with n_split
+// 0 equal shares of all keys of the step (every CTA streams the same number of K/V rows).
 cudaError_t decode_attention(qwen3_ctx *c, const Launch &lc, const float *qkv, const Rows &rows, const float *g_q,
                              const float *g_k, const float2 *rope, int l, int n_split, bf16 *attn, uint32_t *err) {
     const qwen3_config &k = c->cfg;
     const Layout &L = c->lay;
-    if (c->flat_ctas > 0 && attn_decode_flat_supported(rows.B, k.n_q_heads, k.n_kv_heads))
+    if (n_split == 0)
         return launch_attn_decode_flat(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), c->flat_ctas,
                                        c->at<float>(L.o_wsml), c->at<float>(L.o_wso), c->at<int>(L.o_counters), attn,
                                        k.n_q_heads, k.n_kv_heads, k.max_ctx, k.rms_eps, err);
@@ -740,17 +761,10 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
     if (c->dump && c->dump_bytes < (size_t)(c->cfg.n_layers + 1) * B * c->cfg.hidden * 4)
         return c->fail(QWEN3_E_CAPACITY, "debug dump buffer too small for this call");
 
-    // Split plan of the decode attention: from a power-of-two bucket of the longest context,
-    // so a recorded graph stays valid while contexts grow inside the bucket.
-    int bucket = 64;
-    while (bucket < max_len) bucket <<= 1;
-    bucket = std::min(bucket, c->cfg.max_ctx);
-    // One wave of the decode attention: as many key ranges per (sequence, KV head) as the SMs
-    // hold CTAs for all pairs at once, ranges of at least 64 keys.  The kernel divides the
-    // actual keys 0..pos of each sequence evenly over the ranges.
-    const int pairs = B * c->cfg.n_kv_heads;
-    const int slots = c->num_sms * c->attn_ctas_per_sm;
-    const int n_split = std::max(1, std::min({slots / pairs, MAX_SPLIT, (bucket + 63) / 64}));
+    const int n_split = plan_decode_attention(c->num_sms, c->attn_ctas_per_sm,
+                                              c->flat_ctas > 0 &&
+                                                  attn_decode_flat_supported(B, c->cfg.n_q_heads, c->cfg.n_kv_heads),
+                                              B, c->cfg.n_kv_heads, max_len, c->cfg.max_ctx);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);
     if (kv_paged(c)) {  // a block for the appended position where a slot's last block is full
@@ -851,7 +865,11 @@ int qwen3_get_status(qwen3_ctx *c) {
         std::string m = "device error word set:";
         if (word & ERR_TOKEN_RANGE) m += " token id out of range (clamped);";
         if (word & ERR_POSITION) m += " position beyond max_ctx (KV write skipped);";
-        if (word & ERR_TIMEOUT) m += " a bounded wait in a kernel gave up (outputs of that call are not valid);";
+        if (word & ERR_TIMEOUT) {
+            m += " a bounded wait in a kernel gave up (outputs of that call are not valid);";
+            // the decode attention's merge counters may be left mid-count
+            cudaMemset(c->arena + c->lay.o_counters, 0, (size_t)c->cfg.max_seqs * c->cfg.n_kv_heads * 4);
+        }
         return c->fail(QWEN3_E_DEVICE, m);
     }
     return QWEN3_OK;
@@ -1067,6 +1085,26 @@ size_t qwen3_op_attn_decode_workspace_bytes(int32_t B, int32_t n_q_heads, int32_
     const size_t D = 128;
     return align_up((size_t)B * n_q_heads * MAX_SPLIT * 2 * 4) + align_up((size_t)B * n_q_heads * MAX_SPLIT * D * 4) +
            align_up((size_t)B * n_kv_heads * 4);
+}
+
+int32_t qwen3_op_attn_decode_plan(int32_t B, int32_t n_q_heads, int32_t n_kv_heads, int32_t max_len,
+                                  int32_t max_ctx) {
+    g_create_error.clear();
+    if (B < 1 || B > 1024 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads || max_len < 1 ||
+        max_ctx < max_len) {
+        g_create_error = "qwen3_op_attn_decode_plan: bad argument";
+        return QWEN3_E_INVALID;
+    }
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        g_create_error = std::string("qwen3_op_attn_decode_plan: ") + cudaGetErrorString(e);
+        return QWEN3_E_CUDA;
+    }
+    return plan_decode_attention(sms, attn_decode_ctas_per_sm(n_q_heads, n_kv_heads),
+                                 attn_decode_flat_supported(B, n_q_heads, n_kv_heads), B, n_kv_heads, max_len,
+                                 max_ctx);
 }
 
 int qwen3_op_attn_decode(const float *qkv, int32_t B, const int32_t *slots, const int32_t *slots_host,

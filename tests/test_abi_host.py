@@ -167,6 +167,12 @@ def test_attn_decode_op_rejects_bad_arguments_before_any_launch(lib):
         assert "qwen3_op_attn_decode" in binding.qwen3_last_error(None)
 
 
+def test_attn_decode_plan_rejects_bad_arguments(lib):
+    for args in ((0, 16, 8, 10, 64), (4, 16, 3, 10, 64), (4, 16, 8, 0, 64), (4, 16, 8, 65, 64), (1025, 16, 8, 1, 8)):
+        assert lib.qwen3_op_attn_decode_plan(*args) == binding.QWEN3_E_INVALID, args
+        assert "qwen3_op_attn_decode_plan" in binding.qwen3_last_error(None)
+
+
 def test_paged_kv_calls_reject_null(lib):
     assert lib.qwen3_kv_copy_rows(None, 0, 0, 0, 1, 16, 16, None) == binding.QWEN3_E_INVALID
     assert lib.qwen3_kv_free_blocks(None) == -1

@@ -118,16 +118,35 @@ def test_decode_mlp_vs_torch(M):
                                     out.data_ptr(), 0)
 
 
+def test_decode_attention_plan():
+    """Equal shares of all keys from 2^21 (row, KV head) pairs x bucketed context keys on, with
+    two query heads per KV head; otherwise one wave of key ranges per pair, at least 64 keys
+    a range."""
+    gc.ensure_library()
+    plan = binding.qwen3_op_attn_decode_plan
+    assert plan(16, 16, 8, 16401, 16416) == 0      # 128 pairs x 16,416 (bucket capped at max_ctx)
+    assert plan(16, 16, 8, 16384, 40960) == 0      # 128 x 16,384 = 2^21
+    assert plan(32, 16, 8, 1057, 2048) >= 1        # 256 x 2,048
+    assert plan(16, 16, 8, 16384, 40960) == 0
+    assert plan(16, 32, 8, 16401, 40960) >= 1      # four query heads per KV head: ranges only
+    one = plan(1, 16, 8, 64, 64)
+    assert one == 1                                 # a 64-key context: one range
+    assert plan(1, 16, 8, 4096, 4096) == min(64, 4096 // 64, plan(1, 16, 8, 40960, 40960))
+
+
 @pytest.mark.parametrize("positions,n_split", [([0, 64, 200], 0), ([63, 127, 129], 1), ([5, 250, 128], 7),
-                                               ([255, 1, 100], 64)])
+                                               ([255, 1, 100], 64), ([4000, 1, 3000], 0), ([4095, 2047, 128], 0)])
 def test_decode_attention_op_vs_oracle(positions, n_split):
     """qwen3_op_attn_decode against the oracle's per-head RMSNorm, rotate-half RoPE and causal
-    GQA attention, over cached rows drawn at random and the new row at `positions`."""
+    GQA attention, over cached rows drawn at random and the new row at `positions`.  With
+    n_split 0 the long rows are cut into many units of keys, more than one wave of CTAs takes at
+    first, merged per (row, KV head)."""
     import numpy as np
     from oracle import qwen3_oracle as oracle
 
     gc.ensure_library()
-    B, Hq, Hkv, D, max_ctx, eps, theta = len(positions), 16, 8, 128, 256, 1e-6, 1e6
+    max_ctx = 256 if max(positions) < 256 else 4096
+    B, Hq, Hkv, D, eps, theta = len(positions), 16, 8, 128, 1e-6, 1e6
     n_slots = B + 1
     slots = [2, 0, 3][:B]
     g = torch.Generator(device="cpu").manual_seed(sum(positions) + n_split)
