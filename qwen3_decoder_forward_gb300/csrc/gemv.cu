@@ -561,146 +561,207 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restr
 
 // ---- tensor-core lm_head + argmax for 9..32 rows -----------------------------------------
 //
-// Persistent CTAs walk 16-row tiles of the (tied) embedding table through a 4-stage ring
-// filled by bulk copies; each tile is multiplied with the 32 (zero-padded) rows of x on the
-// tensor cores (mma.sync, 4 warps splitting K), its logits optionally stored, and the running
-// best (value, index) of every batch row updated -- lowest index on ties.  One partial per
-// CTA and row goes to part_val/part_idx for the reduction kernel.
-constexpr int LM_STAGES = 4;
+// One CTA per SM walks 32-row tiles of the (tied) embedding table, tiles s, s + grid, ...: a
+// producer warp keeps a two-stage ring of them filled with bulk copies (one 2 KB row a lane),
+// and four MMA warps each multiply 16 of the tile's rows with 16 of the 32 (zero-padded) rows
+// of x over the whole K (mma.sync m16n8k16, four independent accumulator chains per n-tile),
+// store the logits when asked, and keep the running best (value, index) of their batch
+// columns in registers -- lowest index on ties.  A warp frees a stage with an mbarrier
+// arrival; nothing is reduced across warps until the end.  One partial per CTA and row goes
+// to part_val/part_idx for the reduction kernel.
+constexpr int LM_ROWS = 32, LM_STAGES = 2, LM_WARPS = 4, LM_BAR = 1;
+
+__device__ __forceinline__ bool lm_better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
 
 template <int KV>
-__global__ void __launch_bounds__(MMA_WARPS * 32) k_lmhead_mma(const bf16 *__restrict__ X, int M,
-                                                               const bf16 *__restrict__ E, int V,
-                                                               float *__restrict__ logits,
-                                                               float *__restrict__ part_val,
-                                                               int32_t *__restrict__ part_idx, uint32_t *err) {
+__global__ void __launch_bounds__((LM_WARPS + 1) * 32) k_lmhead_mma(const bf16 *__restrict__ X, int M,
+                                                                     const bf16 *__restrict__ E, int V,
+                                                                     float *__restrict__ logits,
+                                                                     float *__restrict__ part_val,
+                                                                     int32_t *__restrict__ part_idx, uint32_t *err) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int C = KV * 256;
-    constexpr int stride = C * 2 + 16;
+    constexpr int stride = C * 2 + 16;                 // padded row (bytes): conflict-free ldmatrix
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);  // [LM_STAGES]
-    uint64_t *xbar = full + LM_STAGES;
-    uint8_t *ring = smem + 128;                          // [LM_STAGES][16][stride]
-    uint8_t *xs = ring + LM_STAGES * MMA_ROWS * stride;  // [32][stride]
-    float *red = reinterpret_cast<float *>(xs + MMA_MPAD * stride);  // [warps][16][32]
-    __shared__ float best_v[MMA_MPAD];
-    __shared__ int best_i[MMA_MPAD];
+    uint64_t *empty = full + LM_STAGES;                   // [LM_STAGES]
+    uint64_t *xbar = empty + LM_STAGES;
+    uint8_t *ring = smem + 128;                                    // [LM_STAGES][LM_ROWS][stride]
+    uint8_t *xs = ring + (size_t)LM_STAGES * LM_ROWS * stride;    // [32][stride]
+    __shared__ float fin_v[2][MMA_MPAD];
+    __shared__ int fin_i[2][MMA_MPAD];
+    __shared__ volatile int s_abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = (V + MMA_ROWS - 1) / MMA_ROWS;
+    const int n_tiles = (V + LM_ROWS - 1) / LM_ROWS;
     const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-
-    auto issue = [&](int i) {  // local tile i into stage i % LM_STAGES (rows beyond V: not copied)
-        const int tile = blockIdx.x + i * gridDim.x, r0 = tile * MMA_ROWS;
-        const int nr = min(MMA_ROWS, V - r0);
-        uint64_t *b = &full[i % LM_STAGES];
-        if (lane == 0) mbar_expect_tx(b, (uint32_t)nr * C * 2);
-        __syncwarp();
-        if (lane < nr) bulk_g2s(ring + (i % LM_STAGES) * MMA_ROWS * stride + lane * stride, E + (size_t)(r0 + lane) * C, C * 2, b);
-    };
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < LM_STAGES; ++st) mbar_init(&full[st], 1);
-        mbar_init(xbar, 1);
-    }
     const long long lim = wait_limit(err);
-    if (threadIdx.x < MMA_MPAD) {
-        best_v[threadIdx.x] = -INFINITY;
-        best_i[threadIdx.x] = 0x7fffffff;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < LM_STAGES; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], LM_WARPS);
+        }
+        mbar_init(xbar, 1);
+        s_abort = 0;
     }
-    for (int i = threadIdx.x; i < (MMA_MPAD - M) * (C / 8); i += MMA_WARPS * 32)
+    for (int i = threadIdx.x; i < (MMA_MPAD - M) * (C / 8); i += blockDim.x)  // rows of x beyond M are zero
         *reinterpret_cast<uint4 *>(xs + (M + i / (C / 8)) * stride + (i % (C / 8)) * 16) = make_uint4(0, 0, 0, 0);
-    // stale rows of a partial last tile must be finite: zero every stage once
-    for (int i = threadIdx.x; i < LM_STAGES * MMA_ROWS * (C / 8); i += MMA_WARPS * 32)
-        *reinterpret_cast<uint4 *>(ring + (i / (C / 8)) * stride + (i % (C / 8)) * 16) = make_uint4(0, 0, 0, 0);
+    if (V % LM_ROWS)  // rows past V in a partial last tile must be finite: zero the stages once
+        for (int i = threadIdx.x; i < LM_STAGES * LM_ROWS * (C / 8); i += blockDim.x)
+            *reinterpret_cast<uint4 *>(ring + (i / (C / 8)) * stride + (i % (C / 8)) * 16) = make_uint4(0, 0, 0, 0);
     __syncthreads();
-    if (warp == 0)
-        for (int i = 0; i < min(LM_STAGES, my_tiles); ++i) issue(i);
-    pdl_wait();
-    pdl_trigger();
-    if (warp == 1) {
+
+    if (warp == LM_WARPS) {
+        // ---- producer: tiles into the ring, x after the dependency wait ----
+        auto issue = [&](int i) {
+            const int st = i % LM_STAGES, r0 = (blockIdx.x + i * gridDim.x) * LM_ROWS;
+            const int nr = min(LM_ROWS, V - r0);
+            if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)nr * C * 2);
+            __syncwarp();
+            if (lane < nr)
+                bulk_g2s(ring + ((size_t)st * LM_ROWS + lane) * stride, E + (size_t)(r0 + lane) * C, C * 2, &full[st]);
+        };
+        int issued = min(LM_STAGES, my_tiles);
+        for (int i = 0; i < issued; ++i) issue(i);
+        pdl_wait();
+        pdl_trigger();
         if (lane == 0) mbar_expect_tx(xbar, (uint32_t)M * C * 2);
         __syncwarp();
         if (lane < M) bulk_g2s(xs + lane * stride, X + (size_t)lane * C, C * 2, xbar);
-    }
-    bool ok = __syncthreads_and(mbar_wait_ctx(xbar, 0, err, lim));
-    const uint32_t xsa = smem_addr(xs);
-    const int g = lane >> 2, t = lane & 3;
-    int stop = 0;  // first tile not consumed: tiles stop .. stop + LM_STAGES - 1 may be in flight
-    for (int i = 0; ok && i < my_tiles; ++i) {
-        const int st = i % LM_STAGES;
-        stop = i;
-        ok = __syncthreads_and(mbar_wait_ctx(&full[st], (i / LM_STAGES) & 1, err, lim));
-        if (!ok) break;
-        const uint32_t wsa = smem_addr(ring + st * MMA_ROWS * stride);
-        float acc[4][4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-#pragma unroll
-        for (int kk = warp * (C / MMA_WARPS); kk < (warp + 1) * (C / MMA_WARPS); kk += 16) {
-            uint32_t a[4];
-            ldsm_x4(a, wsa + (lane & 15) * stride + (kk + (lane >> 4) * 8) * 2);
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-                uint32_t b[4];
-                const int n = nb * 16 + (lane & 7) + ((lane >> 4) << 3);
-                ldsm_x4(b, xsa + n * stride + (kk + ((lane >> 3) & 1) * 8) * 2);
-                mma16816(acc[nb * 2], a, b[0], b[1]);
-                mma16816(acc[nb * 2 + 1], a, b[2], b[3]);
-            }
-        }
-        float *rw = red + warp * MMA_ROWS * MMA_MPAD;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            rw[g * MMA_MPAD + j * 8 + 2 * t] = acc[j][0];
-            rw[g * MMA_MPAD + j * 8 + 2 * t + 1] = acc[j][1];
-            rw[(g + 8) * MMA_MPAD + j * 8 + 2 * t] = acc[j][2];
-            rw[(g + 8) * MMA_MPAD + j * 8 + 2 * t + 1] = acc[j][3];
-        }
-        __syncthreads();  // partial tiles in place; the stage is free
-        if (warp == 0 && i + LM_STAGES < my_tiles) issue(i + LM_STAGES);
-        const int r0 = (blockIdx.x + i * gridDim.x) * MMA_ROWS;
-        // sum the warps' partials; thread handles 4 (row, batch) outputs
-        for (int o = threadIdx.x; o < MMA_ROWS * MMA_MPAD; o += MMA_WARPS * 32) {
-            float v = 0.0f;
-#pragma unroll
-            for (int w = 0; w < MMA_WARPS; ++w) v += red[w * MMA_ROWS * MMA_MPAD + o];
-            red[o] = v;  // warp 0's slot holds the sum (each o read and written by one thread)
-            const int r = o / MMA_MPAD, b = o % MMA_MPAD;
-            if (logits && b < M && r0 + r < V) logits[(size_t)b * V + r0 + r] = v;
-        }
-        __syncthreads();
-        if (threadIdx.x < MMA_MPAD && threadIdx.x < M) {  // running best of batch row b
-            const int b = threadIdx.x;
-            float bv = best_v[b];
-            int bi = best_i[b];
-            for (int r = 0; r < MMA_ROWS && r0 + r < V; ++r) {
-                const float v = red[r * MMA_MPAD + b];
-                if (v > bv) {  // rows increase within and across a CTA's tiles: strict > keeps the lowest
-                    bv = v;
-                    bi = r0 + r;
+        for (int i = LM_STAGES; i < my_tiles; ++i) {
+            // the stage is free once the MMA warps are done with tile i - LM_STAGES
+            bool ok = true;
+            if (lane == 0) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(&empty[i % LM_STAGES], (uint32_t)((i / LM_STAGES - 1) & 1))) {
+                    if (s_abort) { ok = false; break; }
+                    if (clock64() - t0 > lim) {
+                        if (err) atomicOr(err, ERR_TIMEOUT);
+                        ok = false;
+                        break;
+                    }
                 }
             }
-            best_v[b] = bv;
-            best_i[b] = bi;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            issue(i);
+            issued = i + 1;
         }
-        __syncthreads();  // red is rewritten by the next tile
-    }
-    if (!ok) {
-        // Let the copies in flight land: the latest issued phase of each stage.  Then report the
-        // failure through the partials: (+inf, -1) wins the reduction, so the row's token is -1.
-        if (threadIdx.x == 0) {
-            for (int j = stop; j < min(stop + LM_STAGES, my_tiles); ++j)
-                mbar_wait_bounded(&full[j % LM_STAGES], (j / LM_STAGES) & 1, nullptr);
+        // the copies in flight land before the CTA may exit (the MMA warps took them all
+        // unless a wait gave up)
+        if (lane == 0) {
+            for (int j = max(0, issued - LM_STAGES); j < issued; ++j)
+                mbar_wait_bounded(&full[j % LM_STAGES], (uint32_t)((j / LM_STAGES) & 1), nullptr);
             mbar_wait_bounded(xbar, 0, nullptr);
-        }
-        __syncthreads();
-        if (threadIdx.x < M) {
-            part_val[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = INFINITY;
-            part_idx[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = -1;
         }
         return;
     }
+
+    // ---- MMA warps: rows 16 mt .. of each tile, batch columns 16 nh .. 16 nh + 15 ----
+    const int mt = warp & 1, nh = warp >> 1;
+    const bool active = 16 * nh < M;
+    const int g = lane >> 2, t = lane & 3;
+    float bv[2][2];
+    int bi[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            bv[nt][j] = -INFINITY;
+            bi[nt][j] = 0x7fffffff;
+        }
+    bool ok = !__any_sync(0xffffffffu, !mbar_wait_ctx(xbar, 0, err, lim));
+    const uint32_t xsa = smem_addr(xs) + (16 * nh + (lane & 7) + ((lane >> 4) << 3)) * stride + ((lane >> 3) & 1) * 16;
+    for (int i = 0; ok && i < my_tiles; ++i) {
+        const int st = i % LM_STAGES;
+        if (__any_sync(0xffffffffu, !mbar_wait_ctx(&full[st], (uint32_t)((i / LM_STAGES) & 1), err, lim))) {
+            ok = false;
+            break;
+        }
+        if (active) {
+            const uint32_t wsa =
+                smem_addr(ring + ((size_t)st * LM_ROWS + mt * 16 + (lane & 15)) * stride) + (lane >> 4) * 16;
+            float acc[2][4][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) acc[nt][ch][0] = acc[nt][ch][1] = acc[nt][ch][2] = acc[nt][ch][3] = 0.0f;
+#pragma unroll 2
+            for (int kk = 0; kk < C; kk += 64) {
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const int k = kk + ch * 16;
+                    uint32_t a[4], b[4];
+                    ldsm_x4(a, wsa + k * 2);
+                    ldsm_x4(b, xsa + k * 2);
+                    mma16816(acc[0][ch], a, b[0], b[1]);
+                    mma16816(acc[1][ch], a, b[2], b[3]);
+                }
+            }
+            const int r0 = (blockIdx.x + i * gridDim.x) * LM_ROWS + mt * 16;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int e = 2 * h + j;
+                        const float v = acc[nt][0][e] + acc[nt][1][e] + acc[nt][2][e] + acc[nt][3][e];
+                        const int row = r0 + g + 8 * h, b = 16 * nh + 8 * nt + 2 * t + j;
+                        if (row < V && b < M) {
+                            if (logits) logits[(size_t)b * V + row] = v;
+                            if (lm_better(v, row, bv[nt][j], bi[nt][j])) {
+                                bv[nt][j] = v;
+                                bi[nt][j] = row;
+                            }
+                        }
+                    }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta(&empty[st]);
+    }
+    if (!ok && lane == 0) s_abort = 1;  // the producer stops issuing
+    // best of each batch column over the warp's rows (lanes with the same t), then the two halves
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv[nt][j], o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi[nt][j], o);
+                if (lm_better(ov, oi, bv[nt][j], bi[nt][j])) {
+                    bv[nt][j] = ov;
+                    bi[nt][j] = oi;
+                }
+            }
+    if (active && lane < 4)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int b = 16 * nh + 8 * nt + 2 * t + j;
+                if (b < M) {
+                    fin_v[mt][b] = bv[nt][j];
+                    fin_i[mt][b] = bi[nt][j];
+                }
+            }
+    uint32_t any_fail;
+    asm volatile("{ .reg .pred a, b; setp.eq.u32 a, %1, 0; bar.red.or.pred b, %2, %3, a; selp.u32 %0, 1, 0, b; }"
+                 : "=r"(any_fail)
+                 : "r"((uint32_t)ok), "n"(LM_BAR), "n"(LM_WARPS * 32)
+                 : "memory");
     if (threadIdx.x < M) {
-        part_val[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = best_v[threadIdx.x];
-        part_idx[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = best_i[threadIdx.x];
+        const int b = threadIdx.x;
+        float v = fin_v[0][b];
+        int ix = fin_i[0][b];
+        if (lm_better(fin_v[1][b], fin_i[1][b], v, ix)) {
+            v = fin_v[1][b];
+            ix = fin_i[1][b];
+        }
+        if (any_fail) {  // (+inf, -1) wins the reduction: the row's token is -1
+            v = INFINITY;
+            ix = -1;
+        }
+        part_val[(size_t)b * gridDim.x + blockIdx.x] = v;
+        part_idx[(size_t)b * gridDim.x + blockIdx.x] = ix;
     }
 }
 
@@ -708,13 +769,14 @@ cudaError_t launch_lmhead_mma(const Launch &lc, const bf16 *X, int M, int C, con
                               float *part_val, int32_t *part_idx, int n_parts, uint32_t *err) {
     if (C != 1024 || M < 1 || M > MMA_MPAD) return cudaErrorInvalidValue;
     constexpr int KV = 4;
-    const size_t smem = 128 + (size_t)(LM_STAGES * MMA_ROWS + MMA_MPAD) * (KV * 256 * 2 + 16) +
-                        MMA_WARPS * MMA_ROWS * MMA_MPAD * 4;
+    const size_t smem = 128 + (size_t)(LM_STAGES * LM_ROWS + MMA_MPAD) * (KV * 256 * 2 + 16);
     cudaError_t e = cudaFuncSetAttribute(k_lmhead_mma<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch(lc, k_lmhead_mma<KV>, dim3(n_parts), dim3(MMA_WARPS * 32), smem, X, M, E, V, logits, part_val,
+    return launch(lc, k_lmhead_mma<KV>, dim3(n_parts), dim3((LM_WARPS + 1) * 32), smem, X, M, E, V, logits, part_val,
                   part_idx, err);
 }
+
+int lmhead_mma_parts(int num_sms) { return num_sms; }
 
 template <int EPI, int KS>
 cudaError_t run_mma(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N, void *out, uint32_t *err) {

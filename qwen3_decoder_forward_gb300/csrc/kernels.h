@@ -183,6 +183,8 @@ bool gemv_mma_supported(int M, int K, int N);
 // value, index) per CTA and row, as launch_lmhead_argmax's pass 1 writes them.
 cudaError_t launch_lmhead_mma(const Launch &lc, const bf16 *X, int M, int C, const bf16 *E, int V, float *logits,
                               float *part_val, int32_t *part_idx, int n_parts, uint32_t *err);
+// CTAs (and partials per row) of launch_lmhead_mma: one per SM.
+int lmhead_mma_parts(int num_sms);
 cudaError_t launch_gemv_mma(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N, int epi,
                             void *out, uint32_t *err);
 

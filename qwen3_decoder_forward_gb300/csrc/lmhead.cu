@@ -139,7 +139,9 @@ cudaError_t run(const Launch &lc, const bf16 *X, int B, const bf16 *E, int V, fl
     cudaError_t e;
     constexpr int C = KV * 256;
     if (B > 8 && C == 1024) {
-        // 9..32 rows per pass on the tensor cores (the SIMT pass is compute-bound there)
+        // 9..32 rows per pass on the tensor cores (the SIMT pass is compute-bound there), one
+        // wave of CTAs: one partial per SM and row
+        n_parts = n_parts < lmhead_mma_parts(lc.num_sms) ? n_parts : lmhead_mma_parts(lc.num_sms);
         for (int b0 = 0; b0 < B; b0 += MAX_B) {
             const int bc = B - b0 < MAX_B ? B - b0 : MAX_B;
             e = launch_lmhead_mma(lc, X + (size_t)b0 * C, bc, C, E, V, logits ? logits + (size_t)b0 * V : nullptr,
