@@ -46,8 +46,7 @@ L2_BYTES = 129 * 2 ** 20
 # writes 86 MB of its 144 MB output before it ends (the rest leaves L2 later).  The decode
 # attention entries are DRAM bytes per (sequence, position) row of one layer's K and V, scaled
 # by the rows a launch reads (the traffic grows in proportion with the rows).
-TRAFFIC_BYTES = {"gemm_gate_up": 147362304, "mlp_fused": 18910976, "attn_decode_flat_per_key_row": 4099.9,
-                 "attn_decode_fused_per_key_row": 4108.2}
+TRAFFIC_BYTES = {"gemm_gate_up": 147362304, "mlp_fused": 18910976, "attn_decode_per_key_row": 4110.9}
 
 
 def parse_args():
@@ -409,7 +408,7 @@ def measure_mlp_roofline(torch, binding, wl, peaks, peak_kind):
 def measure_attn_roofline(torch, binding, wl, peaks, peak_kind, ctx=None, reps=20):
     """Average duration of the decode attention kernel (QK-norm + RoPE + KV write + attention
     over keys 0..p), the kernel that streams the KV cache, as a decode step of the workload
-    plans it (qwen3_op_attn_decode_plan: equal shares of all keys, or key ranges per pair), at
+    plans it (qwen3_op_attn_decode_plan: key ranges per (sequence, KV head)), at
     the workload's batch and the positions of its middle decode step (or every row at position
     ctx - 1), over one layer's K/V rows of the workload's size in their own buffer (larger than
     L2 for the long contexts), through qwen3_op_attn_decode."""
@@ -453,11 +452,9 @@ def measure_attn_roofline(torch, binding, wl, peaks, peak_kind, ctx=None, reps=2
     algo_bytes = rows * Hkv * D * 2 * 2  # K and V rows 0..p of every (sequence, KV head), the new one written
     achieved = algo_bytes / avg_s / 1e9
     peak = float(peaks["hbm_gbs"])
-    key = "attn_decode_flat_per_key_row" if n_split == 0 else "attn_decode_fused_per_key_row"
-    per_row = TRAFFIC_BYTES.get(key)
+    per_row = TRAFFIC_BYTES.get("attn_decode_per_key_row")
     del kc, vc
-    name = ("k_attn_decode_flat (equal shares of all keys" if n_split == 0 else
-            f"k_attn_decode_fused ({n_split} key range{'s' if n_split > 1 else ''} per pair")
+    name = f"k_attn_decode_fused ({n_split} key range{'s' if n_split > 1 else ''} per pair, tensor cores"
     return {"kernel": f"{name}; QK-norm + RoPE + KV write + attention, {B} rows at "
                       f"positions {min(positions)}..{max(positions)}, {Hq}/{Hkv} heads, one layer)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

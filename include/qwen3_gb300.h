@@ -427,10 +427,9 @@ int qwen3_op_lmhead_argmax_noalloc(const void *x_dev, int32_t B, int32_t C,
 size_t qwen3_op_attn_decode_workspace_bytes(int32_t B, int32_t n_q_heads, int32_t n_kv_heads);
 
 /* The n_split a decode step of B rows whose longest context is max_len tokens (the new one
- * included; 1 <= max_len <= max_ctx) gives its decode attention on the current device: 0 for
- * equal shares of all the step's keys (with Hq == 2 Hkv, where the (row, KV head) pairs times
- * the context rounded up to a power of two reach 2^21 keys), else the key ranges per (row, KV
- * head) of one wave of CTAs, 1..64.  Passed to qwen3_op_attn_decode it runs the kernel a
+ * included; 1 <= max_len <= max_ctx) gives its decode attention on the current device: the key
+ * ranges per (row, KV head) of one wave of CTAs, 1..64 (from the context rounded up to a power
+ * of two, ranges of at least 64 keys).  Passed to qwen3_op_attn_decode it runs the launch a
  * step would.  Errors (negative): E_INVALID, E_CUDA. */
 int32_t qwen3_op_attn_decode_plan(int32_t B, int32_t n_q_heads, int32_t n_kv_heads, int32_t max_len,
                                   int32_t max_ctx);
@@ -446,13 +445,15 @@ int32_t qwen3_op_attn_decode_plan(int32_t B, int32_t n_q_heads, int32_t n_kv_hea
  * qkv_dev fp32 [B, (Hq + 2 Hkv) * 128] (q heads, then k, then v); q_gain_dev, k_gain_dev fp32
  * [128]; rope_dev fp32 [max_ctx][64][2] = (cos, sin) of p * theta^(-2i/128); k_cache_dev,
  * v_cache_dev bf16 [n_slots][Hkv][max_ctx][128] (rows 0..p-1 of each used slot hold the
- * cached keys and values; row p is written); out_dev bf16 [B, Hq, 128].  slots and positions
+ * cached keys and values; row p is written; the last 64-key chunk of a range may read up to 63
+ * rows past its keys, masked, so every row of the cache must hold finite values, e.g. zeros
+ * before first use); out_dev bf16 [B, Hq, 128].  slots and positions
  * are given on the device and on the host (same values; slots distinct, 0 <= slot < n_slots,
- * 0 <= position < max_ctx).  n_split key ranges per (row, KV head), 1..64; or 0 as a decode
- * step runs it: with Hq == 2 Hkv, one wave of CTAs each taking an equal share of all the
- * launch's keys (the keys of all (row, KV head) pairs laid end to end, a pair split over the
- * CTAs its keys fall in), otherwise one wave of equal ranges per pair.  workspace_dev: qwen3_op_attn_decode_workspace_bytes
- * bytes, 256-byte aligned, zero-filled before its first use (calls leave it reusable).
+ * 0 <= position < max_ctx).  n_split key ranges per (row, KV head), 1..64 (whole 64-key
+ * chunks: ceil((p+1)/n_split) rounded up to a multiple of 64 keys each); or 0 as a decode step
+ * plans it for these rows (qwen3_op_attn_decode_plan with the largest position + 1).
+ * workspace_dev: qwen3_op_attn_decode_workspace_bytes bytes, 256-byte aligned, zero-filled
+ * before its first use (calls leave it reusable).
  * head_dim 128; Hq/Hkv in {1, 2, 4, 8}.  Errors: E_INVALID (NULL, bad size or index), E_CUDA. */
 int qwen3_op_attn_decode(const float *qkv_dev, int32_t B, const int32_t *slots_dev,
                          const int32_t *slots_host, const int32_t *positions_dev,

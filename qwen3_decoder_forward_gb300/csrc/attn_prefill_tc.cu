@@ -446,6 +446,18 @@ bool map2d(CUtensorMap *m, const bf16 *base, uint64_t rows, uint64_t cols) {
 
 }  // namespace
 
+bool kv_tile_map(CUtensorMap *m, const bf16 *base, uint64_t rows) {
+    EncodeTiledFn fn = encode();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16 *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool attn_prefill_tc_supported(int Hq, int Hkv) { return Hq == 2 * Hkv && encode() != nullptr; }
 
 cudaError_t launch_attn_prefill_tc(const Launch &lc, const bf16 *q, int N, const bf16 *k_layer,

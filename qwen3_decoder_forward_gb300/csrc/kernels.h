@@ -1,6 +1,7 @@
 // Host-side launchers of the Qwen3 decoder-forward kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -203,6 +204,9 @@ cudaError_t launch_attn_prefill(const Launch &lc, const bf16 *q, const bf16 *k_l
                                 int Hkv, int max_ctx);
 
 // --- attn_prefill_tc.cu (tcgen05 flash attention; q has N rows) ----------------------------
+// Tensor map of a layer's K or V rows ([rows][128] bf16): boxes of 64 rows x 64 columns with
+// the 128-byte swizzle (the decode attention's chunks).
+bool kv_tile_map(CUtensorMap *m, const bf16 *base, uint64_t rows);
 bool attn_prefill_tc_supported(int Hq, int Hkv);
 // Rows of sequence b are positions row_pos[cu[b]] .. of its slot (non-zero when a call
 // continues a slot); keys come from the cache, causal mask aligned bottom-right.
@@ -224,21 +228,12 @@ int attn_decode_ctas_per_sm(int Hq, int Hkv);
 // merge of the n_split key ranges (balanced over keys 0..pos on the device) by the last CTA
 // of each (sequence, KV head).  counters
 // [max_seqs * Hkv] must be zero on entry and are left zero.
+// kv_rows: rows ([128] bf16) of the layer's K and V arrays, the extent of their tensor maps.
 cudaError_t launch_attn_decode_fused(const Launch &lc, const float *qkv, const Rows &r,
                                      const float *q_gain, const float *k_gain, const float2 *rope,
-                                     bf16 *k_layer, bf16 *v_layer, int n_split,
+                                     bf16 *k_layer, bf16 *v_layer, size_t kv_rows, int n_split,
                                      float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
                                      int Hkv, int max_ctx, float eps, uint32_t *err);
-
-// --- attn_decode_flat.cu (decode attention over equal shares of all keys; Hq == 2 Hkv) -----
-// Same contract as launch_attn_decode_fused, with n_ctas CTAs in all (at most
-// (ATTN_DECODE_MAX_SPLIT - 2) * Hkv) instead of n_split per (sequence, KV head).
-bool attn_decode_flat_supported(int B, int Hq, int Hkv);
-int attn_decode_flat_ctas_per_sm();
-cudaError_t launch_attn_decode_flat(const Launch &lc, const float *qkv, const Rows &r, const float *q_gain,
-                                    const float *k_gain, const float2 *rope, bf16 *k_layer, bf16 *v_layer,
-                                    int n_ctas, float *ws_ml, float *ws_o, int *counters, bf16 *out, int Hq,
-                                    int Hkv, int max_ctx, float eps, uint32_t *err);
 
 // --- decode_block.cu (decode of 1-2 rows: one attention-block and one MLP-block kernel per layer)
 // Hidden 1024, head_dim 128, two query heads per KV head.  Row b appends to slot slots[b] at

@@ -19,9 +19,6 @@ namespace {
 
 constexpr size_t ALIGN = 1024;
 constexpr int MAX_SPLIT = ATTN_DECODE_MAX_SPLIT;  // decode attention: key ranges per (sequence, head)
-// Decode steps whose (sequence, KV head) pairs times the bucketed longest context reach this
-// many keys take the decode attention over equal shares of all keys.
-constexpr long long FLAT_MIN_KEYS = 1ll << 21;
 constexpr int MAX_PARTS = 1024; // lm_head partial results per row
 
 size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
@@ -157,7 +154,7 @@ struct qwen3_ctx {
     Layout lay;
     uint8_t *arena = nullptr;
     std::vector<int32_t> len_host;
-    int num_sms = 0, n_parts = 0, attn_ctas_per_sm = 1, flat_ctas = 0;
+    int num_sms = 0, n_parts = 0, attn_ctas_per_sm = 1;
     float *dump = nullptr;
     size_t dump_bytes = 0;
     cudaStream_t cap_stream = nullptr;
@@ -206,36 +203,27 @@ cudaError_t draw_next(qwen3_ctx *c, const Launch &lc, const float *logits, int B
 
 // Plan of the decode attention for B rows whose longest context is max_len: from a
 // power-of-two bucket of it, so a recorded graph stays valid while contexts grow inside the
-// bucket.  Returns 0 for equal shares of all keys of the step (flat_ok: the head ratio allows),
-// where the step streams enough keys to pay for that kernel's fixed costs (prefix sums, pairs
-// split across CTAs and merged): measured on 16 x 16K contexts it streams K/V 11% faster than
-// two ranges per pair on 256 of the 304 CTA slots, while at 32 x 1K, 8 x 4K or 4 x 8K (134 MB of
-// K/V) the ranges per pair are 10-18% faster.  Otherwise the ranges per (sequence, KV head) of
-// one wave: as many as the SMs hold CTAs for all pairs at once, ranges of at least 64 keys (the
-// kernel divides the actual keys 0..pos of each sequence evenly over them).
-int plan_decode_attention(int num_sms, int ctas_per_sm, bool flat_ok, int B, int Hkv, int max_len, int max_ctx) {
+// bucket; the key ranges per (sequence, KV head) of one wave: as many as the SMs hold CTAs for
+// all pairs at once, ranges of at least 64 keys (the kernel divides the actual keys 0..pos of
+// each sequence evenly over them, in whole 64-key chunks).
+int plan_decode_attention(int num_sms, int ctas_per_sm, int B, int Hkv, int max_len, int max_ctx) {
     int bucket = 64;
     while (bucket < max_len) bucket <<= 1;
     bucket = std::min(bucket, max_ctx);
     const long long pairs = (long long)B * Hkv;
-    if (flat_ok && pairs * bucket >= FLAT_MIN_KEYS) return 0;
     const long long slots = (long long)num_sms * ctas_per_sm;
     return (int)std::max(1ll, std::min({slots / pairs, (long long)MAX_SPLIT, (long long)(bucket + 63) / 64}));
 }
 
-// The decode attention of layer l: n_split key ranges per (sequence, KV head), or with n_split
-// 0 equal shares of all keys of the step (every CTA streams the same number of K/V rows).
+// The decode attention of layer l: n_split key ranges per (sequence, KV head).
 cudaError_t decode_attention(qwen3_ctx *c, const Launch &lc, const float *qkv, const Rows &rows, const float *g_q,
                              const float *g_k, const float2 *rope, int l, int n_split, bf16 *attn, uint32_t *err) {
     const qwen3_config &k = c->cfg;
     const Layout &L = c->lay;
-    if (n_split == 0)
-        return launch_attn_decode_flat(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), c->flat_ctas,
-                                       c->at<float>(L.o_wsml), c->at<float>(L.o_wso), c->at<int>(L.o_counters), attn,
-                                       k.n_q_heads, k.n_kv_heads, k.max_ctx, k.rms_eps, err);
-    return launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l), n_split,
-                                    c->at<float>(L.o_wsml), c->at<float>(L.o_wso), c->at<int>(L.o_counters), attn,
-                                    k.n_q_heads, k.n_kv_heads, k.max_ctx, k.rms_eps, err);
+    return launch_attn_decode_fused(lc, qkv, rows, g_q, g_k, rope, c->kcache(l), c->vcache(l),
+                                    L.kv_layer_bytes / (k.head_dim * 2), n_split, c->at<float>(L.o_wsml),
+                                    c->at<float>(L.o_wso), c->at<int>(L.o_counters), attn, k.n_q_heads,
+                                    k.n_kv_heads, k.max_ctx, k.rms_eps, err);
 }
 
 // Everything one call runs, in stream order.  `decode` selects the GEMV projections and the
@@ -594,9 +582,6 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
     c->num_sms = prop.multiProcessorCount;
     c->n_parts = std::min(lmhead_parts(c->num_sms), MAX_PARTS);
     c->attn_ctas_per_sm = attn_decode_ctas_per_sm(cfg->n_q_heads, cfg->n_kv_heads);
-    // the balanced decode attention: one wave of CTAs over all keys of a step
-    if (attn_decode_flat_supported(1, cfg->n_q_heads, cfg->n_kv_heads))
-        c->flat_ctas = std::min(c->num_sms * attn_decode_flat_ctas_per_sm(), (MAX_SPLIT - 2) * cfg->n_kv_heads);
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);
     Launch lc;
     lc.stream = st;
@@ -761,10 +746,8 @@ int qwen3_decode_step(qwen3_ctx *c, const int32_t *tokens_dev, const int32_t *sl
     if (c->dump && c->dump_bytes < (size_t)(c->cfg.n_layers + 1) * B * c->cfg.hidden * 4)
         return c->fail(QWEN3_E_CAPACITY, "debug dump buffer too small for this call");
 
-    const int n_split = plan_decode_attention(c->num_sms, c->attn_ctas_per_sm,
-                                              c->flat_ctas > 0 &&
-                                                  attn_decode_flat_supported(B, c->cfg.n_q_heads, c->cfg.n_kv_heads),
-                                              B, c->cfg.n_kv_heads, max_len, c->cfg.max_ctx);
+    const int n_split =
+        plan_decode_attention(c->num_sms, c->attn_ctas_per_sm, B, c->cfg.n_kv_heads, max_len, c->cfg.max_ctx);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream_v);
     if (kv_paged(c)) {  // a block for the appended position where a slot's last block is full
@@ -1102,8 +1085,7 @@ int32_t qwen3_op_attn_decode_plan(int32_t B, int32_t n_q_heads, int32_t n_kv_hea
         g_create_error = std::string("qwen3_op_attn_decode_plan: ") + cudaGetErrorString(e);
         return QWEN3_E_CUDA;
     }
-    return plan_decode_attention(sms, attn_decode_ctas_per_sm(n_q_heads, n_kv_heads),
-                                 attn_decode_flat_supported(B, n_q_heads, n_kv_heads), B, n_kv_heads, max_len,
+    return plan_decode_attention(sms, attn_decode_ctas_per_sm(n_q_heads, n_kv_heads), B, n_kv_heads, max_len,
                                  max_ctx);
 }
 
@@ -1128,11 +1110,9 @@ int qwen3_op_attn_decode(const float *qkv, int32_t B, const int32_t *slots, cons
             return QWEN3_E_INVALID;
         }
     const Launch lc = op_launch(stream);
-    const bool flat = n_split == 0 && attn_decode_flat_supported(B, n_q_heads, n_kv_heads);
-    if (n_split == 0 && !flat) {  // one wave of CTAs, as a decode step plans it for contexts up to max_ctx
-        const int slots_all = lc.num_sms * attn_decode_ctas_per_sm(n_q_heads, n_kv_heads);
-        n_split = std::max(1, std::min({slots_all / (B * n_kv_heads), MAX_SPLIT, (max_ctx + 63) / 64}));
-    }
+    if (n_split == 0)  // as a decode step plans it for rows whose longest context is the largest position + 1
+        n_split = plan_decode_attention(lc.num_sms, attn_decode_ctas_per_sm(n_q_heads, n_kv_heads), B, n_kv_heads,
+                                        *std::max_element(positions_host, positions_host + B) + 1, max_ctx);
     const size_t D = 128;
     float *ws_ml = static_cast<float *>(ws);
     float *ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + align_up((size_t)B * n_q_heads * MAX_SPLIT * 2 * 4));
@@ -1143,16 +1123,10 @@ int qwen3_op_attn_decode(const float *qkv, int32_t B, const int32_t *slots, cons
     r.row_pos = const_cast<int32_t *>(positions);
     r.B = B;
     r.rows = B;
-    const cudaError_t e =
-        flat ? launch_attn_decode_flat(lc, qkv, r, q_gain, k_gain, reinterpret_cast<const float2 *>(rope),
-                                       static_cast<bf16 *>(k_cache), static_cast<bf16 *>(v_cache),
-                                       std::min(lc.num_sms * attn_decode_flat_ctas_per_sm(), (MAX_SPLIT - 2) * n_kv_heads),
-                                       ws_ml, ws_o, counters, static_cast<bf16 *>(out), n_q_heads, n_kv_heads, max_ctx,
-                                       eps, nullptr)
-             : launch_attn_decode_fused(lc, qkv, r, q_gain, k_gain, reinterpret_cast<const float2 *>(rope),
-                                        static_cast<bf16 *>(k_cache), static_cast<bf16 *>(v_cache), n_split, ws_ml,
-                                        ws_o, counters, static_cast<bf16 *>(out), n_q_heads, n_kv_heads, max_ctx, eps,
-                                        nullptr);
+    const cudaError_t e = launch_attn_decode_fused(
+        lc, qkv, r, q_gain, k_gain, reinterpret_cast<const float2 *>(rope), static_cast<bf16 *>(k_cache),
+        static_cast<bf16 *>(v_cache), (size_t)n_slots * n_kv_heads * max_ctx, n_split, ws_ml, ws_o, counters,
+        static_cast<bf16 *>(out), n_q_heads, n_kv_heads, max_ctx, eps, nullptr);
     if (e != cudaSuccess) {
         g_create_error = std::string("qwen3_op_attn_decode: ") + cudaGetErrorString(e);
         return QWEN3_E_CUDA;

@@ -124,8 +124,9 @@ def test_decode_one_row_layer_matches_chain(model_weights):
     and on the four-kernel chain agree, and the layer launched kernel by kernel agrees with its
     graph.  The residual adds of both paths land as fp32 atomics in an unspecified order, so two
     runs differ in the last bits; over 28 layers the bf16 roundings of GEMM operands that this
-    flips add up to a few 1e-3 of the logits (each run stays within the 1e-2 oracle gate):
-    within 5e-3, half the gate."""
+    flips add up to a few 1e-3 of the logits, and the chain's attention takes q and P in bf16
+    on the tensor cores where the layer's works in fp32 (each run stays within the 1e-2 oracle
+    gate): within 8e-3 between the paths, 5e-3 between the layer's graph and its launches."""
     w, _ = model_weights
     prompt = _prompts([300], 260)[0]
     outs = []
@@ -144,7 +145,7 @@ def test_decode_one_row_layer_matches_chain(model_weights):
         m.close()
         outs.append(got)
     for a, b, c in zip(*outs):
-        assert gc.rel_l2(a, b) <= 5e-3
+        assert gc.rel_l2(a, b) <= 8e-3
         assert gc.rel_l2(a, c) <= 5e-3
 
 

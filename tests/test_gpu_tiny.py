@@ -94,17 +94,19 @@ def test_graph_replay_matches_direct_launches(setup):
 
 
 def test_decode_paths_agree(setup):
-    """The two-kernel layer and the kernel chain agree.  They round at the same points, but
-    take their fp32 sums in different orders, so now and then a value stored in bf16 (the normed
-    projection inputs, the SwiGLU activation) rounds to the neighbouring bf16 number on one
-    path: logits within 5e-3 (half the parity gate) and the same token wherever the gap is
+    """The two-kernel layer and the kernel chain agree.  The chain's attention runs on the
+    tensor cores with q and the probabilities P in bf16 (relative rounding 2^-9, as the prefill
+    attention's P), the one-row layer's attention in fp32; both take their fp32 sums in
+    different orders, so now and then a value stored in bf16 (the normed projection inputs, the
+    SwiGLU activation) also rounds to the neighbouring bf16 number on one path: logits within
+    8e-3 (each path stays within the 1e-2 oracle gate) and the same token wherever the gap is
     clear."""
     w, prompt, ref = setup
     b, lb = run_gpu(w, prompt, ref["fed"], flags=binding.QWEN3_FLAG_DECODE_CHAIN, dump=False)
     c, lc = run_gpu(w, prompt, ref["fed"], flags=0, dump=False)
     assert lc < lb  # two launches per layer on the default path, four on the chain
     for y, z in zip(b, c):
-        assert gc.rel_l2(z["logits"], y["logits"]) <= 5e-3
+        assert gc.rel_l2(z["logits"], y["logits"]) <= 8e-3
         top2 = np.sort(y["logits"])[-2:]
         if top2[1] - top2[0] > 1e-3:
             assert z["token"] == y["token"]
