@@ -133,19 +133,23 @@ def test_decode_attention_plan():
     assert plan(1024, 16, 8, 100, 128) == 1
 
 
-@pytest.mark.parametrize("positions,n_split", [([0, 64, 200], 0), ([63, 127, 129], 1), ([5, 250, 128], 7),
-                                               ([255, 1, 100], 64), ([4000, 1, 3000], 0), ([4095, 2047, 128], 0)])
-def test_decode_attention_op_vs_oracle(positions, n_split):
+@pytest.mark.parametrize("positions,n_split,Hq,Hkv", [
+    ([0, 64, 200], 0, 16, 8), ([63, 127, 129], 1, 16, 8), ([5, 250, 128], 7, 16, 8), ([255, 1, 100], 64, 16, 8),
+    ([4000, 1, 3000], 0, 16, 8), ([4095, 2047, 128], 0, 16, 8),
+    # one, four and eight query heads per KV head: heads in every column pair of the fragments
+    ([130, 7, 255], 3, 8, 8), ([130, 7, 255], 3, 16, 4), ([130, 7, 1000], 0, 16, 2), ([64, 0, 191], 5, 32, 4)])
+def test_decode_attention_op_vs_oracle(positions, n_split, Hq, Hkv):
     """qwen3_op_attn_decode against the oracle's per-head RMSNorm, rotate-half RoPE and causal
     GQA attention, over cached rows drawn at random and the new row at `positions`; n_split 0
     takes the decode step's plan (up to 4 ranges of whole 64-key chunks per pair at 256 keys,
-    more for the 4K contexts: ranges that end inside a chunk, empty ranges past the keys)."""
+    more for the 4K contexts: ranges that end inside a chunk, empty ranges past the keys).
+    Query heads per KV head 1, 2, 4 and 8 (the heads are the N side of the score MMA)."""
     import numpy as np
     from oracle import qwen3_oracle as oracle
 
     gc.ensure_library()
     max_ctx = 256 if max(positions) < 256 else 4096
-    B, Hq, Hkv, D, eps, theta = len(positions), 16, 8, 128, 1e-6, 1e6
+    B, D, eps, theta = len(positions), 128, 1e-6, 1e6
     n_slots = B + 1
     slots = [2, 0, 3][:B]
     g = torch.Generator(device="cpu").manual_seed(sum(positions) + n_split)
