@@ -41,7 +41,6 @@ constexpr int D = 128, BQ = 128, BK = 128, THREADS = 576;
 constexpr int TMA_WARP = 16, MMA_WARP = 17;  // warps 0-15 run the softmax
 constexpr int TILE_BYTES = 128 * D * 2;  // a [128][128] bf16 tile as two 64-column halves
 constexpr int HALF_BYTES = TILE_BYTES / 2;
-constexpr int SMEM_BYTES = TILE_BYTES * 5 + 6144 + 1024;  // Q0, Q1, K ring (2), V, barriers
 constexpr uint32_t TMEM_COLS = 512;  // S0: 0-127, S1: 128-255, O0: 256-383, O1: 384-511
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -139,6 +138,8 @@ struct Bars {
     float xsum[2][2][BQ];     // [head][column half][row]: partial row sums at the end
     int fail[2];              // [head]: a wait gave up (read by every warp of the head after a barrier)
 };
+// 1024 bytes of alignment slack, Q0, Q1, the K ring (2), V, the barriers
+constexpr int SMEM_BYTES = 1024 + TILE_BYTES * 5 + (int)sizeof(Bars);
 
 __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
