@@ -68,6 +68,8 @@ def parse_args():
                    help="run only the roofline kernel's timing of the workload (for ncu captures)")
     p.add_argument("--roofline-ctx", type=int, default=None,
                    help="context of the decode attention roofline launch (default: the workload's)")
+    p.add_argument("--roofline-kernel", default="auto", choices=["auto", "proj"],
+                   help="with --roofline-only: proj times the decode gate_up projection instead")
     return p.parse_args()
 
 
@@ -405,6 +407,38 @@ def measure_mlp_roofline(torch, binding, wl, peaks, peak_kind):
             "peak_source": _peak_source(peak_kind, "hbm_gbs")}
 
 
+def measure_proj_roofline(torch, binding, wl, peaks, peak_kind):
+    """Average duration of the decode gate_up projection (+ SwiGLU; 40% of a layer's weight
+    bytes) at the workload's batch, through qwen3_op_gemv (the tensor-core GEMV from 9 rows),
+    over launches cycling through 28 layers' weights (352 MB, larger than L2)."""
+    s = wl.shape
+    dev = torch.device("cuda")
+    M, C, I = wl.n_seqs, s.hidden, s.intermediate
+    g = torch.Generator(device="cpu").manual_seed(6)
+    layers = [(torch.randn(2 * I, C, generator=g) * 0.02).to(torch.bfloat16).to(dev) for _ in range(s.n_layers)]
+    x = torch.randn(M, C, generator=g).to(torch.bfloat16).to(dev)
+    out = torch.zeros(M, I, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    it = [0]
+
+    def launch():
+        w = layers[it[0] % len(layers)]
+        it[0] += 1
+        binding.qwen3_op_gemv(x.data_ptr(), M, C, w.data_ptr(), 2 * I, binding.QWEN3_EPI_SWIGLU, out.data_ptr(), stream)
+    for _ in range(len(layers)):
+        launch()
+    avg_s = _time_launches(torch, launch, 20 * len(layers))
+    algo_bytes = 2 * I * C * 2 + M * C * 2 + M * I * 2  # weights; x read, act written
+    achieved = algo_bytes / avg_s / 1e9
+    peak = float(peaks["hbm_gbs"])
+    kern = "k_gemv_mma (tensor cores)" if M > 8 else "k_gemv_bulk"
+    return {"kernel": f"{kern} (decode gate_up + SwiGLU, bf16 weights [{2 * I},{C}], {M} row(s))",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": TRAFFIC_BYTES.get(f"gemv_gate_up_{M}"),
+            "algorithmic_bytes_per_launch": algo_bytes, "avg_launch_us": round(avg_s * 1e6, 3),
+            "peak_source": _peak_source(peak_kind, "hbm_gbs")}
+
+
 def measure_attn_roofline(torch, binding, wl, peaks, peak_kind, ctx=None, reps=20):
     """Average duration of the decode attention kernel (QK-norm + RoPE + KV write + attention
     over keys 0..p), the kernel that streams the KV cache, as a decode step of the workload
@@ -703,12 +737,17 @@ def run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, w
                                  f"paged KV cache, {kv_block_tokens}-token blocks")
     else:
         roofline = roofline_for(torch, binding, wl, peaks, peak_kind)
+    # batched decode: the projections' share of the step, shown by its largest kernel
+    proj = (measure_proj_roofline(torch, binding, wl, peaks, peak_kind)
+            if wl.decode_steps and wl.n_seqs > 4 and not kv_block_tokens else None)
     torch.cuda.empty_cache()
     out.update({"value": units_all / (ms_max / 1e3), "unit": unit, "ms_per_step": ms_max / args.steps,
                 "units_per_step": units, "launches": launches, "clocks": clocks,
                 "e2e": {"value": round(e2e_units / (e2e_ms_max / 1e3), 2), "unit": unit,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "roofline": roofline})
+    if proj:
+        out["roofline_proj"] = proj
     step_s = ms_max / 1e3 / args.steps
     if wl.decode_steps:
         out["decode_step_hbm_frac"] = round(decode_step_bytes(wl) / (step_s / wl.decode_steps) / 1e9 /
@@ -885,7 +924,8 @@ def gpu_arm(args, wl):
     args.warmup = max(args.warmup, 3)  # at least three untimed steps
 
     if args.roofline_only:
-        r = roofline_for(torch, binding, wl, peaks, peak_kind, ctx=args.roofline_ctx)
+        r = (measure_proj_roofline(torch, binding, wl, peaks, peak_kind) if args.roofline_kernel == "proj" else
+             roofline_for(torch, binding, wl, peaks, peak_kind, ctx=args.roofline_ctx))
         if rank == 0:
             print(json.dumps({"roofline_only": True, "workload": wl.name, "roofline": r}), flush=True)
         return 0
