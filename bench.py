@@ -965,6 +965,8 @@ def gpu_arm(args, wl):
             "roofline": main["roofline"],
             "cpu_baseline": main["cpu_baseline"],
         }
+        if main.get("roofline_proj"):
+            line["roofline_proj"] = main["roofline_proj"]
         bd = {}
         for k in ("kv_fill", "decode_step_hbm_frac", "decode_step_bytes", "tflops", "tensor_frac"):
             if k in main:
