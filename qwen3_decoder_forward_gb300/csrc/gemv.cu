@@ -468,7 +468,7 @@ __device__ __forceinline__ void mma16816(float *c, const uint32_t *a, uint32_t b
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int EPI, int KS>
+template <int EPI, int KS, int MP>  // MP: batch rows padded to 16 or 32
 __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restrict__ X, int M, int K,
                                                              const bf16 *__restrict__ W, int N, void *out,
                                                              uint32_t *err) {
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restr
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
     uint8_t *ws = smem + 128;                      // [16][stride]
     uint8_t *xs = ws + MMA_ROWS * stride;          // [32][stride]
-    float *red = reinterpret_cast<float *>(xs + MMA_MPAD * stride);  // [warps][16][32]
+    float *red = reinterpret_cast<float *>(xs + MP * stride);  // [warps][16][MP]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = blockIdx.x * MMA_ROWS, ks = blockIdx.y, k0 = ks * Kc;
     uint64_t *xbar = bar + 1;
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restr
     }
     const long long lim = wait_limit(err);
     // rows of X beyond M are zero
-    for (int i = threadIdx.x; i < (MMA_MPAD - M) * (Kc / 8); i += MMA_WARPS * 32)
+    for (int i = threadIdx.x; i < (MP - M) * (Kc / 8); i += MMA_WARPS * 32)
         *reinterpret_cast<uint4 *>(xs + (M + i / (Kc / 8)) * stride + (i % (Kc / 8)) * 16) = make_uint4(0, 0, 0, 0);
     __syncthreads();
     pdl_wait();
@@ -510,16 +510,16 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restr
         mbar_wait_bounded(xbar, 0, nullptr);
         return;
     }
-    float acc[4][4];
+    float acc[MP / 8][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    for (int j = 0; j < MP / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
     const int kq = Kc / MMA_WARPS;  // this warp's quarter of the slice
     const uint32_t wsa = smem_addr(ws), xsa = smem_addr(xs);
     for (int kk = warp * kq; kk < (warp + 1) * kq; kk += 16) {
         uint32_t a[4];
         ldsm_x4(a, wsa + (lane & 15) * stride + (kk + (lane >> 4) * 8) * 2);
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {  // two ldmatrix.x4 cover the 32 padded batch rows
+        for (int nb = 0; nb < MP / 16; ++nb) {  // an ldmatrix.x4 per 16 padded batch rows
             uint32_t b[4];
             const int n = nb * 16 + (lane & 7) + ((lane >> 4) << 3);
             ldsm_x4(b, xsa + n * stride + (kk + ((lane >> 3) & 1) * 8) * 2);
@@ -530,20 +530,20 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restr
     // partial tiles of the 4 warps -> shared memory, then sum
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        float *rw = red + warp * MMA_ROWS * MMA_MPAD;
-        rw[g * MMA_MPAD + j * 8 + 2 * t] = acc[j][0];
-        rw[g * MMA_MPAD + j * 8 + 2 * t + 1] = acc[j][1];
-        rw[(g + 8) * MMA_MPAD + j * 8 + 2 * t] = acc[j][2];
-        rw[(g + 8) * MMA_MPAD + j * 8 + 2 * t + 1] = acc[j][3];
+    for (int j = 0; j < MP / 8; ++j) {
+        float *rw = red + warp * MMA_ROWS * MP;
+        rw[g * MP + j * 8 + 2 * t] = acc[j][0];
+        rw[g * MP + j * 8 + 2 * t + 1] = acc[j][1];
+        rw[(g + 8) * MP + j * 8 + 2 * t] = acc[j][2];
+        rw[(g + 8) * MP + j * 8 + 2 * t + 1] = acc[j][3];
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < MMA_ROWS * MMA_MPAD; i += MMA_WARPS * 32) {
-        const int r = i / MMA_MPAD, b = i % MMA_MPAD;  // r: weight row, b: batch row
+    for (int i = threadIdx.x; i < MMA_ROWS * MP; i += MMA_WARPS * 32) {
+        const int r = i / MP, b = i % MP;  // r: weight row, b: batch row
         if (b >= M) continue;
         float v = 0.0f;
 #pragma unroll
-        for (int w = 0; w < MMA_WARPS; ++w) v += red[w * MMA_ROWS * MMA_MPAD + i];
+        for (int w = 0; w < MMA_WARPS; ++w) v += red[w * MMA_ROWS * MP + i];
         const int n = row0 + r;
         if (EPI == EPI_F32) {
             ((float *)out)[(size_t)b * N + n] = v;
@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(MMA_WARPS * 32) k_gemv_mma(const bf16 *__restr
         } else if ((r & 1) == 0) {  // SwiGLU: rows (2j, 2j+1) = (gate_j, up_j)
             float up = 0.0f;
 #pragma unroll
-            for (int w = 0; w < MMA_WARPS; ++w) up += red[w * MMA_ROWS * MMA_MPAD + i + MMA_MPAD];
+            for (int w = 0; w < MMA_WARPS; ++w) up += red[w * MMA_ROWS * MP + i + MP];
             ((bf16 *)out)[(size_t)b * (N / 2) + (n >> 1)] = __float2bfloat16(silu(v) * up);
         }
     }
@@ -778,14 +778,21 @@ cudaError_t launch_lmhead_mma(const Launch &lc, const bf16 *X, int M, int C, con
 
 int lmhead_mma_parts(int num_sms) { return num_sms; }
 
+template <int EPI, int KS, int MP>
+cudaError_t run_mma_p(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N, void *out, uint32_t *err) {
+    const int Kc = K / KS;
+    const size_t smem = 128 + (size_t)(MMA_ROWS + MP) * (Kc * 2 + 16) + MMA_WARPS * MMA_ROWS * MP * 4;
+    cudaError_t e = cudaFuncSetAttribute(k_gemv_mma<EPI, KS, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch(lc, k_gemv_mma<EPI, KS, MP>, dim3(N / MMA_ROWS, KS), dim3(MMA_WARPS * 32), smem, X, M, K, W, N,
+                  out, err);
+}
+
+// up to 16 rows: half the shared memory (more CTAs an SM) and half the B fragments
 template <int EPI, int KS>
 cudaError_t run_mma(const Launch &lc, const bf16 *X, int M, int K, const bf16 *W, int N, void *out, uint32_t *err) {
-    const int Kc = K / KS;
-    const size_t smem = 128 + (size_t)(MMA_ROWS + MMA_MPAD) * (Kc * 2 + 16) + MMA_WARPS * MMA_ROWS * MMA_MPAD * 4;
-    cudaError_t e = cudaFuncSetAttribute(k_gemv_mma<EPI, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch(lc, k_gemv_mma<EPI, KS>, dim3(N / MMA_ROWS, KS), dim3(MMA_WARPS * 32), smem, X, M, K, W, N, out,
-                  err);
+    return M <= 16 ? run_mma_p<EPI, KS, 16>(lc, X, M, K, W, N, out, err)
+                   : run_mma_p<EPI, KS, 32>(lc, X, M, K, W, N, out, err);
 }
 
 bool gemv_mma_supported(int M, int K, int N) {

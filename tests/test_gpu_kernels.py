@@ -54,7 +54,7 @@ def test_prefill_gemm_vs_torch(M, K, N, epi):
     assert gc.rel_l2(out.cpu().numpy(), ref.cpu().numpy()) <= tol
 
 
-@pytest.mark.parametrize("M", [1, 3, 8, 17, 32])
+@pytest.mark.parametrize("M", [1, 3, 8, 12, 16, 17, 32])
 @pytest.mark.parametrize("K,N", [(1024, 4096), (2048, 1024), (3072, 1024), (1024, 6144)])
 @pytest.mark.parametrize("epi", EPIS)
 def test_decode_gemv_vs_torch(M, K, N, epi):
