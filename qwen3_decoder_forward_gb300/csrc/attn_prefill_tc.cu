@@ -17,8 +17,8 @@
 //   warps 0-7 / 8-15:  eight softmax warps per head -- warps w and w+4 of a head read the same
 //                      32 TMEM lanes (query rows) and split the 128 columns (keys) in halves:
 //                      each thread takes 64 scores of its row (tcgen05.ld), the two halves
-//                      exchange their row maxima through shared memory (one named barrier per
-//                      tile and head), apply the causal mask and the online softmax in fp32,
+//                      exchange their row maxima through shared memory (a named barrier per
+//                      tile and pair of warps), apply the causal mask and the online softmax in fp32,
 //                      write P (bf16) into tensor memory over the first 64 columns of S_h
 //                      (the P V MMA reads its A operand from there, not from shared memory)
 //                      and rescale their half of the row of the TMEM accumulator O_h when the
@@ -136,7 +136,7 @@ struct Bars {
     uint32_t tmem;
     float xmax[2][2][2][BQ];  // [tile parity][head][column half][row]: partial row maxima
     float xsum[2][2][BQ];     // [head][column half][row]: partial row sums at the end
-    int fail[2];              // [head]: a wait gave up (read by every warp of the head after a barrier)
+    int xfail[2][2][2][4];    // [tile parity][head][column half][row quarter]: this warp's wait gave up
 };
 // 1024 bytes of alignment slack, Q0, Q1, the K ring (2), V, the barriers
 constexpr int SMEM_BYTES = 1024 + TILE_BYTES * 5 + (int)sizeof(Bars);
@@ -181,7 +181,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
             mbar_init(&bars->s_full[hh], 1);
             mbar_init(&bars->p_full[hh], 8 * 32);
             mbar_init(&bars->o_full[hh], 1);
-            bars->fail[hh] = 0;
         }
     }
     if (warp == MMA_WARP) {
@@ -276,18 +275,21 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
         const int kend = off + len;   // keys at or beyond kend do not exist yet
         const uint32_t lane_base = (uint32_t)((wl & 3) * 32) << 16;
         const uint32_t t_s = tmem + hh * 128 + ch * 64 + lane_base, t_o = tmem + 256 + hh * 128 + ch * 64 + lane_base;
-        auto head_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + hh), "r"(8 * 32) : "memory"); };
+        // the two warps that share these query rows meet at their own named barrier
+        auto head_sync = [&]() { asm volatile("bar.sync %0, %1;" ::"r"(1 + hh * 4 + (wl & 3)), "r"(2 * 32) : "memory"); };
         float m_run = -INFINITY, l_run = 0.0f;
+        bool gave_up = false;  // warp-uniform
         // P (bf16, two keys per column) overwrites the first 64 columns of S_hh: keys
         // ch*64 + c*32 .. +31 of this row go to columns ch*32 + c*16 .. +15 of its lane.  Both
-        // halves of the row hold their scores in registers past the head's barrier, so no
+        // halves of the row hold their scores in registers past the pair's barrier, so no
         // score is overwritten before it is read.
         const uint32_t t_p = tmem + hh * 128 + ch * 32 + lane_base;
         for (int j = 0; j < n_tiles; ++j) {
-            // A wait that gives up is reported through fail[hh] and acted on after the head's
-            // barrier, so that all eight warps leave the loop at the same barrier.
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars->s_full[hh], j & 1, err)) && lane == 0)
-                bars->fail[hh] = 1;
+            // A wait that gives up is posted with the row maxima and acted on after the pair's
+            // barrier: both warps of the pair see both flags of this tile and leave the loop
+            // together.  The flags alternate with the tile parity, so a partner cannot post the
+            // next tile's flag before this warp has read this one.
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars->s_full[hh], j & 1, err))) gave_up = true;
             fence_after();
             const int k0 = j * BK + ch * 64;  // first key of this thread's half
             // Only tiles reaching above the CTA's first query mask: every key of an earlier
@@ -316,9 +318,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
             const float mh = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
                                    fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
             bars->xmax[j & 1][hh][ch][r] = mh;
+            if (lane == 0) bars->xfail[j & 1][hh][ch][wl & 3] = gave_up;
             head_sync();
             const float mx = fmaxf(mh, bars->xmax[j & 1][hh][ch ^ 1][r]);
-            if (*reinterpret_cast<volatile int *>(&bars->fail[hh])) {
+            if (gave_up || bars->xfail[j & 1][hh][ch ^ 1][wl & 3]) {
                 ok = false;
                 break;
             }
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
             bool o_ok = true;
             if (j > 0 && !__all_sync(0xffffffffu, mbar_wait_bounded(&bars->o_full[hh], (j - 1) & 1, err))) {
                 o_ok = false;
-                if (lane == 0) bars->fail[hh] = 1;  // the loop ends at the next barrier
+                gave_up = true;  // the loop ends at the next barrier
             }
             if (o_ok && j > 0 && __any_sync(0xffffffffu, corr != 1.0f)) {  // rescale this half-row of O_h
 #pragma unroll 1
@@ -385,6 +388,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_attn_prefill_tc(
             fence_before();
             arrive(&bars->p_full[hh]);
         }
+        if (gave_up) ok = false;
         // the two halves' row sums; the output row is then written in two halves
         bars->xsum[hh][ch][r] = l_run;
         head_sync();
