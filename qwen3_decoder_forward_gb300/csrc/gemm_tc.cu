@@ -8,8 +8,12 @@
 //                        4-stage shared-memory ring, completion counted on mbarriers;
 //   warp 1, one thread : MMA issuer -- tcgen05.mma (M=128, N=256, K=16) per stage, the stage
 //                        released back to the producer by tcgen05.commit;
-//   warps 0-3          : epilogue -- tcgen05.ld of TMEM lanes 32w..32w+31 (one output row per
-//                        thread), then the fp32 / residual-add / SwiGLU store.
+//   warps 2-9          : epilogue -- tcgen05.ld of TMEM lanes 32(w%4)..+31 (one output row per
+//                        thread), then the fp32 / residual-add / SwiGLU / QKV store.  The
+//                        residual add moves h through shared memory by TMA: 32 rows x 32
+//                        columns of fp32 per warp in, the sums out, so that the rows (4 KB
+//                        apart) travel as tiles rather than one 16-byte piece of 32 rows per
+//                        instruction.
 // Rows of A beyond M are zero-filled by TMA and dropped on store (ragged token counts).
 // Every mbarrier wait is bounded: on timeout the CTA flags ERR_TIMEOUT, drains, frees its
 // tensor memory and returns.
@@ -29,6 +33,13 @@ constexpr int TC_A_BYTES = TC_BM * TC_BK * 2;                  // 16 KB
 constexpr int TC_B_BYTES = TC_BN * TC_BK * 2;                  // 32 KB
 constexpr int TC_STAGE_BYTES = TC_A_BYTES + TC_B_BYTES;        // 48 KB
 constexpr int TC_SMEM = TC_STAGES * TC_STAGE_BYTES + 256 + 1024;  // ring + barriers + alignment
+// The residual-add epilogue's tiles of h: one per epilogue warp, 32 rows x 32 fp32 columns
+// (128-byte rows, 128-byte swizzle), 1024-aligned after the barriers.
+constexpr int TC_H_BOX = 32;
+constexpr int TC_H_BYTES = TC_H_BOX * TC_H_BOX * 4;  // 4 KB
+constexpr int TC_H_OFF = TC_STAGES * TC_STAGE_BYTES + 1024;
+constexpr int TC_SMEM_RESID = TC_H_OFF + 8 * TC_H_BYTES + 1024;
+static_assert(TC_SMEM_RESID <= 227 * 1024, "residual epilogue tiles exceed shared memory");
 
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with the 128-byte
 // swizzle: rows of 128 bytes (64 elements), 8-row groups 1024 bytes apart.
@@ -54,6 +65,19 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y)
         : "memory");
 }
+
+// Shared -> global tile store through the tensor map (rows past the tensor's end are not written).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_addr(src)), "r"(x), "r"(y)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The stores issued by this thread have read their shared memory.
+__device__ __forceinline__ void tma_store_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// The stores issued by this thread are complete.
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -121,33 +145,6 @@ __device__ __forceinline__ float row_scale(const EpiArgs &ea, int row) {
     return rsqrtf(s / (float)ea.norm_c + ea.eps);
 }
 
-// Residual add of 32 columns that also writes bf16(h * gamma) of the new values (the operand
-// of the next projection, before its row scale) and adds their squares to *ss.
-__device__ __forceinline__ void store_resid_norm(const uint32_t *v, int row, int col, int N, const EpiArgs &ea,
-                                                 float *ss) {
-    float4 *dst = reinterpret_cast<float4 *>((float *)ea.out + (size_t)row * N + col);
-    const float4 *g4 = reinterpret_cast<const float4 *>(ea.gamma_out + col);
-    uint32_t o[16];
-    float s = *ss;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        float4 r = dst[j];
-        r.x += __uint_as_float(v[4 * j]);
-        r.y += __uint_as_float(v[4 * j + 1]);
-        r.z += __uint_as_float(v[4 * j + 2]);
-        r.w += __uint_as_float(v[4 * j + 3]);
-        dst[j] = r;
-        s += r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w;
-        const float4 g = g4[j];
-        o[2 * j] = pack_bf16x2(r.x * g.x, r.y * g.y);
-        o[2 * j + 1] = pack_bf16x2(r.z * g.z, r.w * g.w);
-    }
-    *ss = s;
-    uint4 *xd = reinterpret_cast<uint4 *>(ea.xn_out + (size_t)row * N + col);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) xd[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-}
-
 // SwiGLU of row-scaled gate/up pairs: silu(rs * g) * (rs * u), bf16.
 __device__ __forceinline__ void store_swiglu_scaled(const uint32_t *v, float rs, int row, int col, int N, void *out) {
     uint32_t o[8];
@@ -169,17 +166,6 @@ __device__ __forceinline__ void store_chunk(int EPI_, const uint32_t *v, int row
         for (int j = 0; j < 8; ++j)
             dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
                                  __uint_as_float(v[4 * j + 3]));
-    } else if (EPI_ == EPI_RESID_ADD) {
-        float4 *dst = reinterpret_cast<float4 *>((float *)out + (size_t)row * N + col);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float4 r = dst[j];
-            r.x += __uint_as_float(v[4 * j]);
-            r.y += __uint_as_float(v[4 * j + 1]);
-            r.z += __uint_as_float(v[4 * j + 2]);
-            r.w += __uint_as_float(v[4 * j + 3]);
-            dst[j] = r;
-        }
     } else {  // SwiGLU: columns (2j, 2j+1) are (gate_j, up_j)
         uint32_t o[8];
 #pragma unroll
@@ -204,9 +190,11 @@ __device__ __forceinline__ void store_bf16x32(bf16 *dst, const float *x) {
     for (int j = 0; j < 4; ++j) d[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
 }
 
+// tmH: for the residual add, the fp32 [M, N] residual as 32 x 32 boxes (unused otherwise).
 template <int EPI>
 __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_constant__ CUtensorMap tmA,
-                                                             const __grid_constant__ CUtensorMap tmB, int M, int N,
+                                                             const __grid_constant__ CUtensorMap tmB,
+                                                             const __grid_constant__ CUtensorMap tmH, int M, int N,
                                                              int K, EpiArgs ea, uint32_t *err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -214,7 +202,8 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
     uint64_t *empty = full + TC_STAGES;
     uint64_t *tm_full = empty + TC_STAGES;  // [2]
     uint64_t *tm_empty = tm_full + 2;       // [2]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tm_empty + 2);
+    uint64_t *hbar = tm_empty + 2;          // [8] residual tiles of the epilogue warps
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(hbar + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = K / TC_BK;
@@ -229,6 +218,7 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
             mbar_init(&tm_full[a], 1);
             mbar_init(&tm_empty[a], TCP_EPI_WARPS);  // one arrival per epilogue warp
         }
+        for (int w = 0; w < TCP_EPI_WARPS; ++w) mbar_init(&hbar[w], 1);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -293,24 +283,86 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
         // epilogue warps 2..9
         const int q = warp & 3;         // TMEM lane quarter this warp may access
         const int half = (warp - 2) >> 2;  // 128-column half of the tile
+        const int ew = warp - 2;
+        uint8_t *hbuf = smem + TC_H_OFF + ew * TC_H_BYTES;  // this warp's residual tile
+        uint32_t hph = 0;                                   // phase of hbar[ew]
+        bool failed = false;
         int local = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++local) {
+        for (int t = blockIdx.x; t < tiles && !failed; t += gridDim.x, ++local) {
             const int a = local & 1;
-            const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&tm_full[a], (local >> 1) & 1, err));
-            if (!ready) break;
-            tc_fence_after();
             const int m0 = (t / tiles_n) * TC_BM, n0 = (t % tiles_n) * TC_BN;
             const int row = m0 + q * 32 + lane;
+            // residual add: the warp's 32 rows (none of them past M for `live`), 32 columns at a
+            // time; the first tile of h is requested before the accumulator is ready
+            const bool live = EPI == EPI_RESID_ADD && m0 + q * 32 < M;
+            const int hy = m0 + q * 32;
+            if (live && lane == 0) {
+                mbar_expect_tx(&hbar[ew], TC_H_BYTES);
+                tma_load_2d(hbuf, &tmH, n0 + half * 128, hy, &hbar[ew]);
+            }
+            const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&tm_full[a], (local >> 1) & 1, err));
+            if (!ready) {
+                if (live) mbar_wait_bounded(&hbar[ew], hph, nullptr);  // let the copy land
+                break;
+            }
+            tc_fence_after();
             const uint32_t t_row = tmem + a * TC_BN + ((uint32_t)(q * 32) << 16);
-            if (EPI == EPI_RESID_ADD && ea.xn_out) {
+            if (EPI == EPI_RESID_ADD) {
+                // The thread's row sits at hbuf + 128 lane, its 16-byte piece j at piece
+                // j ^ (lane % 8) of the row (the 128-byte swizzle): 8 lanes reading piece j of
+                // 8 rows touch 8 different bank groups.
+                float4 *hr = reinterpret_cast<float4 *>(hbuf + lane * 128);
                 float ss = 0.0f;
 #pragma unroll 1
                 for (int c = half * 4; c < half * 4 + 4; ++c) {
                     uint32_t v[32];
                     tmem_ld32(t_row + c * 32, v);
-                    if (row < M) store_resid_norm(v, row, n0 + c * 32, N, ea, &ss);
+                    if (!live) continue;
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&hbar[ew], hph, err))) {
+                        mbar_wait_bounded(&hbar[ew], hph, nullptr);  // let the copy land
+                        failed = true;
+                        break;
+                    }
+                    hph ^= 1;
+                    const int col = n0 + c * 32;
+                    const float4 *g4 = reinterpret_cast<const float4 *>(ea.gamma_out + col);
+                    uint32_t o[16];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int u = j ^ (lane & 7);
+                        float4 r = hr[u];
+                        r.x += __uint_as_float(v[4 * j]);
+                        r.y += __uint_as_float(v[4 * j + 1]);
+                        r.z += __uint_as_float(v[4 * j + 2]);
+                        r.w += __uint_as_float(v[4 * j + 3]);
+                        hr[u] = r;
+                        if (ea.xn_out) {
+                            ss += r.x * r.x + r.y * r.y + r.z * r.z + r.w * r.w;
+                            const float4 g = g4[j];
+                            o[2 * j] = pack_bf16x2(r.x * g.x, r.y * g.y);
+                            o[2 * j + 1] = pack_bf16x2(r.z * g.z, r.w * g.w);
+                        }
+                    }
+                    if (ea.xn_out && row < M) {
+                        uint4 *xd = reinterpret_cast<uint4 *>(ea.xn_out + (size_t)row * N + col);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) xd[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                    }
+                    // the sums go out as a tile; the buffer then takes the next 32 columns
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmH, hbuf, col, hy);
+                        tma_store_wait_read();
+                        if (c + 1 < half * 4 + 4) {
+                            mbar_expect_tx(&hbar[ew], TC_H_BYTES);
+                            tma_load_2d(hbuf, &tmH, col + 32, hy, &hbar[ew]);
+                        }
+                    }
+                    __syncwarp();
                 }
-                if (row < M) ea.ss_out[(size_t)row * (N / 128) + n0 / 128 + half] = ss;
+                if (failed) break;
+                if (ea.xn_out && live && row < M) ea.ss_out[(size_t)row * (N / 128) + n0 / 128 + half] = ss;
             } else if (EPI == EPI_SWIGLU && ea.ss_in) {
                 const float rs = row < M ? row_scale(ea, row) : 0.0f;
 #pragma unroll 1
@@ -397,6 +449,7 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&tm_empty[a])) : "memory");
         }
+        if (EPI == EPI_RESID_ADD && lane == 0) tma_store_wait_all();  // the sums are in global memory
     }
     pdl_trigger();
     tc_fence_before();
@@ -435,14 +488,30 @@ bool make_map(CUtensorMap *map, const bf16 *base, int rows, int cols, int box_ro
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map of the fp32 residual [rows, cols] as boxes of 32 x 32 (128-byte rows, 128-byte swizzle).
+bool make_map_h(CUtensorMap *map, const float *base, int rows, int cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)TC_H_BOX, (cuuint32_t)TC_H_BOX};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI>
 cudaError_t run_tcp(const Launch &lc, const CUtensorMap &ma, const CUtensorMap &mb, int M, int N, int K,
                     const EpiArgs &ea, uint32_t *err) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tcp<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    CUtensorMap mh = {};
+    if (EPI == EPI_RESID_ADD && !make_map_h(&mh, static_cast<const float *>(ea.out), M, N)) return cudaErrorInvalidValue;
+    const int smem = EPI == EPI_RESID_ADD ? TC_SMEM_RESID : TC_SMEM;
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tcp<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int tiles = ((M + TC_BM - 1) / TC_BM) * (N / TC_BN);
     const int grid = tiles < lc.num_sms ? tiles : lc.num_sms;
-    return launch(lc, k_gemm_tcp<EPI>, dim3(grid), dim3(TCP_THREADS), TC_SMEM, ma, mb, M, N, K, ea, err);
+    return launch(lc, k_gemm_tcp<EPI>, dim3(grid), dim3(TCP_THREADS), smem, ma, mb, mh, M, N, K, ea, err);
 }
 
 }  // namespace
@@ -455,6 +524,8 @@ cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const 
                            void *out, uint32_t *err, const RowNorm &rn) {
     if (!gemm_tc_supported(M, K, N) || epi == EPI_QKV) return cudaErrorInvalidValue;
     if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(W)) & 15) return cudaErrorInvalidValue;
+    // the residual travels by TMA: 16-byte aligned base (N % 256 == 0 gives the row pitch)
+    if (epi == EPI_RESID_ADD && (reinterpret_cast<uintptr_t>(out) & 15)) return cudaErrorInvalidValue;
     if (rn.xn_out && (epi != EPI_RESID_ADD || !rn.ss_out || !rn.gamma_out || N % 128)) return cudaErrorInvalidValue;
     if (rn.ss_in && (epi != EPI_SWIGLU || rn.norm_c != K || K % 128)) return cudaErrorInvalidValue;
     CUtensorMap ma, mb;
