@@ -300,6 +300,15 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                 mbar_expect_tx(&hbar[ew], TC_H_BYTES);
                 tma_load_2d(hbuf, &tmH, n0 + half * 128, hy, &hbar[ew]);
             }
+            // what a row's epilogue needs besides the accumulator, read while the MMAs run: the
+            // folded input norm's row scale, and for QKV the row's cache slot and position
+            float rs = 1.0f;
+            int slot = 0, pos = 0;
+            if ((EPI == EPI_SWIGLU || EPI == EPI_QKV) && ea.ss_in && row < M) rs = row_scale(ea, row);
+            if (EPI == EPI_QKV && row < M) {
+                slot = ea.row_slot[row];
+                pos = ea.row_pos[row];
+            }
             const bool ready = __all_sync(0xffffffffu, mbar_wait_bounded(&tm_full[a], (local >> 1) & 1, err));
             if (!ready) {
                 if (live) mbar_wait_bounded(&hbar[ew], hph, nullptr);  // let the copy land
@@ -364,7 +373,6 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                 if (failed) break;
                 if (ea.xn_out && live && row < M) ea.ss_out[(size_t)row * (N / 128) + n0 / 128 + half] = ss;
             } else if (EPI == EPI_SWIGLU && ea.ss_in) {
-                const float rs = row < M ? row_scale(ea, row) : 0.0f;
 #pragma unroll 1
                 for (int c = half * 4; c < half * 4 + 4; ++c) {
                     uint32_t v[32];
@@ -380,10 +388,7 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                 }
             } else {
                 // two heads of 128 columns per tile: head index within [q | k | v]
-                const int slot = row < M ? ea.row_slot[row] : 0;
-                const int pos = row < M ? ea.row_pos[row] : 0;
-                // the input RMSNorm's row scale (1 when the operand came normalised)
-                const float rs = ea.ss_in && row < M ? row_scale(ea, row) : 1.0f;
+                // rs: the input RMSNorm's row scale (1 when the operand came normalised)
                 {
                     const int hh = half;
                     const int head = n0 / 128 + hh;
