@@ -45,8 +45,11 @@ L2_BYTES = 129 * 2 ** 20
 # weights; the prefill gate_up GEMM at 23,460 rows reads A (48 MB) and W (12.6 MB) once and
 # writes 86 MB of its 144 MB output before it ends (the rest leaves L2 later).  The decode
 # attention entries are DRAM bytes per (sequence, position) row of one layer's K and V, scaled
-# by the rows a launch reads (the traffic grows in proportion with the rows).
-TRAFFIC_BYTES = {"gemm_gate_up": 147362304, "mlp_fused": 18910976, "attn_decode_per_key_row": 4110.9}
+# by the rows a launch reads (the traffic grows in proportion with the rows).  The decode gate_up
+# projections at 16 and 32 rows read their 12.6 MB of weights once and write nothing to DRAM
+# before they end.
+TRAFFIC_BYTES = {"gemm_gate_up": 146836992, "mlp_fused": 18910976, "attn_decode_per_key_row": 4110.9,
+                 "gemv_gate_up_16": 12630912, "gemv_gate_up_32": 12664704}
 
 
 def parse_args():
