@@ -121,7 +121,8 @@ struct EpiArgs {
     // [rows, Hq, 128], k and v into the layer's cache at (row_slot, row_pos).
     const int32_t *row_slot, *row_pos;
     const float *q_gain, *k_gain;
-    const float2 *rope_t;  // (cos, sin) by frequency: rope_t[i * max_ctx + pos], i < 64
+    // (cos, sin) of frequencies 2k and 2k+1 at position pos: rope_t[k * max_ctx + pos], k < 32
+    const float4 *rope_t;
     bf16 *q_out, *k_layer, *v_layer;
     int Hq, Hkv, max_ctx;
     KvMap kv;  // where the cache row of (slot, head, pos) lives
@@ -432,16 +433,27 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                                     xh[j] = __uint_as_float(hi[j]) * inv;
                                 }
                             } else {
-                                // frequency-major table: the 32 lanes (rows at mostly
-                                // consecutive positions) read neighbouring entries
-                                const float2 *cs = ea.rope_t + (size_t)(c * 32) * ea.max_ctx + pos;
+                                // frequency-pair-major table: the 32 lanes (rows at mostly
+                                // consecutive positions) read neighbouring 16-byte entries;
+                                // gains and table in 16-byte loads (four columns per step)
+                                const float4 *cs = ea.rope_t + (size_t)(c * 16) * ea.max_ctx + pos;
+                                const float4 *gl4 = reinterpret_cast<const float4 *>(gain + c * 32);
+                                const float4 *gh4 = reinterpret_cast<const float4 *>(gain + 64 + c * 32);
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) {
-                                    const float a0 = __uint_as_float(lo[j]) * inv * gain[c * 32 + j];
-                                    const float b0 = __uint_as_float(hi[j]) * inv * gain[64 + c * 32 + j];
-                                    const float2 r = cs[(size_t)j * ea.max_ctx];
-                                    xl[j] = a0 * r.x - b0 * r.y;  // x_i cos - x_{i+64} sin
-                                    xh[j] = b0 * r.x + a0 * r.y;  // x_{i+64} cos + x_i sin
+                                for (int qd = 0; qd < 8; ++qd) {
+                                    const float4 ga = gl4[qd], gb = gh4[qd];
+                                    const float4 r0 = cs[(size_t)(2 * qd) * ea.max_ctx];      // i = 4 qd, 4 qd + 1
+                                    const float4 r1 = cs[(size_t)(2 * qd + 1) * ea.max_ctx];  // i = 4 qd + 2, 4 qd + 3
+                                    const float gav[4] = {ga.x, ga.y, ga.z, ga.w}, gbv[4] = {gb.x, gb.y, gb.z, gb.w};
+                                    const float cv[4] = {r0.x, r0.z, r1.x, r1.z}, sv[4] = {r0.y, r0.w, r1.y, r1.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const int j = 4 * qd + e;
+                                        const float a0 = __uint_as_float(lo[j]) * inv * gav[e];
+                                        const float b0 = __uint_as_float(hi[j]) * inv * gbv[e];
+                                        xl[j] = a0 * cv[e] - b0 * sv[e];  // x_i cos - x_{i+64} sin
+                                        xh[j] = b0 * cv[e] + a0 * sv[e];  // x_{i+64} cos + x_i sin
+                                    }
                                 }
                             }
                             store_bf16x32(dst + c * 32, xl);
@@ -552,7 +564,7 @@ cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const 
 }
 
 cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, const Rows &r,
-                               const float *q_gain, const float *k_gain, const float2 *rope_t, bf16 *q_out,
+                               const float *q_gain, const float *k_gain, const float4 *rope_t, bf16 *q_out,
                                bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv, int max_ctx, float eps,
                                uint32_t *err, const float *ss_in) {
     if (!gemm_tc_supported(M, K, N) || N != (Hq + 2 * Hkv) * 128 || (ss_in && K % 128)) return cudaErrorInvalidValue;

@@ -150,10 +150,10 @@ struct RowNorm {
 cudaError_t launch_gemm_tc(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, int epi,
                            void *out, uint32_t *err, const RowNorm &rn = RowNorm());
 // QKV projection with the epilogue of launch_qknorm_rope_kv fused in (no fp32 qkv buffer).
-// rope_t is the RoPE table by frequency: (cos, sin) of frequency i at position p at
-// rope_t[i * max_ctx + p].
+// rope_t is the RoPE table by pairs of frequencies: (cos, sin) of frequencies 2k and 2k+1 at
+// position p at rope_t[k * max_ctx + p], k < 64 / 2.
 cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, const bf16 *W, int N, const Rows &r,
-                               const float *q_gain, const float *k_gain, const float2 *rope_t, bf16 *q_out,
+                               const float *q_gain, const float *k_gain, const float4 *rope_t, bf16 *q_out,
                                bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv, int max_ctx, float eps,
                                uint32_t *err, const float *ss_in = nullptr);
 

@@ -98,7 +98,7 @@ Layout make_layout(const qwen3_config &c) {
     L.o_embed = take((size_t)c.vocab * C * 2);
     L.o_gfinal = take(C * 4);
     L.o_rope = take((size_t)c.max_ctx * (D / 2) * 8);
-    L.o_rope_t = take((size_t)c.max_ctx * (D / 2) * 8);  // the same table, frequency-major
+    L.o_rope_t = take((size_t)c.max_ctx * (D / 2) * 8);  // the same table, by pairs of frequencies
     if (c.kv_block_tokens > 0) {  // paged: a pool of blocks [block][Hkv][bs][D] and a block table
         L.kv_layer_bytes = (size_t)c.kv_pool_blocks * Hkv * c.kv_block_tokens * D * 2;
         L.kv_max_blocks = (c.max_ctx + c.kv_block_tokens - 1) / c.kv_block_tokens;
@@ -242,7 +242,7 @@ cudaError_t run_forward(qwen3_ctx *c, const Launch &lc, const int32_t *tokens, c
     uint32_t *err = c->at<uint32_t>(L.o_err);
     const bf16 *embed = c->at<bf16>(L.o_embed);
     const float2 *rope = c->at<float2>(L.o_rope);
-    const float2 *rope_t = c->at<float2>(L.o_rope_t);
+    const float4 *rope_t = c->at<float4>(L.o_rope_t);
     auto dump = [&](int l, const float *src) -> cudaError_t {
         if (!c->dump) return cudaSuccess;
         return cudaMemcpyAsync(c->dump + (size_t)l * R * C, src, (size_t)R * C * 4,
@@ -632,10 +632,15 @@ int qwen3_create(const qwen3_config *cfg, const qwen3_weights *w, void *arena_de
             }
         Q3_TRY(cudaMemcpyAsync(c->arena + lay.o_rope, tab.data(), tab.size() * sizeof(float2),
                                cudaMemcpyHostToDevice, st));
-        std::vector<float2> tab_t(tab.size());  // [D/2][max_ctx]: rows at consecutive positions
-        for (int p = 0; p < cfg->max_ctx; ++p)  // read neighbouring entries
-            for (size_t i = 0; i < D / 2; ++i) tab_t[i * cfg->max_ctx + p] = tab[(size_t)p * (D / 2) + i];
-        Q3_TRY(cudaMemcpyAsync(c->arena + lay.o_rope_t, tab_t.data(), tab_t.size() * sizeof(float2),
+        // [D/4][max_ctx] of (cos, sin) of frequencies 2k, 2k+1: rows at consecutive positions read
+        // neighbouring 16-byte entries
+        std::vector<float4> tab_t(tab.size() / 2);
+        for (int p = 0; p < cfg->max_ctx; ++p)
+            for (size_t k = 0; k < D / 4; ++k) {
+                const float2 a = tab[(size_t)p * (D / 2) + 2 * k], b = tab[(size_t)p * (D / 2) + 2 * k + 1];
+                tab_t[k * cfg->max_ctx + p] = make_float4(a.x, a.y, b.x, b.y);
+            }
+        Q3_TRY(cudaMemcpyAsync(c->arena + lay.o_rope_t, tab_t.data(), tab_t.size() * sizeof(float4),
                                cudaMemcpyHostToDevice, st));
         // The KV cache starts at zero: the tensor-core prefill attention multiplies whole
         // 128-key tiles, so rows past a sequence's end (weight 0) must hold finite values --
