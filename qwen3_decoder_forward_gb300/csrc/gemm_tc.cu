@@ -181,17 +181,6 @@ __device__ __forceinline__ void store_chunk(int EPI_, const uint32_t *v, int row
     }
 }
 
-// Stores 32 bf16 values (already in fp32 registers) at dst.
-__device__ __forceinline__ void store_bf16x32(bf16 *dst, const float *x) {
-    uint32_t o[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) o[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) d[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-}
-
-// tmH: for the residual add, the fp32 [M, N] residual as 32 x 32 boxes (unused otherwise).
 template <int EPI>
 __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB,
@@ -295,7 +284,8 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
             const int row = m0 + q * 32 + lane;
             // residual add: the warp's 32 rows (none of them past M for `live`), 32 columns at a
             // time; the first tile of h is requested before the accumulator is ready
-            const bool live = EPI == EPI_RESID_ADD && m0 + q * 32 < M;
+            const bool rows_live = m0 + q * 32 < M;
+            const bool live = EPI == EPI_RESID_ADD && rows_live;
             const int hy = m0 + q * 32;
             if (live && lane == 0) {
                 mbar_expect_tx(&hbar[ew], TC_H_BYTES);
@@ -418,19 +408,24 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                         dst = (is_v ? ea.v_layer : ea.k_layer) +
                               kv_row(ea.kv, slot, ea.Hkv, g, ea.max_ctx, pos < ea.max_ctx ? pos : 0) * 128;
                     }
+                    // q leaves as TMA tiles of 32 rows x 32 columns (two a pass); k and v go
+                    // to their cache rows, which need not be contiguous across the warp's rows
+                    const bool q_tma = head < ea.Hq && rows_live;
                     // pass 2: elements i (chunk c) and i+64 (chunk c+2) rotate together
 #pragma unroll 1
                     for (int c = 0; c < 2; ++c) {
                         uint32_t lo[32], hi[32];
                         tmem_ld32(th + c * 32, lo);
                         tmem_ld32(th + (c + 2) * 32, hi);
-                        if (row < M && pos < ea.max_ctx) {
-                            float xl[32], xh[32];
+                        const bool valid = row < M && pos < ea.max_ctx;
+                        // the results as bf16 pairs, packed as soon as they are computed
+                        uint32_t pl[16], ph[16];
+                        if (valid) {
                             if (is_v) {
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) {
-                                    xl[j] = __uint_as_float(lo[j]) * inv;
-                                    xh[j] = __uint_as_float(hi[j]) * inv;
+                                for (int j = 0; j < 16; ++j) {
+                                    pl[j] = pack_bf16x2(__uint_as_float(lo[2 * j]) * inv, __uint_as_float(lo[2 * j + 1]) * inv);
+                                    ph[j] = pack_bf16x2(__uint_as_float(hi[2 * j]) * inv, __uint_as_float(hi[2 * j + 1]) * inv);
                                 }
                             } else {
                                 // frequency-pair-major table: the 32 lanes (rows at mostly
@@ -446,18 +441,53 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
                                     const float4 r1 = cs[(size_t)(2 * qd + 1) * ea.max_ctx];  // i = 4 qd + 2, 4 qd + 3
                                     const float gav[4] = {ga.x, ga.y, ga.z, ga.w}, gbv[4] = {gb.x, gb.y, gb.z, gb.w};
                                     const float cv[4] = {r0.x, r0.z, r1.x, r1.z}, sv[4] = {r0.y, r0.w, r1.y, r1.w};
+                                    float xl[4], xh[4];
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) {
                                         const int j = 4 * qd + e;
                                         const float a0 = __uint_as_float(lo[j]) * inv * gav[e];
                                         const float b0 = __uint_as_float(hi[j]) * inv * gbv[e];
-                                        xl[j] = a0 * cv[e] - b0 * sv[e];  // x_i cos - x_{i+64} sin
-                                        xh[j] = b0 * cv[e] + a0 * sv[e];  // x_{i+64} cos + x_i sin
+                                        xl[e] = a0 * cv[e] - b0 * sv[e];  // x_i cos - x_{i+64} sin
+                                        xh[e] = b0 * cv[e] + a0 * sv[e];  // x_{i+64} cos + x_i sin
                                     }
+                                    pl[2 * qd] = pack_bf16x2(xl[0], xl[1]);
+                                    pl[2 * qd + 1] = pack_bf16x2(xl[2], xl[3]);
+                                    ph[2 * qd] = pack_bf16x2(xh[0], xh[1]);
+                                    ph[2 * qd + 1] = pack_bf16x2(xh[2], xh[3]);
                                 }
                             }
-                            store_bf16x32(dst + c * 32, xl);
-                            store_bf16x32(dst + 64 + c * 32, xh);
+                        }
+                        if (q_tma) {
+                            // the two boxes of this pass, 64-byte rows with the 64-byte swizzle:
+                            // 16-byte piece u of row r sits at piece u ^ ((r / 2) % 4), so 8
+                            // lanes storing piece u of 8 rows touch 8 different bank groups
+                            uint8_t *bl = hbuf, *bh = hbuf + TC_H_BYTES / 2;
+                            const int sw = (lane >> 1) & 3;
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                uint4 va = make_uint4(0, 0, 0, 0), vb = va;  // rows past M or max_ctx: zeros
+                                if (valid) {
+                                    va = make_uint4(pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+                                    vb = make_uint4(ph[4 * u], ph[4 * u + 1], ph[4 * u + 2], ph[4 * u + 3]);
+                                }
+                                *reinterpret_cast<uint4 *>(bl + lane * 64 + ((u ^ sw) << 4)) = va;
+                                *reinterpret_cast<uint4 *>(bh + lane * 64 + ((u ^ sw) << 4)) = vb;
+                            }
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tmH, bl, head * 128 + c * 32, hy);
+                                tma_store_2d(&tmH, bh, head * 128 + 64 + c * 32, hy);
+                                tma_store_wait_read();  // the buffer is free for the next pass
+                            }
+                            __syncwarp();
+                        } else if (valid) {
+                            uint4 *dl = reinterpret_cast<uint4 *>(dst + c * 32), *dh = reinterpret_cast<uint4 *>(dst + 64 + c * 32);
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                dl[u] = make_uint4(pl[4 * u], pl[4 * u + 1], pl[4 * u + 2], pl[4 * u + 3]);
+                                dh[u] = make_uint4(ph[4 * u], ph[4 * u + 1], ph[4 * u + 2], ph[4 * u + 3]);
+                            }
                         }
                     }
                 }
@@ -466,7 +496,7 @@ __global__ void __launch_bounds__(TCP_THREADS, 1) k_gemm_tcp(const __grid_consta
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(&tm_empty[a])) : "memory");
         }
-        if (EPI == EPI_RESID_ADD && lane == 0) tma_store_wait_all();  // the sums are in global memory
+        if ((EPI == EPI_RESID_ADD || EPI == EPI_QKV) && lane == 0) tma_store_wait_all();  // tiles are in global memory
     }
     pdl_trigger();
     tc_fence_before();
@@ -518,12 +548,26 @@ bool make_map_h(CUtensorMap *map, const float *base, int rows, int cols) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map of q [rows, Hq * 128] bf16 as boxes of 32 columns x 32 rows (64-byte rows, 64-byte swizzle).
+bool make_map_q(CUtensorMap *map, const bf16 *base, int rows, int cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)TC_H_BOX, (cuuint32_t)TC_H_BOX};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16 *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI>
 cudaError_t run_tcp(const Launch &lc, const CUtensorMap &ma, const CUtensorMap &mb, int M, int N, int K,
                     const EpiArgs &ea, uint32_t *err) {
     CUtensorMap mh = {};
     if (EPI == EPI_RESID_ADD && !make_map_h(&mh, static_cast<const float *>(ea.out), M, N)) return cudaErrorInvalidValue;
-    const int smem = EPI == EPI_RESID_ADD ? TC_SMEM_RESID : TC_SMEM;
+    if (EPI == EPI_QKV && !make_map_q(&mh, ea.q_out, M, ea.Hq * 128)) return cudaErrorInvalidValue;
+    const int smem = EPI == EPI_RESID_ADD || EPI == EPI_QKV ? TC_SMEM_RESID : TC_SMEM;
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tcp<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int tiles = ((M + TC_BM - 1) / TC_BM) * (N / TC_BN);
@@ -568,6 +612,7 @@ cudaError_t launch_gemm_tc_qkv(const Launch &lc, const bf16 *A, int M, int K, co
                                bf16 *k_layer, bf16 *v_layer, int Hq, int Hkv, int max_ctx, float eps,
                                uint32_t *err, const float *ss_in) {
     if (!gemm_tc_supported(M, K, N) || N != (Hq + 2 * Hkv) * 128 || (ss_in && K % 128)) return cudaErrorInvalidValue;
+    if (reinterpret_cast<uintptr_t>(q_out) & 15) return cudaErrorInvalidValue;  // q leaves by TMA
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, M, K, TC_BM) || !make_map(&mb, W, N, K, TC_BN)) return cudaErrorInvalidValue;
     EpiArgs ea = {};
