@@ -375,7 +375,9 @@ int qwen3_op_mlp_decode(const float *h_dev, int32_t M, int32_t C, const float *g
                         void *stream);
 
 /* Prefill projection (tiled tensor-core GEMM), same operands and epilogues as qwen3_op_gemv;
- * N a multiple of 128, K a multiple of 32, any M >= 1.  Errors: E_INVALID, E_CUDA. */
+ * N a multiple of 128, K a multiple of 32, any M >= 1; x_dev, w_dev and out_dev 16-byte
+ * aligned (the residual of QWEN3_EPI_RESID_ADD is read and written as tiles).
+ * Errors: E_INVALID (NULL, bad size, misaligned pointer), E_CUDA. */
 int qwen3_op_gemm(const void *x_dev, int32_t M, int32_t K, const void *w_dev, int32_t N,
                   int32_t epilogue, void *out_dev, void *stream);
 

@@ -1000,6 +1000,11 @@ int qwen3_op_gemm(const void *x, int32_t M, int32_t K, const void *w, int32_t N,
         g_create_error = "qwen3_op_gemm: bad argument";
         return QWEN3_E_INVALID;
     }
+    // operands and output move by TMA / 16-byte vector accesses
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(out)) & 15) {
+        g_create_error = "qwen3_op_gemm: x, w and out must be 16-byte aligned";
+        return QWEN3_E_INVALID;
+    }
     const Launch lc = op_launch(stream);
     cudaError_t e = gemm_tc_supported(M, K, N)
                         ? launch_gemm_tc(lc, (const bf16 *)x, M, K, (const bf16 *)w, N, epi, out, nullptr)

@@ -167,6 +167,16 @@ def test_attn_decode_op_rejects_bad_arguments_before_any_launch(lib):
         assert "qwen3_op_attn_decode" in binding.qwen3_last_error(None)
 
 
+def test_gemm_op_rejects_bad_arguments_before_any_launch(lib):
+    p = 256  # any non-NULL, 256-byte aligned value: the checks return before a pointer is used
+    for args in ((None, 64, 1024, p, 1024, 1, p), (p, 0, 1024, p, 1024, 1, p), (p, 64, 1000, p, 1024, 1, p),
+                 (p, 64, 1024, p, 1000, 1, p), (p, 64, 1024, p, 1024, 3, p),
+                 (p + 8, 64, 1024, p, 1024, 0, p), (p, 64, 1024, p + 4, 1024, 2, p),
+                 (p, 64, 1024, p, 1024, 1, p + 8)):  # residual not 16-byte aligned
+        assert lib.qwen3_op_gemm(*args, None) == binding.QWEN3_E_INVALID, args
+        assert "qwen3_op_gemm" in binding.qwen3_last_error(None)
+
+
 def test_attn_decode_plan_rejects_bad_arguments(lib):
     for args in ((0, 16, 8, 10, 64), (4, 16, 3, 10, 64), (4, 16, 8, 0, 64), (4, 16, 8, 65, 64), (1025, 16, 8, 1, 8)):
         assert lib.qwen3_op_attn_decode_plan(*args) == binding.QWEN3_E_INVALID, args
