@@ -218,7 +218,7 @@ def decode_positions(wl):
 # GPU runner
 # --------------------------------------------------------------------------------------
 
-class GpuRunner:
+class DeviceRunner:
     """Holds the model and the device buffers of one replica and runs steps of the workload."""
 
     def __init__(self, wl, device, flags=0, weights=None, kv_block_tokens=0):
@@ -711,7 +711,7 @@ def run_workload(args, wl, device, flags, peaks, peak_kind, world, local_rank, w
     import torch
     from qwen3_decoder_forward_gb300 import binding
 
-    runner = GpuRunner(wl, device, flags, weights, kv_block_tokens)
+    runner = DeviceRunner(wl, device, flags, weights, kv_block_tokens)
     units, unit = units_per_step(wl)
     out = {}
     if wl.decode_steps:
